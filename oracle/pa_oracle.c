@@ -1,0 +1,409 @@
+/*
+ * Reference oracle for paged decode attention and the KV-cache append step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain, obviously-correct
+ * statement of what the GPU path computes.  Only the test suite, the smoke
+ * check and the benchmark's CPU-baseline leg may load it.  It shares no code,
+ * header, table or constant generator with the CUDA library, and it never
+ * reads a value produced by that library.
+ *
+ * Sources (four web pages on vLLM PagedAttention):
+ *   - "Optimizing Llama 3.1 405B Inference with vLLM PagedAttention",
+ *     sections "Why Standard Attention Fails at Scale" (fixed-size pages of
+ *     16 tokens, logical blocks mapped to physical pages) and "PagedAttention
+ *     Mechanics" (a page table per sequence; appending a token writes into the
+ *     sequence's last page, a fresh page only when needed; shared prefix pages).
+ *   - "vLLM PagedAttention: Memory Optimization & High-Throughput LLM Inference
+ *     Tuning", section 2 (the kernel fetches K/V by walking the block table;
+ *     only the last block of a request is partially filled; shared prompt
+ *     blocks) and section 1 (each new token attends to all cached tokens).
+ *   - "Optimizing vLLM Throughput with PagedAttention and Continuous Batching
+ *     for Llama 3" (grouped-query attention: several query heads share one KV
+ *     head).
+ *   - "vLLM PagedAttention Optimization: Complete Step-by-Step Tuning Guide",
+ *     Step 1 (KV bytes per token formula) and Step 3 (FP8 KV cache); the
+ *     E4M3 format is named in the first page, "Quantization Without Quality
+ *     Loss".
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   - cache layout [num_blocks][num_kv_heads][block_size][head_dim];
+ *   - logical token t of a sequence lives in block_tables[s][t / B] at
+ *     offset t % B;
+ *   - query head hq reads KV head hq / G with G = Hq / Hkv;
+ *   - the new token is appended before attention, so context_lens includes it;
+ *   - a negative slot means "skip"; a zero-length context yields zeros;
+ *   - FP8 uses one per-tensor scale: stored = e4m3(x / scale) rounded to
+ *     nearest-even with saturation to +-448; read back as e4m3(b) * scale.
+ *
+ * Arithmetic is fp64 except the fp8 encode, which divides in fp32 as the
+ * quantisation step is defined on fp32 values.  No blocking, no fusion, no
+ * reordering: one (sequence, query head) at a time, tokens in logical order.
+ * The outer loop over (sequence, query head) may run on several host threads
+ * (OpenMP); every output is written by exactly one thread.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* number formats                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* bfloat16 is the upper half of an IEEE binary32: widen and convert. */
+double pa_oracle_bf16_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* OCP 8-bit floating point, E4M3 flavour: 1 sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits; exponent field 0 encodes subnormals
+ * (m/8 * 2^-6); S.1111.111 is NaN; there is no infinity, so the largest
+ * finite magnitude is 1.75 * 2^8 = 448. */
+double pa_oracle_e4m3_to_double(uint8_t code)
+{
+    int sign = (code >> 7) & 1;
+    int expo = (code >> 3) & 15;
+    int mant = code & 7;
+    double mag;
+    if (expo == 15 && mant == 7)
+        return NAN;
+    if (expo == 0)
+        mag = ldexp((double)mant / 8.0, 1 - 7);
+    else
+        mag = ldexp(1.0 + (double)mant / 8.0, expo - 7);
+    return sign ? -mag : mag;
+}
+
+/* Encode a binary32 value as E4M3: round to the nearest representable value,
+ * ties to the code whose mantissa LSB is zero; magnitudes beyond the largest
+ * finite value saturate to +-448 (no NaN or infinity is produced from a
+ * finite or infinite input); NaN maps to the NaN code 0x7F.  Done by plain
+ * search over the 127 non-negative finite codes. */
+uint8_t pa_oracle_e4m3_from_float(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    int neg = signbit(x) ? 1 : 0;
+    double a = fabs((double)x);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        double v = pa_oracle_e4m3_to_double((uint8_t)c);
+        double err = fabs(v - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(best | (neg << 7));
+}
+
+/* ------------------------------------------------------------------------ */
+/* KV bytes per token (Step 1 of the tuning guide)                            */
+/* ------------------------------------------------------------------------ */
+
+/* 2 (K and V) * layers * KV heads * head_dim * bytes per element. */
+int64_t pa_oracle_kv_bytes_per_token(int64_t num_layers, int64_t num_kv_heads,
+                                     int64_t head_dim, int64_t bytes_per_elem)
+{
+    return 2 * num_layers * num_kv_heads * head_dim * bytes_per_elem;
+}
+
+/* ------------------------------------------------------------------------ */
+/* slot of the newest token                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* The token that just arrived sits at logical position ctx - 1; its slot is
+ * the physical block holding that position times B plus the offset in it.
+ * An empty sequence has no newest token: slot -1. */
+void pa_oracle_slot_mapping(const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, int num_seqs,
+                            int block_size, int32_t *slot_mapping)
+{
+    for (int s = 0; s < num_seqs; ++s) {
+        int ctx = context_lens[s];
+        if (ctx <= 0) {
+            slot_mapping[s] = -1;
+            continue;
+        }
+        int pos = ctx - 1;
+        int32_t block = block_tables[(int64_t)s * max_blocks_per_seq + pos / block_size];
+        slot_mapping[s] = block * block_size + pos % block_size;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* append                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Scatter token i's K and V rows (bf16 [T][Hkv][D]) into the cache slot
+ * slot_mapping[i].  kv_dtype 0: copy the bf16 bits.  kv_dtype 1: store
+ * e4m3(float(x) / scale).  Negative slots are skipped. */
+void pa_oracle_cache_append(const uint16_t *k, const uint16_t *v,
+                            const int32_t *slot_mapping, int num_tokens,
+                            void *k_cache, void *v_cache, int num_kv_heads,
+                            int head_dim, int block_size, int kv_dtype, float scale)
+{
+    for (int i = 0; i < num_tokens; ++i) {
+        int32_t slot = slot_mapping[i];
+        if (slot < 0)
+            continue;
+        int64_t block = slot / block_size;
+        int64_t off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            for (int d = 0; d < head_dim; ++d) {
+                int64_t src = ((int64_t)i * num_kv_heads + h) * head_dim + d;
+                int64_t dst = ((block * num_kv_heads + h) * block_size + off) * head_dim + d;
+                if (kv_dtype == 0) {
+                    ((uint16_t *)k_cache)[dst] = k[src];
+                    ((uint16_t *)v_cache)[dst] = v[src];
+                } else {
+                    float kf = (float)pa_oracle_bf16_to_double(k[src]);
+                    float vf = (float)pa_oracle_bf16_to_double(v[src]);
+                    ((uint8_t *)k_cache)[dst] = pa_oracle_e4m3_from_float(kf / scale);
+                    ((uint8_t *)v_cache)[dst] = pa_oracle_e4m3_from_float(vf / scale);
+                }
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* attention                                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Read back one cached element as a real number. */
+static double cache_value(const void *cache, int64_t index, int kv_dtype, double kv_scale)
+{
+    if (kv_dtype == 0)
+        return pa_oracle_bf16_to_double(((const uint16_t *)cache)[index]);
+    return pa_oracle_e4m3_to_double(((const uint8_t *)cache)[index]) * kv_scale;
+}
+
+/* Element index of (logical token t, KV head h, dim d) of sequence s. */
+static int64_t token_index(const int32_t *block_tables, int max_blocks_per_seq,
+                           int s, int t, int h, int d, int num_kv_heads,
+                           int head_dim, int block_size)
+{
+    int64_t block = block_tables[(int64_t)s * max_blocks_per_seq + t / block_size];
+    int64_t off = t % block_size;
+    return ((block * num_kv_heads + h) * block_size + off) * head_dim + d;
+}
+
+/* Attention of one query head over logical tokens [t_begin, t_end) of one
+ * sequence.  Writes o[d] = sum_t p_t V[t][d] with p = softmax over the range
+ * of x_t = softmax_scale * q . K[t], and returns the range's max m = max_t x_t
+ * and l = sum_t exp(x_t - m) through *m_out and *l_out.  An empty range gives
+ * o = 0, m = -inf, l = 0. */
+static void attend_range(const uint16_t *q_row, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, int max_blocks_per_seq, int s, int kvh,
+                         int t_begin, int t_end, int num_kv_heads, int head_dim, int block_size,
+                         double softmax_scale, int kv_dtype, double kv_scale,
+                         double *x, double *o, double *m_out, double *l_out)
+{
+    int n = t_end - t_begin;
+    for (int d = 0; d < head_dim; ++d)
+        o[d] = 0.0;
+    if (n <= 0) {
+        *m_out = -INFINITY;
+        *l_out = 0.0;
+        return;
+    }
+    /* scores */
+    for (int i = 0; i < n; ++i) {
+        int t = t_begin + i;
+        double dot = 0.0;
+        for (int d = 0; d < head_dim; ++d) {
+            int64_t idx = token_index(block_tables, max_blocks_per_seq, s, t, kvh, d,
+                                      num_kv_heads, head_dim, block_size);
+            dot += pa_oracle_bf16_to_double(q_row[d]) * cache_value(k_cache, idx, kv_dtype, kv_scale);
+        }
+        x[i] = softmax_scale * dot;
+    }
+    /* softmax (max-subtracted for range safety; mathematically the same) */
+    double m = x[0];
+    for (int i = 1; i < n; ++i)
+        if (x[i] > m)
+            m = x[i];
+    double l = 0.0;
+    for (int i = 0; i < n; ++i) {
+        x[i] = exp(x[i] - m);
+        l += x[i];
+    }
+    /* weighted sum of values */
+    for (int i = 0; i < n; ++i) {
+        int t = t_begin + i;
+        double p = x[i] / l;
+        for (int d = 0; d < head_dim; ++d) {
+            int64_t idx = token_index(block_tables, max_blocks_per_seq, s, t, kvh, d,
+                                      num_kv_heads, head_dim, block_size);
+            o[d] += p * cache_value(v_cache, idx, kv_dtype, kv_scale);
+        }
+    }
+    *m_out = m;
+    *l_out = l;
+}
+
+/* Single-query decode attention through the block table.
+ *   q            bf16 [S][Hq][D]
+ *   caches       [num_blocks][Hkv][B][D] of kv_dtype (0 bf16, 1 e4m3)
+ *   block_tables int32 [S][max_blocks_per_seq]
+ *   context_lens int32 [S]
+ *   out          fp64 [S][Hq][D]
+ * out[s][hq] = softmax(softmax_scale * q[s][hq] . K_s^T) V_s with K_s, V_s the
+ * first context_lens[s] logical tokens of KV head hq / (Hq / Hkv). */
+void pa_oracle_decode(const uint16_t *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, int num_seqs, int num_q_heads,
+                      int num_kv_heads, int head_dim, int block_size,
+                      double softmax_scale, int kv_dtype, double kv_scale, double *out)
+{
+    int group = num_q_heads / num_kv_heads;
+    int max_ctx = 0;
+    for (int s = 0; s < num_seqs; ++s)
+        if (context_lens[s] > max_ctx)
+            max_ctx = context_lens[s];
+#pragma omp parallel
+    {
+        double *x = (double *)malloc(sizeof(double) * (size_t)(max_ctx > 0 ? max_ctx : 1));
+#pragma omp for collapse(2) schedule(dynamic)
+        for (int s = 0; s < num_seqs; ++s) {
+            for (int hq = 0; hq < num_q_heads; ++hq) {
+                int kvh = hq / group;
+                double m, l;
+                attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,
+                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s],
+                             num_kv_heads, head_dim, block_size, softmax_scale, kv_dtype,
+                             kv_scale, x, out + ((int64_t)s * num_q_heads + hq) * head_dim, &m, &l);
+            }
+        }
+        free(x);
+    }
+}
+
+/* Decode attention for a subset of (sequence, query head) pairs, used to
+ * check sampled outputs of large workloads one by one.  pairs is int32
+ * [n_pairs][2] of (s, hq); out is fp64 [n_pairs][D]. */
+void pa_oracle_decode_pairs(const uint16_t *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, int num_q_heads,
+                            int num_kv_heads, int head_dim, int block_size,
+                            double softmax_scale, int kv_dtype, double kv_scale,
+                            const int32_t *pairs, int n_pairs, double *out)
+{
+    int group = num_q_heads / num_kv_heads;
+#pragma omp parallel for schedule(dynamic)
+    for (int i = 0; i < n_pairs; ++i) {
+        int s = pairs[2 * i], hq = pairs[2 * i + 1];
+        int n = context_lens[s];
+        double *x = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        double m, l;
+        attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,
+                     block_tables, max_blocks_per_seq, s, hq / group, 0, n, num_kv_heads,
+                     head_dim, block_size, softmax_scale, kv_dtype, kv_scale, x,
+                     out + (int64_t)i * head_dim, &m, &l);
+        free(x);
+    }
+}
+
+/* Attention restricted to context partition p = [p * P, min((p + 1) * P, ctx))
+ * of every (sequence, query head): o fp64 [S][Hq][max_partitions][D],
+ * m and l fp64 [S][Hq][max_partitions].  Partitions at or past the end of a
+ * sequence get o = 0, m = -inf, l = 0. */
+void pa_oracle_decode_partitions(const uint16_t *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *block_tables, int max_blocks_per_seq,
+                                 const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size,
+                                 double softmax_scale, int kv_dtype, double kv_scale,
+                                 int partition_size, int max_partitions,
+                                 double *o, double *m, double *l)
+{
+    int group = num_q_heads / num_kv_heads;
+#pragma omp parallel
+    {
+        double *x = (double *)malloc(sizeof(double) * (size_t)partition_size);
+#pragma omp for collapse(2) schedule(dynamic)
+        for (int s = 0; s < num_seqs; ++s) {
+            for (int hq = 0; hq < num_q_heads; ++hq) {
+                for (int p = 0; p < max_partitions; ++p) {
+                    int64_t row = ((int64_t)s * num_q_heads + hq) * max_partitions + p;
+                    int t0 = p * partition_size;
+                    int t1 = t0 + partition_size;
+                    if (t1 > context_lens[s])
+                        t1 = context_lens[s];
+                    attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache,
+                                 v_cache, block_tables, max_blocks_per_seq, s, hq / group, t0,
+                                 t1, num_kv_heads, head_dim, block_size, softmax_scale,
+                                 kv_dtype, kv_scale, x, o + row * head_dim, &m[row], &l[row]);
+                }
+            }
+        }
+        free(x);
+    }
+}
+
+/* Log-sum-exp merge of partition results.  For each (s, hq) with
+ * n = ceil(ctx / P) partitions: M = max_p m_p, w_p = l_p exp(m_p - M),
+ * out = sum_p w_p o_p / sum_p w_p.  n = 0 gives zeros.  Inputs are the
+ * partial arrays laid out as in pa_oracle_decode_partitions (fp32 here, as
+ * a caller stores them); out is fp64 [S][Hq][D]. */
+void pa_oracle_merge_partitions(const float *o, const float *m, const float *l,
+                                const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                int head_dim, int partition_size, int max_partitions,
+                                double *out)
+{
+    for (int s = 0; s < num_seqs; ++s) {
+        int ctx = context_lens[s];
+        int n = ctx > 0 ? (ctx + partition_size - 1) / partition_size : 0;
+        for (int hq = 0; hq < num_q_heads; ++hq) {
+            int64_t base = ((int64_t)s * num_q_heads + hq) * max_partitions;
+            double *dst = out + ((int64_t)s * num_q_heads + hq) * head_dim;
+            for (int d = 0; d < head_dim; ++d)
+                dst[d] = 0.0;
+            if (n == 0)
+                continue;
+            double big = -INFINITY;
+            for (int p = 0; p < n; ++p)
+                if ((double)m[base + p] > big)
+                    big = (double)m[base + p];
+            double total = 0.0;
+            for (int p = 0; p < n; ++p)
+                total += (double)l[base + p] * exp((double)m[base + p] - big);
+            for (int p = 0; p < n; ++p) {
+                double w = (double)l[base + p] * exp((double)m[base + p] - big) / total;
+                for (int d = 0; d < head_dim; ++d)
+                    dst[d] += w * (double)o[(base + p) * head_dim + d];
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* threads                                                                   */
+/* ------------------------------------------------------------------------ */
+
+void pa_oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int pa_oracle_get_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

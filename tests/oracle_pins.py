@@ -1,0 +1,277 @@
+"""Checks that pin the oracle to things other than itself.
+
+Each ``pin_*`` function takes an ``Oracle`` and raises AssertionError when the
+oracle disagrees with what the pages or the mathematics fix:
+
+* the KV-bytes formula's worked example printed in the tuning guide (golden);
+* torch's own float8_e4m3fn conversions (a library implementation of the
+  OCP E4M3 format the pages name);
+* torch ``scaled_dot_product_attention`` in float64 over the LOGICAL K/V,
+  repeated per query group (a library routine; the oracle instead walks the
+  block table of a randomly permuted pool);
+* invariants: any physical permutation gives the same result, shared prefix
+  blocks equal private copies, a one-token context returns V, identical keys
+  return the mean of V, a large softmax scale stays finite;
+* brute-force enumeration of every slot of a sequence for the slot mapping;
+* read-back of appended rows through the block table;
+* the log-sum-exp identity: merging partition results equals one softmax
+  over the union.
+
+``tests/test_oracle.py`` runs them on the oracle; ``tests/test_oracle_mutants.py``
+runs them on deliberately broken copies to show each plausible mistake trips
+at least one of them.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+import torch
+
+from paged_cases import LogicalCase, bits_to_f64
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _e4m3_torch(codes: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(codes.astype(np.uint8)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _encode_many(o, xs_bits: np.ndarray, scale: float) -> np.ndarray:
+    """Run the oracle's append over a one-element-per-token cache so the whole
+    array is encoded in one call."""
+    n = xs_bits.size
+    k = xs_bits.reshape(n, 1, 1).astype(np.uint16)
+    kc = np.zeros((n, 1, 1, 1), np.uint8)
+    vc = np.zeros_like(kc)
+    o.cache_append(k, k, np.arange(n, dtype=np.int32), kc, vc, 1, 1, scale)
+    assert np.array_equal(kc, vc)
+    return kc.reshape(n)
+
+
+def pin_kv_formula(o):
+    with open(os.path.join(GOLDEN, "kv_bytes_per_token.json")) as f:
+        g = json.load(f)
+    for c in g["cases"]:
+        b = o.kv_bytes_per_token(c["num_layers"], c["num_kv_heads"], c["head_dim"], c["bytes_per_elem"])
+        assert b == c["bytes_per_token"], b
+        assert b // 1024 == c["kib_per_token"]
+        assert b * c["context_tokens"] == c["bytes_per_sequence"]
+        assert b * c["context_tokens"] == c["gib_per_sequence"] * 2**30
+
+
+def pin_e4m3_decode(o):
+    codes = np.arange(256)
+    ref = _e4m3_torch(codes)
+    got = np.array([o.e4m3_to_double(c) for c in codes])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert sorted(np.flatnonzero(nan).tolist()) == [0x7F, 0xFF]
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0**-9
+
+
+def pin_e4m3_encode(o, exhaustive=True):
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    if not exhaustive:
+        allbits = allbits[::17]
+    x = bits_to_f64(allbits).astype(np.float32)
+    for scale in (1.0, float(np.float32(4.5) / np.float32(448.0)), 0.37):
+        got = _encode_many(o, allbits, scale)
+        with np.errstate(invalid="ignore", over="ignore"):
+            y = x / np.float32(scale)
+        isnan = np.isnan(y)
+        assert np.all((got[isnan] & 0x7F) == 0x7F)
+        big = ~isnan & (np.abs(y) > 448.0)
+        want_big = np.where(np.signbit(y[big]), 0xFE, 0x7E)
+        assert np.array_equal(got[big], want_big)
+        fine = ~isnan & ~big
+        want = torch.from_numpy(y[fine]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(got[fine], want), np.flatnonzero(got[fine] != want)[:8]
+
+
+def pin_e4m3_roundtrip(o):
+    for c in range(256):
+        if c in (0x7F, 0xFF):
+            continue
+        assert o.e4m3_from_float(o.e4m3_to_double(c)) == c, c
+
+
+def _case(ctx=(1, 5, 16, 17, 40), Hq=8, Hkv=2, D=16, seed=3, **kw):
+    return LogicalCase(ctx, Hq, Hkv, D, seed, **kw)
+
+
+def pin_attention_sdpa(o):
+    rng = np.random.default_rng(7)
+    for B, (Hq, Hkv) in ((16, (8, 2)), (4, (6, 3)), (32, (4, 4)), (8, (16, 1))):
+        c = _case(Hq=Hq, Hkv=Hkv, seed=B + Hq)
+        tables, kc, vc = c.paged(B, 40, rng)
+        out = o.decode(c.q, kc, vc, tables, np.array(c.ctx), Hkv, B, 0.3)
+        ref = c.sdpa(0.3)
+        assert np.isfinite(out).all()
+        assert np.abs(out - ref).max() < 1e-12, np.abs(out - ref).max()
+
+
+def pin_attention_fp8(o):
+    rng = np.random.default_rng(8)
+    c = _case(seed=11)
+    tables, _, _ = c.paged(16, 30, rng)
+    scale = 0.02
+    codes_k = [np.array([[[_byte(o, x, scale) for x in row] for row in h] for h in k]) for k in c.k]
+    codes_v = [np.array([[[_byte(o, x, scale) for x in row] for row in h] for h in v]) for v in c.v]
+    kc = np.full((30, c.Hkv, 16, c.D), 0x7F, np.uint8)
+    vc = np.full_like(kc, 0x7F)
+    for s, n in enumerate(c.ctx):
+        for t in range(n):
+            kc[tables[s, t // 16], :, t % 16, :] = codes_k[s][:, t, :]
+            vc[tables[s, t // 16], :, t % 16, :] = codes_v[s][:, t, :]
+    out = o.decode(c.q, kc, vc, tables, np.array(c.ctx), c.Hkv, 16, 0.25, kv_dtype=1, kv_scale=scale)
+    c.k, c.v = codes_k, codes_v
+    ref = c.sdpa(0.25, deq_k=lambda a: _e4m3_torch(a) * scale, deq_v=lambda a: _e4m3_torch(a) * scale)
+    assert np.abs(out - ref).max() < 1e-12, np.abs(out - ref).max()
+
+
+def _byte(o, bits, scale):
+    x = np.float32(bits_to_f64(np.array([bits], np.uint16))[0])
+    return o.e4m3_from_float(x / np.float32(scale))
+
+
+def pin_extreme_scores(o):
+    rng = np.random.default_rng(9)
+    c = _case(ctx=(30, 64), seed=5)
+    tables, kc, vc = c.paged(16, 12, rng)
+    out = o.decode(c.q, kc, vc, tables, np.array(c.ctx), c.Hkv, 16, 400.0)
+    ref = c.sdpa(400.0)
+    assert np.isfinite(out).all()
+    assert np.abs(out - ref).max() < 1e-9
+
+
+def pin_permutation(o):
+    c = _case(seed=13)
+    outs = []
+    for seed in (1, 2, 3):
+        tables, kc, vc = c.paged(16, 50, np.random.default_rng(seed))
+        outs.append(o.decode(c.q, kc, vc, tables, np.array(c.ctx), c.Hkv, 16, 0.2))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def pin_prefix_sharing(o):
+    def same_prefix(ks):
+        ks = [k.copy() for k in ks]
+        for k in ks[1:]:
+            k[:, :32, :] = ks[0][:, :32, :]
+        return ks
+    c = _case(ctx=(40, 33, 64), seed=17)
+    c.k = same_prefix(c.k)
+    c.v = same_prefix(c.v)
+    t_sh, k_sh, v_sh = c.paged(16, 20, np.random.default_rng(4), share_prefix_tokens=32)
+    t_pr, k_pr, v_pr = c.paged(16, 20, np.random.default_rng(5))
+    assert t_sh[0, 0] == t_sh[1, 0] == t_sh[2, 0]
+    a = o.decode(c.q, k_sh, v_sh, t_sh, np.array(c.ctx), c.Hkv, 16, 0.2)
+    b = o.decode(c.q, k_pr, v_pr, t_pr, np.array(c.ctx), c.Hkv, 16, 0.2)
+    assert np.array_equal(a, b)
+
+
+def pin_context_one(o):
+    c = _case(ctx=(1, 1, 1), seed=19)
+    tables, kc, vc = c.paged(16, 8, np.random.default_rng(6))
+    out = o.decode(c.q, kc, vc, tables, np.array(c.ctx), c.Hkv, 16, 0.7)
+    G = c.Hq // c.Hkv
+    for s in range(3):
+        for hq in range(c.Hq):
+            assert np.array_equal(out[s, hq], bits_to_f64(c.v[s][hq // G, 0]))
+
+
+def pin_identical_keys(o):
+    def same_keys(ks):
+        return [np.repeat(k[:, :1, :], k.shape[1], axis=1) for k in ks]
+    c = _case(ctx=(7, 33), seed=23, k_override=same_keys)
+    tables, kc, vc = c.paged(16, 10, np.random.default_rng(7))
+    out = o.decode(c.q, kc, vc, tables, np.array(c.ctx), c.Hkv, 16, 0.9)
+    G = c.Hq // c.Hkv
+    for s, n in enumerate(c.ctx):
+        for hq in range(c.Hq):
+            mean = bits_to_f64(c.v[s][hq // G]).mean(axis=0)
+            assert np.abs(out[s, hq] - mean).max() < 1e-12
+
+
+def pin_empty_context(o):
+    c = _case(ctx=(0, 3), seed=29)
+    tables, kc, vc = c.paged(16, 4, np.random.default_rng(8))
+    out = o.decode(c.q, kc, vc, tables, np.array(c.ctx), c.Hkv, 16, 0.5)
+    assert np.array_equal(out[0], np.zeros_like(out[0]))
+    assert np.isfinite(out[1]).all()
+
+
+def pin_slot_mapping(o):
+    rng = np.random.default_rng(10)
+    for B in (1, 4, 16, 32):
+        ctx = np.array([0, 1, B, B + 1, 3 * B - 1, 100], np.int32)
+        mb = int(max((c + B - 1) // B for c in ctx))
+        tables = np.full((len(ctx), mb), -1, np.int32)
+        pool = list(rng.permutation(1000))
+        for s, c in enumerate(ctx):
+            for j in range((c + B - 1) // B):
+                tables[s, j] = pool.pop()
+        got = o.slot_mapping(tables, ctx, B)
+        for s, c in enumerate(ctx):
+            slots = [int(b) * B + off for b in tables[s] if b >= 0 for off in range(B)][:c]
+            assert got[s] == (slots[-1] if c > 0 else -1), (B, s)
+
+
+def pin_append_readback(o):
+    rng = np.random.default_rng(11)
+    B, Hkv, D, NB = 16, 2, 8, 12
+    for kv_dtype in (0, 1):
+        ctx = np.array([5, 16, 17, 1], np.int32)
+        tables = np.full((4, 2), -1, np.int32)
+        pool = list(rng.permutation(NB))
+        for s, c in enumerate(ctx):
+            for j in range((c + B - 1) // B):
+                tables[s, j] = pool.pop()
+        slots = np.array([tables[s, (c - 1) // B] * B + (c - 1) % B for s, c in enumerate(ctx)], np.int32)
+        slots[3] = -1
+        g = torch.Generator().manual_seed(kv_dtype)
+        k = torch.randn(4, Hkv, D, generator=g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        v = torch.randn(4, Hkv, D, generator=g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        dt = np.uint16 if kv_dtype == 0 else np.uint8
+        fill = 0x7FC0 if kv_dtype == 0 else 0x7F
+        kc = np.full((NB, Hkv, B, D), fill, dt)
+        vc = np.full_like(kc, fill)
+        before_k = kc.copy()
+        o.cache_append(k, v, slots, kc, vc, B, kv_dtype, 0.01)
+        changed = np.argwhere((kc != before_k).any(axis=(1, 3)))
+        assert len(changed) == 3
+        for s in range(3):
+            b, off = divmod(int(slots[s]), B)
+            if kv_dtype == 0:
+                assert np.array_equal(kc[b, :, off, :], k[s]) and np.array_equal(vc[b, :, off, :], v[s])
+            else:
+                kd = _e4m3_torch(kc[b, :, off, :]) * 0.01
+                assert np.abs(kd - bits_to_f64(k[s])).max() <= 0.01 * 16  # within half a step at 448
+                for h in range(Hkv):
+                    for d in range(D):
+                        assert kc[b, h, off, d] == _byte(o, k[s, h, d], 0.01)
+
+
+def pin_partition_merge(o):
+    rng = np.random.default_rng(12)
+    c = _case(ctx=(1, 16, 17, 70, 0), seed=31)
+    tables, kc, vc = c.paged(16, 30, rng)
+    ctx = np.array(c.ctx)
+    full = o.decode(c.q, kc, vc, tables, ctx, c.Hkv, 16, 0.4)
+    for P in (16, 32, 48, 128):
+        n = int(np.ceil(ctx.max() / P))
+        po, pm, pl = o.decode_partitions(c.q, kc, vc, tables, ctx, c.Hkv, 16, 0.4, P, n)
+        merged = o.merge_partitions(po.astype(np.float32), pm.astype(np.float32),
+                                    pl.astype(np.float32), ctx, P)
+        assert np.abs(merged - full).max() < 1e-6, (P, np.abs(merged - full).max())
+        if P >= ctx.max():
+            assert np.array_equal(po[:, :, 0, :], full)
+
+
+ALL = [pin_kv_formula, pin_e4m3_decode, pin_e4m3_encode, pin_e4m3_roundtrip, pin_attention_sdpa,
+       pin_attention_fp8, pin_extreme_scores, pin_permutation, pin_prefix_sharing, pin_context_one,
+       pin_identical_keys, pin_empty_context, pin_slot_mapping, pin_append_readback,
+       pin_partition_merge]

@@ -1,0 +1,72 @@
+"""Each plausible mistake planted in a COPY of the oracle (compiled on the CPU
+into a temporary directory) must trip at least one pin.  This shows the pins
+constrain every part of the oracle: the gather index, the grouping, the
+softmax, the value sum, the fp8 codec, the slot formula, the append and the
+partition merge."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+from oracle import build as obuild
+
+MUTANTS = {
+    "gqa_modulo": ("int kvh = hq / group;", "int kvh = hq % num_kv_heads;"),
+    "offset_shift": ("int64_t off = t % block_size;", "int64_t off = (t + 1) % block_size;"),
+    "block_index": ("+ t / block_size];\n    int64_t off", "+ t / block_size / 2];\n    int64_t off"),
+    "scale_dropped": ("x[i] = softmax_scale * dot;", "x[i] = dot;"),
+    "no_max_subtraction": ("x[i] = exp(x[i] - m);", "x[i] = exp(x[i]);"),
+    "not_normalised": ("double p = x[i] / l;", "double p = x[i];"),
+    "values_from_keys": ("o[d] += p * cache_value(v_cache", "o[d] += p * cache_value(k_cache"),
+    "e4m3_bias": ("expo - 7);", "expo - 8);"),
+    "e4m3_subnormal": ("ldexp((double)mant / 8.0, 1 - 7)", "ldexp((double)mant / 8.0, -7)"),
+    "e4m3_ties_odd": ("(c & 1) == 0", "(c & 1) == 1"),
+    "e4m3_no_saturation_top": ("c <= 0x7E;", "c <= 0x7D;"),
+    "slot_off_by_one": ("int pos = ctx - 1;", "int pos = ctx;"),
+    "append_block_offset_swapped": ("int64_t block = slot / block_size;\n        int64_t off = slot % block_size;",
+                                    "int64_t block = slot % block_size;\n        int64_t off = slot / block_size;"),
+    "merge_drops_l": ("total += (double)l[base + p] * exp(", "total += exp("),
+    "partition_short": ("int t1 = t0 + partition_size;", "int t1 = t0 + partition_size - 1;"),
+    "last_token_dropped": ("attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s],",
+                           "attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s] - (context_lens[s] > 1),"),
+}
+
+
+_RUNNER = r"""
+import sys
+sys.path[:0] = [{tests!r}, {root!r}]
+import oracle_pins
+from oracle import Oracle
+o = Oracle(path={lib!r})
+failed = []
+for pin in oracle_pins.ALL:
+    try:
+        if pin is oracle_pins.pin_e4m3_encode:
+            pin(o, exhaustive=False)
+        else:
+            pin(o)
+    except Exception as e:
+        failed.append(pin.__name__)
+print("FAILED:" + ",".join(failed))
+"""
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(obuild.SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    mutated = tmp_path / "pa_oracle_mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = obuild.build(force=True, src=str(mutated), out=str(tmp_path / "libmutant.so"))
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = _RUNNER.format(tests=here, root=os.path.dirname(here), lib=lib)
+    # A broken gather can read or write out of bounds and kill the process:
+    # run the pins in a child and count a crash as caught.
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    if r.returncode != 0:
+        return
+    line = [ln for ln in r.stdout.splitlines() if ln.startswith("FAILED:")][-1]
+    failed = [f for f in line[len("FAILED:"):].split(",") if f]
+    assert failed, f"mutant {name} passed every pin"
