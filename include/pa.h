@@ -1,0 +1,215 @@
+/*
+ * pa.h -- C ABI of the paged decode-attention library (libpa.so), sm_103a.
+ *
+ * The library implements the decode-time hot path of PagedAttention as the
+ * four source pages describe it:
+ *   - "Optimizing Llama 3.1 405B Inference with vLLM PagedAttention",
+ *     "Why Standard Attention Fails at Scale": the KV cache is split into
+ *     fixed-size pages (16 tokens by default) mapped from logical blocks;
+ *     "PagedAttention Mechanics": a page table per sequence, a new token is
+ *     appended into the sequence's last page (a fresh page only when needed),
+ *     and sequences may point at the same physical pages (shared prefixes).
+ *   - "vLLM PagedAttention: Memory Optimization & High-Throughput LLM
+ *     Inference Tuning", section 2: the attention kernel fetches the K/V
+ *     vectors by walking the block table; only a request's last block is
+ *     partially filled.  Section 1: the new token attends to every cached one.
+ *   - "Optimizing vLLM Throughput with PagedAttention and Continuous Batching
+ *     for Llama 3": grouped-query attention, several query heads per KV head.
+ *   - "vLLM PagedAttention Optimization: Complete Step-by-Step Tuning Guide",
+ *     Step 3: an FP8 KV cache halves the bytes read; the format is E4M3
+ *     (first page, "Quantization Without Quality Loss").
+ *
+ * Conventions for every entry point
+ *   - All pointers are DEVICE pointers of the current CUDA device unless a
+ *     comment says otherwise; the caller owns every buffer.  The library
+ *     allocates no device memory, never synchronises the stream it is given,
+ *     and enqueues its kernels on `stream` (0 = the legacy default stream).
+ *   - Tensors are dense, row-major, in the shapes given below:
+ *       q            bf16  [num_seqs][num_q_heads][head_dim]
+ *       k_cache/v_cache    [num_blocks][num_kv_heads][block_size][head_dim]
+ *                          of bf16 (PA_KV_BF16) or E4M3 bytes (PA_KV_FP8_E4M3)
+ *       block_tables int32 [num_seqs][max_blocks_per_seq]; entry j of row s is
+ *                          the physical block holding logical tokens
+ *                          [j*block_size, (j+1)*block_size) of sequence s
+ *       context_lens int32 [num_seqs]; includes the token appended this step
+ *       out          bf16  [num_seqs][num_q_heads][head_dim]
+ *   - Query head hq attends with KV head hq / (num_q_heads / num_kv_heads).
+ *   - Logical token t of sequence s is slot block_tables[s][t / block_size] *
+ *     block_size + t % block_size; slot x is row x % block_size of block
+ *     x / block_size.
+ *   - Supported: head_dim 64 or 128; block_size 16 or 32; group size
+ *     num_q_heads / num_kv_heads from 1 to 16; partition_size 0 or a
+ *     positive multiple of block_size.  Other values return
+ *     PA_ERR_UNSUPPORTED before anything is launched.
+ *   - Host-side checks (null or misaligned pointers, negative sizes, shapes
+ *     out of range) return an error before anything is launched.  Pointers
+ *     must be 16-byte aligned.  A failed CUDA call returns PA_ERR_CUDA; the
+ *     message is available from pa_last_error().
+ *   - Checks that need the device data (a block id outside [0, num_blocks),
+ *     a context longer than the table, a slot outside the pool) are made in
+ *     the kernels, which skip the offending item and set a bit in the
+ *     library's device error word; read it with pa_device_errors().
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, negative or inconsistent size */
+    PA_ERR_UNSUPPORTED = 2, /* well-formed but not built: head_dim, block_size, group, dtype */
+    PA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than pa_decode_workspace_size */
+    PA_ERR_CUDA = 4         /* a CUDA call failed; see pa_last_error() */
+} pa_status;
+
+typedef enum pa_kv_dtype {
+    PA_KV_BF16 = 0,      /* cache holds bf16 */
+    PA_KV_FP8_E4M3 = 1   /* cache holds OCP E4M3 bytes; value = e4m3(byte) * kv_scale */
+} pa_kv_dtype;
+
+/* Bits of the device error word (pa_device_errors). */
+#define PA_DEVERR_BAD_BLOCK   0x1u /* a block-table entry outside [0, num_blocks): page read as zeros */
+#define PA_DEVERR_BAD_CONTEXT 0x2u /* context_lens[s] > max_blocks_per_seq * block_size: clamped */
+#define PA_DEVERR_TIMEOUT     0x4u /* a wait for a page copy exceeded its time limit; output invalid */
+#define PA_DEVERR_BAD_SLOT    0x8u /* slot_mapping entry >= num_blocks * block_size: token skipped */
+
+/*
+ * pa_slot_mapping -- slot of each sequence's newest token.
+ * Source: "PagedAttention Mechanics" (first page): the arriving token is
+ * appended at the end of the sequence's logical blocks.
+ *   slot_mapping[s] = block_tables[s][(n-1) / block_size] * block_size
+ *                     + (n-1) % block_size,   n = context_lens[s] > 0
+ *   slot_mapping[s] = -1                      n <= 0
+ * The host allocator must already have put a block in the table for
+ * position n-1 ("a fresh physical page only if needed").
+ * block_tables, context_lens: inputs as above.  slot_mapping: int32
+ * [num_seqs] output.  One kernel.
+ */
+pa_status pa_slot_mapping(const int32_t *block_tables, int max_blocks_per_seq,
+                          const int32_t *context_lens, int num_seqs, int block_size,
+                          int32_t *slot_mapping, cudaStream_t stream);
+
+/*
+ * pa_cache_append -- write each new token's K and V into its cache slot.
+ * Source: "PagedAttention Mechanics" (first page, append on token arrival);
+ * Step 3 of the tuning guide (FP8 KV cache).
+ *   k, v          bf16 [num_tokens][num_kv_heads][head_dim] (inputs)
+ *   slot_mapping  int32 [num_tokens]; a negative slot skips the token
+ *   k_cache, v_cache  written in place at row slot % block_size of block
+ *                 slot / block_size, for every KV head
+ *   kv_dtype      PA_KV_BF16: the bf16 bits are copied.
+ *                 PA_KV_FP8_E4M3: each element is stored as
+ *                 e4m3_rn_satfinite((float)x / scale) (IEEE fp32 division,
+ *                 round to nearest even, saturating to +-448).
+ *   scale         > 0 and finite for FP8; ignored for bf16.
+ * Distinct tokens must have distinct slots.  One kernel.
+ */
+pa_status pa_cache_append(const void *k, const void *v, const int32_t *slot_mapping,
+                          int num_tokens, void *k_cache, void *v_cache, int num_blocks,
+                          int num_kv_heads, int head_dim, int block_size,
+                          pa_kv_dtype kv_dtype, float scale, cudaStream_t stream);
+
+/*
+ * Number of context partitions the workspace is laid out for:
+ * ceil(max_blocks_per_seq * block_size / partition_size); 1 when
+ * partition_size == 0.
+ */
+int pa_decode_max_partitions(int max_blocks_per_seq, int block_size, int partition_size);
+
+/*
+ * Bytes of workspace pa_decode / pa_decode_partitions need (0 when
+ * partition_size == 0).  Layout, with P = pa_decode_max_partitions(...):
+ *   float o[num_seqs][num_q_heads][P][head_dim]  partition output, normalised
+ *                                                (sum_t p_t V[t] / sum_t p_t)
+ *   float m[num_seqs][num_q_heads][P]            partition max of
+ *                                                softmax_scale * q.K[t]
+ *   float l[num_seqs][num_q_heads][P]            sum_t exp(score_t - m)
+ * Only partitions p < ceil(context_lens[s] / partition_size) are written.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                int max_blocks_per_seq, int block_size, int partition_size);
+
+/*
+ * pa_decode_partitions -- single-query paged attention, per context partition.
+ * Source: section 2 of "vLLM PagedAttention: Memory Optimization ..." (the
+ * kernel walks the block table), the GQA passage of the Llama 3 page, and
+ * the FP8 KV passage of the tuning guide; the split over long contexts with
+ * a log-sum-exp merge is this library's design for 128K contexts (the pages
+ * only motivate them: 128000-token max_model_len, ~40 GB per sequence).
+ * For every sequence s, KV head h and partition p < ceil(n_s / partition_size)
+ * (n_s = context_lens[s]), and every query head hq of h's group, computes
+ * over logical tokens t in [p*partition_size, min((p+1)*partition_size, n_s)):
+ *   score_t = softmax_scale * kscale * (q[s][hq] . K[t]),
+ *   m = max_t score_t, l = sum_t exp(score_t - m),
+ *   o = sum_t exp(score_t - m) * vscale * V[t] / l
+ * and stores (o, m, l) into the workspace (layout above).  kscale = vscale =
+ * kv_scale for FP8, 1 for bf16.  partition_size must be > 0.
+ * One kernel.  For the FP8 cache the query is rounded to fp16 for the tensor
+ * core product (exact for bf16 values of magnitude in [2^-14, 65504]).
+ */
+pa_status pa_decode_partitions(const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                               pa_kv_dtype kv_dtype, float kv_scale, float softmax_scale,
+                               int partition_size, void *workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+
+/*
+ * pa_decode_reduce -- log-sum-exp merge of the partitions into the output.
+ * For each (s, hq) with n = ceil(context_lens[s] / partition_size) > 0:
+ *   M = max_p m_p,  w_p = l_p * exp(m_p - M),
+ *   out[s][hq] = bf16_rn( sum_p w_p o_p / sum_p w_p )
+ * and zeros when n = 0.  workspace as written by pa_decode_partitions (or
+ * by the caller in the documented layout) for the same max_blocks_per_seq,
+ * block_size and partition_size.  One kernel.
+ */
+pa_status pa_decode_reduce(const void *workspace, size_t workspace_bytes,
+                           const int32_t *context_lens, int num_seqs, int num_q_heads,
+                           int head_dim, int max_blocks_per_seq, int block_size,
+                           int partition_size, void *out, cudaStream_t stream);
+
+/*
+ * pa_decode -- single-query paged decode attention, bf16 output.
+ *   out[s][hq] = bf16_rn( softmax_t(softmax_scale * kscale * q[s][hq] . K[t])
+ *                         . vscale * V )  over the n_s cached tokens of KV head
+ *                hq / group; zeros when n_s = 0.
+ * partition_size == 0: one pass per (sequence, KV head); workspace unused
+ * (may be NULL).  partition_size > 0: pa_decode_partitions followed by
+ * pa_decode_reduce on the same stream (two kernels).
+ */
+pa_status pa_decode(const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *context_lens, int num_seqs, int num_q_heads,
+                    int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                    pa_kv_dtype kv_dtype, float kv_scale, float softmax_scale,
+                    int partition_size, void *workspace, size_t workspace_bytes,
+                    void *out, cudaStream_t stream);
+
+/*
+ * pa_device_errors -- read (and with clear != 0, reset) the device error
+ * word of the current device into *flags (PA_DEVERR_* bits).  This call
+ * synchronises the device.  flags is a HOST pointer.
+ */
+pa_status pa_device_errors(unsigned int *flags, int clear);
+
+/* Static description of a status code (never NULL). */
+const char *pa_status_string(pa_status status);
+
+/* Message describing the most recent failure on the calling host thread
+ * (which argument was rejected, or the CUDA error); "" if none. */
+const char *pa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

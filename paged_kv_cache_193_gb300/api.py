@@ -1,0 +1,243 @@
+"""Thin PyTorch binding of the C ABI (``include/pa.h``).
+
+Only argument marshalling lives here: tensors are checked for device, dtype
+and layout, then their device pointers, sizes and the current CUDA stream are
+passed to ``libpa.so``.  Every step of the computation runs in the library's
+kernels; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+from ._lib import PA_KV_BF16, PA_KV_FP8_E4M3
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(message)
+
+
+def _lib_handle():
+    return _lib.load()
+
+
+def _check(status: int) -> None:
+    if status != _lib.PA_OK:
+        lib = _lib_handle()
+        what = lib.pa_status_string(status).decode()
+        detail = lib.pa_last_error().decode()
+        raise PagedAttentionError(status, f"{what}: {detail}")
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtypes, ndim: int | None = None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions (got shape {tuple(t.shape)})")
+
+
+_CACHE_DTYPES = {PA_KV_BF16: (torch.bfloat16,), PA_KV_FP8_E4M3: (torch.uint8, torch.float8_e4m3fn)}
+
+
+def cache_dtype_of(cache: torch.Tensor) -> int:
+    return PA_KV_BF16 if cache.dtype == torch.bfloat16 else PA_KV_FP8_E4M3
+
+
+def slot_mapping(block_tables: torch.Tensor, context_lens: torch.Tensor, block_size: int,
+                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """int32 [S] slot of each sequence's newest token (-1 for empty ones)."""
+    _need(block_tables, "block_tables", (torch.int32,), 2)
+    _need(context_lens, "context_lens", (torch.int32,), 1)
+    S, MB = block_tables.shape
+    if out is None:
+        out = torch.empty(S, dtype=torch.int32, device=block_tables.device)
+    _need(out, "out", (torch.int32,), 1)
+    _check(_lib_handle().pa_slot_mapping(block_tables.data_ptr(), MB, context_lens.data_ptr(), S,
+                                         block_size, out.data_ptr(), _stream(stream)))
+    return out
+
+
+def cache_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                 k_cache: torch.Tensor, v_cache: torch.Tensor, scale: float = 1.0,
+                 stream=None) -> None:
+    """Write token i's K/V rows (bf16 [T, Hkv, D]) into slot slot_mapping[i]
+    of the caches ([NB, Hkv, B, D], bf16 or E4M3 bytes); in place."""
+    _need(k, "k", (torch.bfloat16,), 3)
+    _need(v, "v", (torch.bfloat16,), 3)
+    _need(slot_mapping, "slot_mapping", (torch.int32,), 1)
+    kv_dtype = cache_dtype_of(k_cache)
+    _need(k_cache, "k_cache", _CACHE_DTYPES[kv_dtype], 4)
+    _need(v_cache, "v_cache", _CACHE_DTYPES[kv_dtype], 4)
+    T, Hkv, D = k.shape
+    NB, Hkv2, B, D2 = k_cache.shape
+    if (Hkv2, D2) != (Hkv, D) or v.shape != k.shape or v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent K/V and cache shapes")
+    if slot_mapping.shape[0] != T:
+        raise ValueError("slot_mapping must have one entry per token")
+    _check(_lib_handle().pa_cache_append(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
+                                         k_cache.data_ptr(), v_cache.data_ptr(), NB, Hkv, D, B,
+                                         kv_dtype, float(scale), _stream(stream)))
+
+
+def max_partitions(max_blocks_per_seq: int, block_size: int, partition_size: int) -> int:
+    return int(_lib_handle().pa_decode_max_partitions(max_blocks_per_seq, block_size, partition_size))
+
+
+def workspace_size(num_seqs: int, num_q_heads: int, head_dim: int, max_blocks_per_seq: int,
+                   block_size: int, partition_size: int) -> int:
+    return int(_lib_handle().pa_decode_workspace_size(num_seqs, num_q_heads, head_dim,
+                                                      max_blocks_per_seq, block_size,
+                                                      partition_size))
+
+
+def alloc_workspace(q: torch.Tensor, block_tables: torch.Tensor, block_size: int,
+                    partition_size: int) -> torch.Tensor | None:
+    S, Hq, D = q.shape
+    n = workspace_size(S, Hq, D, block_tables.shape[1], block_size, partition_size)
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8, device=q.device)
+
+
+def _decode_common(q, k_cache, v_cache, block_tables, context_lens):
+    _need(q, "q", (torch.bfloat16,), 3)
+    kv_dtype = cache_dtype_of(k_cache)
+    _need(k_cache, "k_cache", _CACHE_DTYPES[kv_dtype], 4)
+    _need(v_cache, "v_cache", _CACHE_DTYPES[kv_dtype], 4)
+    _need(block_tables, "block_tables", (torch.int32,), 2)
+    _need(context_lens, "context_lens", (torch.int32,), 1)
+    S, Hq, D = q.shape
+    NB, Hkv, B, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent q / cache shapes")
+    if block_tables.shape[0] != S or context_lens.shape[0] != S:
+        raise ValueError("block_tables and context_lens need one row per sequence")
+    return kv_dtype, S, Hq, D, NB, Hkv, B
+
+
+def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+           block_tables: torch.Tensor, context_lens: torch.Tensor, softmax_scale: float | None = None,
+           kv_scale: float = 1.0, partition_size: int = 0, workspace: torch.Tensor | None = None,
+           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Paged decode attention; returns bf16 [S, Hq, D].  ``partition_size``
+    0 = one pass per (sequence, KV head); > 0 = split context + merge."""
+    kv_dtype, S, Hq, D, NB, Hkv, B = _decode_common(q, k_cache, v_cache, block_tables, context_lens)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", (torch.bfloat16,), 3)
+    if partition_size and workspace is None:
+        workspace = alloc_workspace(q, block_tables, B, partition_size)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib_handle().pa_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                   block_tables.data_ptr(), block_tables.shape[1],
+                                   context_lens.data_ptr(), S, Hq, Hkv, D, NB, B, kv_dtype,
+                                   float(kv_scale), float(softmax_scale), int(partition_size),
+                                   ws_ptr, ws_bytes, out.data_ptr(), _stream(stream)))
+    return out
+
+
+def decode_partitions(q, k_cache, v_cache, block_tables, context_lens, softmax_scale, kv_scale,
+                      partition_size, workspace, stream=None) -> None:
+    """Per-partition (o, m, l) into ``workspace`` (layout in include/pa.h)."""
+    kv_dtype, S, Hq, D, NB, Hkv, B = _decode_common(q, k_cache, v_cache, block_tables, context_lens)
+    _check(_lib_handle().pa_decode_partitions(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        block_tables.shape[1], context_lens.data_ptr(), S, Hq, Hkv, D, NB, B, kv_dtype,
+        float(kv_scale), float(softmax_scale), int(partition_size), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def decode_reduce(workspace: torch.Tensor, context_lens: torch.Tensor, num_q_heads: int,
+                  head_dim: int, max_blocks_per_seq: int, block_size: int, partition_size: int,
+                  out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Log-sum-exp merge of the workspace partitions into bf16 ``out``."""
+    _need(context_lens, "context_lens", (torch.int32,), 1)
+    _need(out, "out", (torch.bfloat16,), 3)
+    S = context_lens.shape[0]
+    _check(_lib_handle().pa_decode_reduce(workspace.data_ptr(),
+                                          workspace.numel() * workspace.element_size(),
+                                          context_lens.data_ptr(), S, num_q_heads, head_dim,
+                                          max_blocks_per_seq, block_size, partition_size,
+                                          out.data_ptr(), _stream(stream)))
+    return out
+
+
+def workspace_views(workspace: torch.Tensor, num_seqs: int, num_q_heads: int, head_dim: int,
+                    parts: int):
+    """(o, m, l) fp32 views of a workspace: [S,Hq,P,D], [S,Hq,P], [S,Hq,P]."""
+    f = workspace.view(torch.float32)
+    n = num_seqs * num_q_heads * parts
+    o = f[: n * head_dim].view(num_seqs, num_q_heads, parts, head_dim)
+    m = f[n * head_dim: n * head_dim + n].view(num_seqs, num_q_heads, parts)
+    l = f[n * head_dim + n: n * head_dim + 2 * n].view(num_seqs, num_q_heads, parts)
+    return o, m, l
+
+
+def device_errors(clear: bool = True) -> int:
+    """PA_DEVERR_* bits set by kernels since the last clear (synchronises)."""
+    flags = ctypes.c_uint(0)
+    _check(_lib_handle().pa_device_errors(ctypes.byref(flags), 1 if clear else 0))
+    return int(flags.value)
+
+
+class DecodeStep:
+    """One decode step of one attention layer over a paged cache, with every
+    buffer allocated up front: slot mapping of the newest tokens, append of
+    their K/V, partitioned attention and (when split) the merge.  Calling it
+    launches 3 or 4 kernels on the current stream and allocates nothing."""
+
+    def __init__(self, k_cache, v_cache, block_tables, context_lens, num_q_heads,
+                 softmax_scale=None, kv_scale=1.0, partition_size=0):
+        self.k_cache, self.v_cache = k_cache, v_cache
+        self.block_tables, self.context_lens = block_tables, context_lens
+        NB, self.Hkv, self.B, self.D = k_cache.shape
+        self.S = block_tables.shape[0]
+        self.Hq = num_q_heads
+        self.softmax_scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(self.D)
+        self.kv_scale = kv_scale
+        self.partition_size = partition_size
+        dev = k_cache.device
+        self.slots = torch.empty(self.S, dtype=torch.int32, device=dev)
+        self.out = torch.empty(self.S, self.Hq, self.D, dtype=torch.bfloat16, device=dev)
+        n = workspace_size(self.S, self.Hq, self.D, block_tables.shape[1], self.B, partition_size)
+        self.workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+
+    def append(self, k_new, v_new, stream=None):
+        slot_mapping(self.block_tables, self.context_lens, self.B, out=self.slots, stream=stream)
+        cache_append(k_new, v_new, self.slots, self.k_cache, self.v_cache, self.kv_scale, stream=stream)
+
+    def attend(self, q, stream=None):
+        if self.partition_size:
+            decode_partitions(q, self.k_cache, self.v_cache, self.block_tables, self.context_lens,
+                              self.softmax_scale, self.kv_scale, self.partition_size,
+                              self.workspace, stream=stream)
+            decode_reduce(self.workspace, self.context_lens, self.Hq, self.D,
+                          self.block_tables.shape[1], self.B, self.partition_size, self.out,
+                          stream=stream)
+        else:
+            decode(q, self.k_cache, self.v_cache, self.block_tables, self.context_lens,
+                   self.softmax_scale, self.kv_scale, 0, None, self.out, stream=stream)
+        return self.out
+
+    def __call__(self, q, k_new, v_new, stream=None):
+        self.append(k_new, v_new, stream)
+        return self.attend(q, stream)

@@ -1,0 +1,794 @@
+// Paged decode attention for sm_103a.
+//
+// What it computes: for each sequence s and query head hq, softmax over the
+// sequence's cached tokens of softmax_scale * q . K[t], applied to V, where
+// K/V rows are found by walking the sequence's block table ("vLLM
+// PagedAttention: Memory Optimization & High-Throughput LLM Inference
+// Tuning", section 2) and hq reads KV head hq / group (grouped-query
+// attention, "Optimizing vLLM Throughput with PagedAttention and Continuous
+// Batching for Llama 3").  Long contexts are cut into partitions whose
+// results are merged by log-sum-exp (reduce kernel in pa_small.cu).
+//
+// How (one CTA per (partition, KV head, sequence), NW warps):
+//  * Each warp owns the partition's pages j = warp, warp + NW, ... and keeps
+//    SPW of them in flight: lane 0 issues 2-D TMA tile loads of the K and V
+//    page of this KV head (one [block_size x 128 B] box per 128-byte column
+//    slab, hardware 128B/64B swizzle, L2 evict-first) completing on the
+//    stage's mbarrier; when the warp has used a stage it refills it with its
+//    page SPW further on.  Block-table entries are read 32 at a time by the
+//    warp's lanes, one chunk ahead of use.
+//  * The whole GQA group reuses each page: S^T = K Q^T is one m16n8k16
+//    tensor-core product per 16 tokens x 16 head dims with the group (padded
+//    to 8 or 16) as N, then a warp-shuffle online softmax over the tokens,
+//    and O^T += V^T P^T with the head dim as M.  bf16 pages feed ldmatrix
+//    directly (the swizzle makes it conflict-free); E4M3 pages are read with
+//    plain shared loads and widened to fp16 in registers, with the head-dim
+//    order permuted consistently on Q and K (and on the output) so every
+//    thread reads whole 16-byte or 4-byte words.
+//  * The warps' (max, sum, accumulator) triples are merged through shared
+//    memory; the CTA writes bf16 output (unsplit) or the fp32 partition
+//    result (o, m, l) to the workspace.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+struct DecodeArgs {
+    const __nv_bfloat16 *q;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    int max_blocks;      // table row length
+    int num_blocks;      // pool size
+    int num_q_heads;
+    int num_kv_heads;
+    int group;           // query heads per KV head
+    int partition_size;  // tokens per partition (the whole table when unsplit)
+    int max_partitions;  // workspace stride
+    float score_scale;   // softmax_scale * kscale * log2(e): scores in base-2 units
+    float v_scale;       // vscale
+    int split;           // 1: write (o, m, l) to the workspace; 0: write bf16 out
+    __nv_bfloat16 *out;
+    float *ws_o;
+    float *ws_m;
+    float *ws_l;
+    unsigned int *err;
+};
+
+// Give up on a page copy after this long (normal waits are microseconds).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr float kLn2 = 0.693147180559945309f;
+
+template <int D, int BS, bool FP8, int NT, int NW, int SPW>
+struct Cfg {
+    static constexpr int ELEM = FP8 ? 1 : 2;
+    static constexpr int ROWB = D * ELEM;                     // bytes of one token row of one head
+    static constexpr int SLAB = ROWB >= 128 ? 128 : ROWB;     // TMA box width in bytes = swizzle span
+    static constexpr int NSLAB = ROWB / SLAB;
+    static constexpr int PAGE = BS * ROWB;                    // one K (or V) page of one head
+    static constexpr int STAGE = 2 * PAGE;                    // K page, then V page
+    static constexpr int NSTAGE = NW * SPW;
+    static constexpr int RING = NSTAGE * STAGE;
+    static constexpr int NP = 8 * NT;                         // group rows padded to the MMA N
+    static constexpr int OSTR = D + 4;                        // epilogue row stride (floats)
+    static constexpr int EPI = (NW * NP * OSTR + 3 * NW * NP + 2 * NP) * 4;
+    static constexpr int SMEM = (RING > EPI ? RING : EPI) + 1024;  // + 1 KB for base alignment
+    static constexpr int MT = BS / 16;                        // 16-token m-tiles per page
+    static constexpr int KSTEPS = D / 16;
+    static constexpr int DT = D / 16;                         // 16-dim tiles of the output
+    static constexpr int CPT = D / 64;                        // fp8: 16-byte chunks per thread and row
+    static_assert(SLAB == 128 || SLAB == 64, "swizzle span");
+    static_assert((BS * SLAB) % 1024 == 0 || SLAB == 64, "slab alignment");
+};
+
+// Shared-memory address of byte `b` of token row `t` in a page tile laid
+// down by the TMA with the swizzle that matches the slab width: 16-byte
+// chunk c of a 128-byte row lands at c ^ (t & 7); of a 64-byte row at
+// c ^ ((t >> 1) & 3).
+template <class C, int BS>
+__device__ __forceinline__ uint32_t swz(uint32_t base, int t, int b) {
+    const int slab = b / C::SLAB;
+    const int within = b % C::SLAB;
+    const int chunk = within >> 4;
+    const int phys = C::SLAB == 128 ? (chunk ^ (t & 7)) : (chunk ^ ((t >> 1) & 3));
+    return base + slab * (BS * C::SLAB) + t * C::SLAB + (phys << 4) + (within & 15);
+}
+
+template <int D, int BS, bool FP8, int NT, int NW, int SPW>
+__global__ void __launch_bounds__(NW * 32, 2)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const DecodeArgs a) {
+    using C = Cfg<D, BS, FP8, NT, NW, SPW>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[C::NSTAGE];
+
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t ring = (raw + 1023u) & ~1023u;
+    float *epi = reinterpret_cast<float *>(smem_raw + (ring - raw));
+
+    const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = lane >> 2, c = lane & 3;
+
+    int n = a.context_lens[s];
+    const int cap = a.max_blocks * BS;
+    if (n > cap) {
+        if (tid == 0 && part == 0 && h == 0) set_device_error(a.err, PA_DEVERR_BAD_CONTEXT);
+        n = cap;
+    }
+    if (n < 0) n = 0;
+    const int t_begin = part * a.partition_size;
+    if (a.split && t_begin >= n) return;  // past this sequence's end: nothing to write
+    const int t_end = min(t_begin + a.partition_size, n);
+    const int page0 = t_begin / BS;
+    const int npages = t_end > t_begin ? (t_end - t_begin + BS - 1) / BS : 0;
+
+    if (tid == 0) {
+#pragma unroll
+        for (int i = 0; i < C::NSTAGE; ++i) mbar_init(smem_addr(&bars[i]), 1);
+        fence_barrier_init();
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
+    __syncthreads();
+
+    // ---- this warp's pages and their block-table entries -----------------
+    const int my_pages = npages > warp ? (npages - warp + NW - 1) / NW : 0;
+    const int32_t *bt = a.block_tables + static_cast<int64_t>(s) * a.max_blocks + page0 + warp;
+    int ent_cur = lane < my_pages ? bt[lane * NW] : -1;
+    int ent_next = 32 + lane < my_pages ? bt[(32 + lane) * NW] : -1;
+    int chunk_cur = 0;
+    const uint64_t policy = l2_evict_first_policy();
+    const int rows_total = a.num_blocks * a.num_kv_heads * BS;
+
+    // Entry of the warp's k-th page; called by all lanes with k = 0, 1, 2, ...
+    auto entry = [&](int k) -> int {
+        const int ck = k >> 5;
+        if (ck != chunk_cur) {
+            ent_cur = ent_next;
+            chunk_cur = ck;
+            const int kk = (ck + 1) * 32 + lane;
+            ent_next = kk < my_pages ? bt[kk * NW] : -1;
+        }
+        return __shfl_sync(0xffffffffu, ent_cur, k & 31);
+    };
+    // Lane 0: start the copies of the warp's k-th page (physical block blk).
+    auto issue = [&](int k, int blk) {
+        const int st = warp * SPW + k % SPW;
+        const uint32_t bar = smem_addr(&bars[st]);
+        const uint32_t kdst = ring + st * C::STAGE;
+        const uint32_t vdst = kdst + C::PAGE;
+        int y;
+        if (blk < 0 || blk >= a.num_blocks) {
+            set_device_error(a.err, PA_DEVERR_BAD_BLOCK);
+            y = rows_total;  // wholly outside the tensor: the TMA fills zeros
+        } else {
+            y = (blk * a.num_kv_heads + h) * BS;
+        }
+        mbar_arrive_expect_tx(bar, C::STAGE);
+#pragma unroll
+        for (int sl = 0; sl < C::NSLAB; ++sl) {
+            tma_load_2d(kdst + sl * (BS * C::SLAB), &tmK, sl * (C::SLAB / C::ELEM), y, bar, policy);
+            tma_load_2d(vdst + sl * (BS * C::SLAB), &tmV, sl * (C::SLAB / C::ELEM), y, bar, policy);
+        }
+    };
+
+    const int prolog = my_pages < SPW ? my_pages : SPW;
+    for (int k = 0; k < prolog; ++k) {
+        const int blk = entry(k);
+        if (lane == 0) issue(k, blk);
+    }
+
+    // ---- query fragments (B operand of S^T = K Q^T), resident in registers
+    uint32_t qf[C::KSTEPS][NT][2];
+    {
+        const __nv_bfloat16 *qh = a.q + (static_cast<int64_t>(s) * a.num_q_heads + h * a.group) * D;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int g = nt * 8 + r;
+            const bool live = g < a.group;
+            const __nv_bfloat16 *qg = qh + g * D;
+#pragma unroll
+            for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                if constexpr (!FP8) {
+                    // logical k = 2c, 2c+1 and 2c+8, 2c+9 of this 16-dim step
+                    qf[kk][nt][0] = live ? *reinterpret_cast<const uint32_t *>(qg + kk * 16 + 2 * c) : 0u;
+                    qf[kk][nt][1] = live ? *reinterpret_cast<const uint32_t *>(qg + kk * 16 + 8 + 2 * c) : 0u;
+                } else {
+                    // permuted order: this thread's dims are c*16*CPT + 4*kk + {0,1,2,3}
+                    uint2 w = live ? *reinterpret_cast<const uint2 *>(qg + c * 16 * C::CPT + 4 * kk)
+                                   : make_uint2(0u, 0u);
+                    float2 f0 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w.x));
+                    float2 f1 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w.y));
+                    qf[kk][nt][0] = pack2<true>(f0.x, f0.y);
+                    qf[kk][nt][1] = pack2<true>(f1.x, f1.y);
+                }
+            }
+        }
+    }
+
+    float o[C::DT][NT][4];
+#pragma unroll
+    for (int dt = 0; dt < C::DT; ++dt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[dt][nt][e] = 0.f;
+    float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        m_run[nt][0] = m_run[nt][1] = -INFINITY;
+        l_run[nt][0] = l_run[nt][1] = 0.f;
+    }
+
+    // ---- main loop over this warp's pages ---------------------------------
+    bool ok = true;
+    int k_fail = 0;
+    for (int k = 0; k < my_pages; ++k) {
+        const int st = warp * SPW + k % SPW;
+        if (!mbar_wait_bounded(smem_addr(&bars[st]), (k / SPW) & 1, kWaitLimitNs)) {
+            ok = false;
+            k_fail = k;
+            break;
+        }
+        const uint32_t kbase = ring + st * C::STAGE;
+        const uint32_t vbase = kbase + C::PAGE;
+        const int tok0 = (page0 + warp + k * NW) * BS;
+        const int valid = min(BS, t_end - tok0);
+
+        if (valid < BS) {
+            // Rows past the context hold whatever the pool held (never read
+            // as tokens): zero the V rows so 0-probability x garbage is 0.
+            constexpr int CH = C::NSLAB * (C::SLAB / 16);
+            for (int i = lane; i < (BS - valid) * CH; i += 32) {
+                const int row = valid + i / CH;
+                const int rem = i % CH;
+                sts128_zero(vbase + (rem / (C::SLAB / 16)) * (BS * C::SLAB) + row * C::SLAB +
+                            (rem % (C::SLAB / 16)) * 16);
+            }
+            __syncwarp();
+        }
+
+        // S^T[t][g] for the page's tokens
+        float sc[C::MT][NT][4];
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
+
+        if constexpr (!FP8) {
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                const int t = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(swz<C, BS>(kbase, t, (kk * 16 + (lane >> 4) * 8) * 2), a0, a1, a2, a3);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma16816<false>(sc[mt][nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                const int t0 = mt * 16 + r, t1 = t0 + 8;
+                uint4 ra[C::CPT], rb[C::CPT];
+#pragma unroll
+                for (int j = 0; j < C::CPT; ++j) {
+                    ra[j] = lds128(swz<C, BS>(kbase, t0, (c * C::CPT + j) * 16));
+                    rb[j] = lds128(swz<C, BS>(kbase, t1, (c * C::CPT + j) * 16));
+                }
+#pragma unroll
+                for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                    const uint4 &A = ra[kk / 4];
+                    const uint4 &B = rb[kk / 4];
+                    const uint32_t wa = (kk % 4 == 0) ? A.x : (kk % 4 == 1) ? A.y : (kk % 4 == 2) ? A.z : A.w;
+                    const uint32_t wb = (kk % 4 == 0) ? B.x : (kk % 4 == 1) ? B.y : (kk % 4 == 2) ? B.z : B.w;
+                    const uint32_t a0 = e4m3x2_to_f16x2(wa & 0xFFFFu);
+                    const uint32_t a1 = e4m3x2_to_f16x2(wb & 0xFFFFu);
+                    const uint32_t a2 = e4m3x2_to_f16x2(wa >> 16);
+                    const uint32_t a3 = e4m3x2_to_f16x2(wb >> 16);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma16816<true>(sc[mt][nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
+                }
+            }
+        }
+
+        // online softmax over the page's tokens, per group column
+        uint32_t pb[C::MT][NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+                    for (int hi = 0; hi < 2; ++hi) {
+                        const int row = mt * 16 + r + hi * 8;
+                        float x = sc[mt][nt][hi * 2 + j] * a.score_scale;
+                        x = row < valid ? x : -INFINITY;
+                        sc[mt][nt][hi * 2 + j] = x;
+                        mx = fmaxf(mx, x);
+                    }
+                }
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float m_new = fmaxf(m_run[nt][j], mx);
+                const float alpha = fast_exp2(m_run[nt][j] - m_new);
+                m_run[nt][j] = m_new;
+                float sum = 0.f;
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+                    for (int hi = 0; hi < 2; ++hi) {
+                        const float pr = fast_exp2(sc[mt][nt][hi * 2 + j] - m_new);
+                        sc[mt][nt][hi * 2 + j] = pr;
+                        sum += pr;
+                    }
+                }
+                l_run[nt][j] = l_run[nt][j] * alpha + sum;
+#pragma unroll
+                for (int dt = 0; dt < C::DT; ++dt) {
+                    o[dt][nt][j] *= alpha;
+                    o[dt][nt][j + 2] *= alpha;
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                pb[mt][nt][0] = movmatrix_trans(pack2<FP8>(sc[mt][nt][0], sc[mt][nt][1]));
+                pb[mt][nt][1] = movmatrix_trans(pack2<FP8>(sc[mt][nt][2], sc[mt][nt][3]));
+            }
+        }
+
+        // O^T += V^T P^T
+        if constexpr (!FP8) {
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                const int t = mt * 16 + (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+                for (int dt = 0; dt < C::DT; ++dt) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_trans(swz<C, BS>(vbase, t, (dt * 16 + ((lane >> 3) & 1) * 8) * 2), a0, a1,
+                                  a2, a3);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma16816<false>(o[dt][nt], a0, a1, a2, a3, pb[mt][nt][0], pb[mt][nt][1]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                const int tb = mt * 16 + 2 * c;
+#pragma unroll
+                for (int gi = 0; gi < D / 32; ++gi) {
+                    const int b = gi * 32 + 4 * r;
+                    const uint32_t w0 = lds32(swz<C, BS>(vbase, tb, b));
+                    const uint32_t w1 = lds32(swz<C, BS>(vbase, tb + 1, b));
+                    const uint32_t w2 = lds32(swz<C, BS>(vbase, tb + 8, b));
+                    const uint32_t w3 = lds32(swz<C, BS>(vbase, tb + 9, b));
+#pragma unroll
+                    for (int mu = 0; mu < 2; ++mu) {
+                        const uint32_t sel = mu ? 0x7362u : 0x5140u;
+                        const uint32_t lo = __byte_perm(w0, w1, sel);
+                        const uint32_t hi = __byte_perm(w2, w3, sel);
+                        const uint32_t a0 = e4m3x2_to_f16x2(lo & 0xFFFFu);
+                        const uint32_t a1 = e4m3x2_to_f16x2(lo >> 16);
+                        const uint32_t a2 = e4m3x2_to_f16x2(hi & 0xFFFFu);
+                        const uint32_t a3 = e4m3x2_to_f16x2(hi >> 16);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma16816<true>(o[gi * 2 + mu][nt], a0, a1, a2, a3, pb[mt][nt][0],
+                                           pb[mt][nt][1]);
+                    }
+                }
+            }
+        }
+
+        // hand the stage back to the TMA: refill with the page SPW ahead
+        __syncwarp();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (k + SPW < my_pages) {
+            const int blk = entry(k + SPW);
+            if (lane == 0) issue(k + SPW, blk);
+        }
+    }
+    if (!ok) {
+        // A copy never arrived: flag it, wait (bounded) for the copies still
+        // in flight into this warp's stages, and fall through with zeros.
+        if (lane == 0) set_device_error(a.err, PA_DEVERR_TIMEOUT);
+        const int issued = min(my_pages, k_fail + SPW);
+        for (int k = k_fail; k < issued; ++k)
+            mbar_wait_bounded(smem_addr(&bars[warp * SPW + k % SPW]), (k / SPW) & 1, kWaitLimitNs);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            m_run[nt][0] = m_run[nt][1] = -INFINITY;
+            l_run[nt][0] = l_run[nt][1] = 0.f;
+        }
+    }
+
+    // ---- merge the warps ----------------------------------------------------
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float l = l_run[nt][j];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            l_run[nt][j] = l;
+        }
+    __syncthreads();  // every warp is done with the page ring
+    float *osm = epi;                               // [NW][NP][OSTR]
+    float *msm = osm + NW * C::NP * C::OSTR;        // [NW][NP]
+    float *lsm = msm + NW * C::NP;                  // [NW][NP]
+    float *wsm = lsm + NW * C::NP;                  // [NW][NP]
+    float *fin = wsm + NW * C::NP;                  // [2][NP]: M, L
+#pragma unroll
+    for (int dt = 0; dt < C::DT; ++dt) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int g = nt * 8 + 2 * c + (e & 1);
+                int d;
+                if constexpr (!FP8)
+                    d = dt * 16 + r + (e >> 1) * 8;
+                else
+                    d = (dt >> 1) * 32 + 4 * r + 2 * (dt & 1) + (e >> 1);
+                osm[(warp * C::NP + g) * C::OSTR + d] = o[dt][nt][e];
+            }
+        }
+    }
+    if (r == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int g = nt * 8 + 2 * c + j;
+                msm[warp * C::NP + g] = m_run[nt][j];
+                lsm[warp * C::NP + g] = l_run[nt][j];
+            }
+    }
+    __syncthreads();
+    if (tid < C::NP) {
+        const int g = tid;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, msm[w * C::NP + g]);
+        float L = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) L += lsm[w * C::NP + g] * fast_exp2(msm[w * C::NP + g] - M);
+        }
+        const float inv = L > 0.f ? a.v_scale / L : 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+            wsm[w * C::NP + g] = L > 0.f ? fast_exp2(msm[w * C::NP + g] - M) * inv : 0.f;
+        fin[g] = M;
+        fin[C::NP + g] = L;
+    }
+    __syncthreads();
+
+    const int64_t row0 = static_cast<int64_t>(s) * a.num_q_heads + h * a.group;
+    for (int i = tid; i < a.group * (D / 2); i += NW * 32) {
+        const int g = i / (D / 2);
+        const int d = (i % (D / 2)) * 2;
+        float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float wt = wsm[w * C::NP + g];
+            const float *src = osm + (w * C::NP + g) * C::OSTR + d;
+            v0 += wt * src[0];
+            v1 += wt * src[1];
+        }
+        if (!a.split) {
+            *reinterpret_cast<__nv_bfloat162 *>(a.out + (row0 + g) * D + d) = __floats2bfloat162_rn(v0, v1);
+        } else {
+            *reinterpret_cast<float2 *>(a.ws_o + ((row0 + g) * a.max_partitions + part) * D + d) =
+                make_float2(v0, v1);
+        }
+    }
+    if (a.split && tid < a.group) {
+        const int64_t idx = (row0 + tid) * a.max_partitions + part;
+        a.ws_m[idx] = fin[tid] * kLn2;  // natural-log units
+        a.ws_l[idx] = fin[C::NP + tid];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// Tensor map over a cache viewed as [num_blocks * num_kv_heads * block_size
+// rows][head_dim], one box = [block_size rows][min(row bytes, 128) bytes].
+static pa_status make_map(CUtensorMap *map, const void *cache, bool fp8, int head_dim,
+                          int64_t rows, int block_size) {
+    auto fn = encode_fn();
+    if (!fn) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const int elem = fp8 ? 1 : 2;
+    const int row_bytes = head_dim * elem;
+    const int slab = row_bytes >= 128 ? 128 : row_bytes;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(slab / elem), static_cast<cuuint32_t>(block_size)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult res = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                      const_cast<void *>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      slab == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (res != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(res));
+    return PA_OK;
+}
+
+constexpr int kWarps = 4;
+constexpr int kStagesPerWarp = 2;
+
+template <int D, int BS, bool FP8, int NT>
+static pa_status launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
+                               dim3 grid, cudaStream_t stream) {
+    using C = Cfg<D, BS, FP8, NT, kWarps, kStagesPerWarp>;
+    auto kern = decode_kernel<D, BS, FP8, NT, kWarps, kStagesPerWarp>;
+    pa_status st = cuda_check(
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM),
+        "cudaFuncSetAttribute(decode)");
+    if (st != PA_OK) return st;
+    kern<<<grid, kWarps * 32, C::SMEM, stream>>>(tk, tv, a);
+    return cuda_check(cudaGetLastError(), "decode launch");
+}
+
+template <int D, int BS, bool FP8>
+static pa_status launch_nt(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
+                           dim3 grid, cudaStream_t stream) {
+    if (a.group <= 8) return launch_decode<D, BS, FP8, 1>(tk, tv, a, grid, stream);
+    return launch_decode<D, BS, FP8, 2>(tk, tv, a, grid, stream);
+}
+
+template <int D, int BS>
+static pa_status launch_dtype(bool fp8, const CUtensorMap &tk, const CUtensorMap &tv,
+                              const DecodeArgs &a, dim3 grid, cudaStream_t stream) {
+    if (fp8) return launch_nt<D, BS, true>(tk, tv, a, grid, stream);
+    return launch_nt<D, BS, false>(tk, tv, a, grid, stream);
+}
+
+struct DecodeShape {
+    int num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks;
+    int partition_size;
+    pa_kv_dtype kv_dtype;
+};
+
+static pa_status check_shape(const DecodeShape &sh, float kv_scale, float softmax_scale) {
+    if (sh.num_seqs < 0 || sh.num_q_heads <= 0 || sh.num_kv_heads <= 0 || sh.num_blocks <= 0 ||
+        sh.max_blocks <= 0 || sh.partition_size < 0)
+        return fail(PA_ERR_INVALID_ARG,
+                    "bad size (num_seqs=%d, num_q_heads=%d, num_kv_heads=%d, num_blocks=%d, "
+                    "max_blocks_per_seq=%d, partition_size=%d)",
+                    sh.num_seqs, sh.num_q_heads, sh.num_kv_heads, sh.num_blocks, sh.max_blocks,
+                    sh.partition_size);
+    if (sh.num_q_heads % sh.num_kv_heads != 0)
+        return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d",
+                    sh.num_q_heads, sh.num_kv_heads);
+    if (sh.num_q_heads / sh.num_kv_heads > 16)
+        return fail(PA_ERR_UNSUPPORTED, "query group of %d heads (supported: 1..16)",
+                    sh.num_q_heads / sh.num_kv_heads);
+    if (sh.head_dim != 64 && sh.head_dim != 128)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", sh.head_dim);
+    if (sh.block_size != 16 && sh.block_size != 32)
+        return fail(PA_ERR_UNSUPPORTED, "block_size %d (supported: 16, 32)", sh.block_size);
+    if (sh.kv_dtype != PA_KV_BF16 && sh.kv_dtype != PA_KV_FP8_E4M3)
+        return fail(PA_ERR_UNSUPPORTED, "kv_dtype %d", static_cast<int>(sh.kv_dtype));
+    if (sh.partition_size % sh.block_size != 0)
+        return fail(PA_ERR_UNSUPPORTED, "partition_size %d is not a multiple of block_size %d",
+                    sh.partition_size, sh.block_size);
+    if (static_cast<int64_t>(sh.num_blocks) * sh.num_kv_heads * sh.block_size > 0x7fffffffLL)
+        return fail(PA_ERR_UNSUPPORTED, "pool of %d blocks x %d heads x %d rows exceeds 2^31 rows",
+                    sh.num_blocks, sh.num_kv_heads, sh.block_size);
+    if (static_cast<int64_t>(sh.max_blocks) * sh.block_size > 0x7fffffffLL)
+        return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq * block_size exceeds 2^31");
+    if (sh.num_seqs > 65535 || sh.num_kv_heads > 65535)
+        return fail(PA_ERR_UNSUPPORTED, "more than 65535 sequences or KV heads");
+    if (!isfinite(softmax_scale)) return fail(PA_ERR_INVALID_ARG, "softmax_scale is not finite");
+    if (sh.kv_dtype == PA_KV_FP8_E4M3 && !(kv_scale > 0.f && isfinite(kv_scale)))
+        return fail(PA_ERR_INVALID_ARG, "fp8 kv_scale must be positive and finite");
+    return PA_OK;
+}
+
+static int64_t max_partitions_of(int max_blocks, int block_size, int partition_size) {
+    if (partition_size <= 0) return 1;
+    int64_t tokens = static_cast<int64_t>(max_blocks) * block_size;
+    return (tokens + partition_size - 1) / partition_size;
+}
+
+static size_t workspace_bytes_of(int num_seqs, int num_q_heads, int head_dim, int64_t parts) {
+    return static_cast<size_t>(num_seqs) * num_q_heads * parts * (head_dim + 2) * sizeof(float);
+}
+
+// Launch the per-partition (split) or whole-context (unsplit) kernel.
+static pa_status run_decode(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, const int32_t *context_lens,
+                            const DecodeShape &sh, float kv_scale, float softmax_scale,
+                            void *workspace, void *out, cudaStream_t stream) {
+    const bool split = sh.partition_size > 0;
+    const int64_t parts = max_partitions_of(sh.max_blocks, sh.block_size, sh.partition_size);
+    const bool fp8 = sh.kv_dtype == PA_KV_FP8_E4M3;
+    const int64_t rows = static_cast<int64_t>(sh.num_blocks) * sh.num_kv_heads * sh.block_size;
+    CUtensorMap tk, tv;
+    pa_status st = make_map(&tk, k_cache, fp8, sh.head_dim, rows, sh.block_size);
+    if (st != PA_OK) return st;
+    st = make_map(&tv, v_cache, fp8, sh.head_dim, rows, sh.block_size);
+    if (st != PA_OK) return st;
+    unsigned int *err = device_error_word();
+    if (!err) return fail(PA_ERR_CUDA, "cannot resolve the device error word");
+
+    DecodeArgs a;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.max_blocks = sh.max_blocks;
+    a.num_blocks = sh.num_blocks;
+    a.num_q_heads = sh.num_q_heads;
+    a.num_kv_heads = sh.num_kv_heads;
+    a.group = sh.num_q_heads / sh.num_kv_heads;
+    a.partition_size = split ? sh.partition_size : sh.max_blocks * sh.block_size;
+    a.max_partitions = static_cast<int>(parts);
+    const float kscale = fp8 ? kv_scale : 1.f;
+    a.score_scale = softmax_scale * kscale * 1.4426950408889634f;
+    a.v_scale = fp8 ? kv_scale : 1.f;
+    a.split = split ? 1 : 0;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.ws_o = static_cast<float *>(workspace);
+    const int64_t wrows = static_cast<int64_t>(sh.num_seqs) * sh.num_q_heads;
+    a.ws_m = split ? a.ws_o + wrows * parts * sh.head_dim : nullptr;
+    a.ws_l = split ? a.ws_m + wrows * parts : nullptr;
+    a.err = err;
+
+    if (parts > 0x7fffffffLL) return fail(PA_ERR_UNSUPPORTED, "too many partitions");
+    dim3 grid(static_cast<unsigned>(split ? parts : 1), sh.num_kv_heads, sh.num_seqs);
+    if (sh.head_dim == 128) {
+        if (sh.block_size == 16) return launch_dtype<128, 16>(fp8, tk, tv, a, grid, stream);
+        return launch_dtype<128, 32>(fp8, tk, tv, a, grid, stream);
+    }
+    if (sh.block_size == 16) return launch_dtype<64, 16>(fp8, tk, tv, a, grid, stream);
+    return launch_dtype<64, 32>(fp8, tk, tv, a, grid, stream);
+}
+
+static pa_status check_pointers(const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *block_tables, const int32_t *context_lens) {
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return fail(PA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARG, "q, k_cache and v_cache must be 16-byte aligned");
+    return PA_OK;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_decode_max_partitions(int max_blocks_per_seq, int block_size, int partition_size) {
+    if (max_blocks_per_seq <= 0 || block_size <= 0) return 0;
+    int64_t p = max_partitions_of(max_blocks_per_seq, block_size, partition_size);
+    return p > 0x7fffffffLL ? -1 : static_cast<int>(p);
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                int max_blocks_per_seq, int block_size, int partition_size) {
+    if (partition_size <= 0 || num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 ||
+        max_blocks_per_seq <= 0 || block_size <= 0)
+        return 0;
+    return workspace_bytes_of(num_seqs, num_q_heads, head_dim,
+                              max_partitions_of(max_blocks_per_seq, block_size, partition_size));
+}
+
+pa_status pa_decode_partitions(const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                               pa_kv_dtype kv_dtype, float kv_scale, float softmax_scale,
+                               int partition_size, void *workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+    clear_error();
+    DecodeShape sh{num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                   max_blocks_per_seq, partition_size, kv_dtype};
+    pa_status st = check_shape(sh, kv_scale, softmax_scale);
+    if (st != PA_OK) return st;
+    if (partition_size <= 0)
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_partitions needs partition_size > 0");
+    if (num_seqs == 0) return PA_OK;
+    st = check_pointers(q, k_cache, v_cache, block_tables, context_lens);
+    if (st != PA_OK) return st;
+    size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_blocks_per_seq,
+                                           block_size, partition_size);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need)
+        return fail(PA_ERR_WORKSPACE, "workspace %p of %zu bytes (need %zu, 16-byte aligned)",
+                    workspace, workspace_bytes, need);
+    return run_decode(q, k_cache, v_cache, block_tables, context_lens, sh, kv_scale,
+                      softmax_scale, workspace, nullptr, stream);
+}
+
+pa_status pa_decode_reduce(const void *workspace, size_t workspace_bytes,
+                           const int32_t *context_lens, int num_seqs, int num_q_heads,
+                           int head_dim, int max_blocks_per_seq, int block_size,
+                           int partition_size, void *out, cudaStream_t stream) {
+    clear_error();
+    if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 ||
+        partition_size <= 0)
+        return fail(PA_ERR_INVALID_ARG, "bad size (num_seqs=%d, num_q_heads=%d, max_blocks_per_seq=%d, "
+                    "block_size=%d, partition_size=%d)", num_seqs, num_q_heads, max_blocks_per_seq,
+                    block_size, partition_size);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+    if (num_seqs > 65535 || num_q_heads > 0x7fffffff)
+        return fail(PA_ERR_UNSUPPORTED, "more than 65535 sequences");
+    if (num_seqs == 0) return PA_OK;
+    if (!context_lens || !out) return fail(PA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(out)) return fail(PA_ERR_INVALID_ARG, "out must be 16-byte aligned");
+    int64_t parts = max_partitions_of(max_blocks_per_seq, block_size, partition_size);
+    if (parts * 4 > 200 * 1024)
+        return fail(PA_ERR_UNSUPPORTED, "%lld partitions exceed the merge kernel's shared memory",
+                    static_cast<long long>(parts));
+    size_t need = workspace_bytes_of(num_seqs, num_q_heads, head_dim, parts);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need)
+        return fail(PA_ERR_WORKSPACE, "workspace %p of %zu bytes (need %zu, 16-byte aligned)",
+                    workspace, workspace_bytes, need);
+    return launch_reduce(workspace, context_lens, num_seqs, num_q_heads, head_dim, partition_size,
+                         static_cast<int>(parts), out, stream);
+}
+
+pa_status pa_decode(const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *context_lens, int num_seqs, int num_q_heads,
+                    int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                    pa_kv_dtype kv_dtype, float kv_scale, float softmax_scale,
+                    int partition_size, void *workspace, size_t workspace_bytes,
+                    void *out, cudaStream_t stream) {
+    clear_error();
+    DecodeShape sh{num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                   max_blocks_per_seq, partition_size, kv_dtype};
+    pa_status st = check_shape(sh, kv_scale, softmax_scale);
+    if (st != PA_OK) return st;
+    if (num_seqs == 0) return PA_OK;
+    st = check_pointers(q, k_cache, v_cache, block_tables, context_lens);
+    if (st != PA_OK) return st;
+    if (!out || !aligned16(out)) return fail(PA_ERR_INVALID_ARG, "out must be non-null and 16-byte aligned");
+    if (partition_size == 0)
+        return run_decode(q, k_cache, v_cache, block_tables, context_lens, sh, kv_scale,
+                          softmax_scale, nullptr, out, stream);
+    int64_t parts = max_partitions_of(max_blocks_per_seq, block_size, partition_size);
+    if (parts * 4 > 200 * 1024)
+        return fail(PA_ERR_UNSUPPORTED, "%lld partitions exceed the merge kernel's shared memory",
+                    static_cast<long long>(parts));
+    size_t need = workspace_bytes_of(num_seqs, num_q_heads, head_dim, parts);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need)
+        return fail(PA_ERR_WORKSPACE, "workspace %p of %zu bytes (need %zu, 16-byte aligned)",
+                    workspace, workspace_bytes, need);
+    st = run_decode(q, k_cache, v_cache, block_tables, context_lens, sh, kv_scale, softmax_scale,
+                    workspace, nullptr, stream);
+    if (st != PA_OK) return st;
+    return launch_reduce(workspace, context_lens, num_seqs, num_q_heads, head_dim, partition_size,
+                         static_cast<int>(parts), out, stream);
+}
+
+}  // extern "C"
