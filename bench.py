@@ -69,6 +69,8 @@ def parse():
     ap.add_argument("--num-seqs", type=int, default=None, help="shrink the workload (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--min-warmup-seconds", type=float, default=1.0,
+                    help="keep warming up at least this long (clocks settle, sampler fills)")
     ap.add_argument("--cpu-seconds", type=float, default=8.0,
                     help="wall-time budget of the oracle sample")
     return ap.parse_args()
@@ -338,7 +340,7 @@ def run_ours(args):
     api.device_errors(clear=True)
     t_w = time.time()
     done = 0
-    while done < args.warmup or time.time() - t_w < 1.0:
+    while done < args.warmup or time.time() - t_w < args.min_warmup_seconds:
         step(wl.q, wl.k_new, wl.v_new)
         done += 1
         if done % 50 == 0:
