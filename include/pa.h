@@ -195,6 +195,36 @@ pa_status pa_decode(const void *q, const void *k_cache, const void *v_cache,
                     void *out, cudaStream_t stream);
 
 /*
+ * pa_decode_static_workspace -- pa_decode with partition_size > 0, without
+ * the caller's workspace.
+ * The source pages have no counterpart to this entry point.  It exists for
+ * callers that cannot allocate device memory at the time they run attention
+ * (device memory owned by another framework's pool, hosts that forbid
+ * allocation after start-up, paths where the device-wide synchronisation of
+ * cudaMalloc/cudaFree is not acceptable).  The split path's scratch lives in
+ * a fixed array of PA_STATIC_WORKSPACE_BYTES inside the library, which every
+ * GPU holds from the moment the library's module is loaded on it until the
+ * process exits.  The call allocates nothing.
+ *   Arguments, layouts and results: as pa_decode; partition_size must be
+ *   > 0.  A call whose scratch (pa_decode_workspace_size) would exceed
+ *   PA_STATIC_WORKSPACE_BYTES returns PA_ERR_WORKSPACE before launching.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before capturing any stream.
+ *   All calls share the one array and nothing in it needs to start at zero;
+ *   calls that can overlap on the GPU (other streams, other host threads)
+ *   race on it and must be serialised by the caller.  Two kernels.
+ */
+#define PA_STATIC_WORKSPACE_BYTES (32u << 20)
+pa_status pa_decode_static_workspace(const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *block_tables, int max_blocks_per_seq,
+                                     const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                     int num_kv_heads, int head_dim, int num_blocks,
+                                     int block_size, pa_kv_dtype kv_dtype, float kv_scale,
+                                     float softmax_scale, int partition_size, void *out,
+                                     cudaStream_t stream);
+
+/*
  * pa_device_errors -- read (and with clear != 0, reset) the device error
  * word of the current device into *flags (PA_DEVERR_* bits).  This call
  * synchronises the device.  flags is a HOST pointer.

@@ -20,6 +20,8 @@ PA_ERR_CUDA = 4
 PA_KV_BF16 = 0
 PA_KV_FP8_E4M3 = 1
 
+PA_STATIC_WORKSPACE_BYTES = 32 << 20
+
 PA_DEVERR_BAD_BLOCK = 0x1
 PA_DEVERR_BAD_CONTEXT = 0x2
 PA_DEVERR_TIMEOUT = 0x4
@@ -37,6 +39,8 @@ SIGNATURES = {
     "pa_decode_reduce": (_I, [_P, _SZ, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pa_decode": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F, _I, _P, _SZ,
                        _P, _P]),
+    "pa_decode_static_workspace": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F,
+                                        _F, _I, _P, _P]),
     "pa_device_errors": (_I, [ctypes.POINTER(ctypes.c_uint), _I]),
     "pa_status_string": (ctypes.c_char_p, [_I]),
     "pa_last_error": (ctypes.c_char_p, []),

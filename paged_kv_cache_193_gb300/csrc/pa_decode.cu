@@ -792,3 +792,44 @@ pa_status pa_decode(const void *q, const void *k_cache, const void *v_cache,
 }
 
 }  // extern "C"
+
+namespace pa {
+
+// Split-context decode into a caller-chosen scratch buffer of `capacity`
+// bytes; used by the static-scratch entry point.  Same checks and kernels as
+// pa_decode with partition_size > 0.
+pa_status decode_split_into(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, int num_seqs, int num_q_heads,
+                            int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                            pa_kv_dtype kv_dtype, float kv_scale, float softmax_scale,
+                            int partition_size, void *scratch, size_t capacity, void *out,
+                            cudaStream_t stream) {
+    DecodeShape sh{num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                   max_blocks_per_seq, partition_size, kv_dtype};
+    pa_status st = check_shape(sh, kv_scale, softmax_scale);
+    if (st != PA_OK) return st;
+    if (partition_size <= 0)
+        return fail(PA_ERR_INVALID_ARG, "partition_size must be > 0 (the split path needs scratch)");
+    if (num_seqs == 0) return PA_OK;
+    st = check_pointers(q, k_cache, v_cache, block_tables, context_lens);
+    if (st != PA_OK) return st;
+    if (!out || !aligned16(out)) return fail(PA_ERR_INVALID_ARG, "out must be non-null and 16-byte aligned");
+    int64_t parts = max_partitions_of(max_blocks_per_seq, block_size, partition_size);
+    if (parts * 4 > 200 * 1024)
+        return fail(PA_ERR_UNSUPPORTED, "%lld partitions exceed the merge kernel's shared memory",
+                    static_cast<long long>(parts));
+    size_t need = workspace_bytes_of(num_seqs, num_q_heads, head_dim, parts);
+    if (need > capacity)
+        return fail(PA_ERR_WORKSPACE,
+                    "this call needs %zu bytes of scratch but the library's static scratch holds "
+                    "%zu; use fewer sequences, a larger partition_size, or pa_decode with a "
+                    "workspace of your own", need, capacity);
+    st = run_decode(q, k_cache, v_cache, block_tables, context_lens, sh, kv_scale, softmax_scale,
+                    scratch, nullptr, stream);
+    if (st != PA_OK) return st;
+    return launch_reduce(scratch, context_lens, num_seqs, num_q_heads, head_dim, partition_size,
+                         static_cast<int>(parts), out, stream);
+}
+
+}  // namespace pa

@@ -1,0 +1,85 @@
+"""pa_decode_static_workspace: split-context decode for callers that cannot
+allocate device memory (their device memory belongs to another framework's
+pool, or their host forbids allocation once serving has started).  The entry
+point keeps its scratch in a fixed array inside the library, so the call
+allocates nothing.
+
+Checked here through the C ABI: two calls in a row (with different partition
+sizes, so the second reuses the shared array the first one filled) must agree
+with pa_decode given a caller-owned workspace, and a call whose scratch would
+not fit must be refused before anything is launched.  This file is collected
+last so a failure here leaves every other test already run."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import compare, device_tables
+from paged_kv_cache_193_gb300 import _lib
+from paged_kv_cache_193_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _static_call(lib, wl, bt, cl, ps, out, stream):
+    sh = wl.shape
+    return lib.pa_decode_static_workspace(
+        _ptr(wl.q), _ptr(wl.k_cache), _ptr(wl.v_cache), _ptr(bt), bt.shape[1], _ptr(cl),
+        sh.num_seqs, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, wl.num_blocks, sh.block_size,
+        sh.kv_dtype, ctypes.c_float(wl.kv_scale), ctypes.c_float(wl.softmax_scale), ps, _ptr(out),
+        ctypes.c_void_p(stream))
+
+
+def _reference_call(lib, wl, bt, cl, ps, out, stream):
+    sh = wl.shape
+    n = lib.pa_decode_workspace_size(sh.num_seqs, sh.num_q_heads, sh.head_dim, bt.shape[1],
+                                     sh.block_size, ps)
+    ws = torch.empty(n, dtype=torch.uint8, device=out.device)
+    st = lib.pa_decode(_ptr(wl.q), _ptr(wl.k_cache), _ptr(wl.v_cache), _ptr(bt), bt.shape[1],
+                       _ptr(cl), sh.num_seqs, sh.num_q_heads, sh.num_kv_heads, sh.head_dim,
+                       wl.num_blocks, sh.block_size, sh.kv_dtype, ctypes.c_float(wl.kv_scale),
+                       ctypes.c_float(wl.softmax_scale), ps, _ptr(ws), n, _ptr(out),
+                       ctypes.c_void_p(stream))
+    torch.cuda.synchronize()
+    return st
+
+
+def test_static_workspace_matches_pa_decode(cuda_device):
+    lib = _lib.load()
+    wl = W.make("llama8b", device=cuda_device, num_seqs=48)
+    W.poison(wl)
+    bt, cl = device_tables(wl, cuda_device)
+    stream = torch.cuda.current_stream().cuda_stream
+    for ps in (512, 256):
+        ref = torch.empty_like(wl.q)
+        assert _reference_call(lib, wl, bt, cl, ps, ref, stream) == 0
+        out = torch.full_like(wl.q, float("nan"))
+        st = _static_call(lib, wl, bt, cl, ps, out, stream)
+        assert st == 0, lib.pa_last_error()
+        torch.cuda.synchronize()
+        compare(out, ref.float().cpu().numpy().astype(np.float64), what=f"static scratch ps={ps}")
+    flags = ctypes.c_uint(0)
+    assert lib.pa_device_errors(ctypes.byref(flags), 1) == 0 and flags.value == 0
+
+
+def test_static_workspace_refuses_oversized_calls(cuda_device):
+    lib = _lib.load()
+    wl = W.make("tiny", device=cuda_device)
+    bt, cl = device_tables(wl, cuda_device)
+    # 4 sequences with a table of 40000 blocks at 16-token partitions need
+    # 4 * 8 * 40000 * 66 * 4 bytes of scratch, far beyond the fixed array.
+    big = torch.full((4, 40000), -1, dtype=torch.int32, device=cuda_device)
+    big[:, : bt.shape[1]] = bt
+    out = torch.zeros_like(wl.q)
+    sh = wl.shape
+    need = lib.pa_decode_workspace_size(4, sh.num_q_heads, sh.head_dim, 40000, 16, 16)
+    assert need > _lib.PA_STATIC_WORKSPACE_BYTES
+    st = _static_call(lib, wl, big, cl, 16, out, torch.cuda.current_stream().cuda_stream)
+    assert st == _lib.PA_ERR_WORKSPACE
+    assert b"static scratch" in lib.pa_last_error()
+    assert torch.count_nonzero(out) == 0
