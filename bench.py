@@ -35,12 +35,14 @@ from paged_kv_cache_193_gb300 import workloads as W  # noqa: E402
 METRIC = "paged decode attention KV GB/s and % of GB300 HBM peak; decode tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 # launch configuration per workload: (block size, partition size)
+# (the long-context 70B-head workload is defined with 512-token partitions;
+# the others are free and use the fastest measured setting)
 DEFAULT_LAUNCH = {
     "tiny": (16, 0),
-    "llama8b": (16, 512),
+    "llama8b": (16, 0),
     "long70b": (16, 512),
-    "prefix_fp8": (16, 512),
-    "ctx128k": (16, 512),
+    "prefix_fp8": (16, 0),
+    "ctx128k": (16, 2048),
 }
 DESCRIPTION = {
     "tiny": "4 seqs, ctx {1,17,100,255}, 8q/2kv heads, head_dim 64, block 16, bf16",
@@ -51,7 +53,7 @@ DESCRIPTION = {
     "prefix_fp8": "256 seqs sharing a 2048-token prefix + suffixes U[64,512], 32q/8kv heads, "
                   "head_dim 128, block 16, e4m3 KV with per-tensor scale",
     "ctx128k": "405B-head 128K context: 8 seqs x 131072 tokens, 128q/8kv heads, head_dim 128, "
-               "block 16, bf16 KV, 512-token partitions",
+               "block 16, bf16 KV, split context + log-sum-exp merge",
 }
 DECODE_SOURCES = ["paged_kv_cache_193_gb300/csrc/pa_decode.cu",
                   "paged_kv_cache_193_gb300/csrc/pa_device.cuh"]
@@ -67,6 +69,8 @@ def parse():
     ap.add_argument("--block-size", type=int, default=None)
     ap.add_argument("--partition-size", type=int, default=None)
     ap.add_argument("--num-seqs", type=int, default=None, help="shrink the workload (profiling)")
+    ap.add_argument("--separate", action="store_true",
+                    help="time the unfused entry points (3-4 kernels per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--min-warmup-seconds", type=float, default=1.0,
@@ -330,11 +334,11 @@ def run_ours(args):
     bt = torch.from_numpy(wl.block_tables).to(device)
     cl = torch.from_numpy(wl.context_lens).to(device)
     step = api.DecodeStep(wl.k_cache, wl.v_cache, bt, cl, sh.num_q_heads, wl.softmax_scale,
-                          wl.kv_scale, ps)
+                          wl.kv_scale, ps, fused=not args.separate)
     stream = torch.cuda.current_stream()
-    launches_per_step = 3 + (1 if ps else 0)
+    launches_per_step = step.launches()
 
-    # warm-up: at least W steps and at least one second of load
+    # warm-up: at least W steps and at least --min-warmup-seconds of load
     clocks = ClockSampler(local)
     clocks.start()
     api.device_errors(clear=True)
@@ -349,7 +353,8 @@ def run_ours(args):
     assert api.device_errors() == 0, "device error flags raised during warm-up"
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
@@ -357,39 +362,52 @@ def run_ours(args):
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for i in range(K):
-        e = ev[i]
-        e[0].record(stream)
-        step.append(wl.k_new, wl.v_new)
-        e[1].record(stream)
-        if ps:
-            api.decode_partitions(wl.q, wl.k_cache, wl.v_cache, bt, cl, wl.softmax_scale,
-                                  wl.kv_scale, ps, step.workspace)
-            e[2].record(stream)
-            api.decode_reduce(step.workspace, cl, sh.num_q_heads, sh.head_dim, bt.shape[1],
-                              sh.block_size, ps, step.out)
-        else:
-            api.decode(wl.q, wl.k_cache, wl.v_cache, bt, cl, wl.softmax_scale, wl.kv_scale, 0,
-                       None, step.out)
-            e[2].record(stream)
-        e[3].record(stream)
+        ev[i][0].record(stream)
+        step(wl.q, wl.k_new, wl.v_new)
+        ev[i][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     t_wall1 = time.time()
-    clocks.stop()
     total_ms = start.elapsed_time(end)
     total_ms = max_over_ranks(total_ms, world, device)
-    t_append = np.mean([e[0].elapsed_time(e[1]) for e in ev])
-    t_decode = np.array([e[1].elapsed_time(e[2]) for e in ev])
-    t_reduce = np.mean([e[2].elapsed_time(e[3]) for e in ev])
+    t_step = np.array([a.elapsed_time(b) for a, b in ev])
     assert api.device_errors() == 0, "device error flags raised during the timed steps"
+
+    # The dominant kernel on its own.  Unsplit, the fused step IS one kernel
+    # (the per-step events above).  Split, time the attention kernel and the
+    # merge one launch each with events between them (this breaks the
+    # overlap of the merge's launch with the attention tail, so it is kept
+    # out of the timed steps).
+    if ps == 0 and step.fused:
+        dec_ms, red_ms, kname = float(np.mean(t_step)), 0.0, "decode_kernel (fused step)"
+    else:
+        n2 = min(K, 200)
+        e = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n2)]
+        for i in range(n2):
+            e[i][0].record(stream)
+            if ps:
+                api.decode_partitions(wl.q, wl.k_cache, wl.v_cache, bt, cl, wl.softmax_scale,
+                                      wl.kv_scale, ps, step.workspace)
+            else:
+                api.decode(wl.q, wl.k_cache, wl.v_cache, bt, cl, wl.softmax_scale, wl.kv_scale,
+                           0, None, step.out)
+            e[i][1].record(stream)
+            if ps:
+                api.decode_reduce(step.workspace, cl, sh.num_q_heads, sh.head_dim, bt.shape[1],
+                                  sh.block_size, ps, step.out)
+            e[i][2].record(stream)
+        torch.cuda.synchronize()
+        dec_ms = float(np.mean([x[0].elapsed_time(x[1]) for x in e]))
+        red_ms = float(np.mean([x[1].elapsed_time(x[2]) for x in e]))
+        kname = "decode_kernel (per-partition attention)" if ps else "decode_kernel"
+    clocks.stop()
 
     kv = wl.kv_bytes()
     ms_per_step = total_ms / K
     value = world * kv * K / (total_ms / 1e3) / 1e9
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", 6800.0))
-    dec_ms = float(np.mean(t_decode))
     achieved = kv / (dec_ms / 1e3) / 1e9
     traffic = recorded_traffic(wl, ps)
 
@@ -403,10 +421,15 @@ def run_ours(args):
         "tokens_per_s": round(world * sh.num_seqs * K / (total_ms / 1e3), 1),
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         f"pct_of_{peak_kind}_hbm": round(100 * value / world / hbm, 2),
-        "breakdown_ms": {"slot_mapping+append": round(float(t_append), 5),
-                         "decode": round(dec_ms, 5), "reduce": round(float(t_reduce), 5)},
+        "breakdown_ms": {"step_median": round(float(np.median(t_step)), 5),
+                         "step_min": round(float(np.min(t_step)), 5),
+                         "decode_kernel": round(dec_ms, 5), "merge_kernel": round(red_ms, 5)},
+        "step_path": "pa_decode_step (slot mapping + append + attention fused; merge as a "
+                     "programmatic dependent launch when split)" if step.fused else
+                     "separate pa_slot_mapping, pa_cache_append, pa_decode[_partitions], "
+                     "pa_decode_reduce",
         "gpu_launches": K * launches_per_step,
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
                      "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",

@@ -195,6 +195,29 @@ pa_status pa_decode(const void *q, const void *k_cache, const void *v_cache,
                     void *out, cudaStream_t stream);
 
 /*
+ * pa_decode_step -- one whole decode step of one layer in one launch (two
+ * when split): slot mapping, append and attention fused.
+ * For every sequence s with n = context_lens[s] > 0, the new token's rows
+ * k_new[s], v_new[s] (bf16 [num_seqs][num_kv_heads][head_dim]) are written
+ * into slot block_tables[s][(n-1)/block_size]*block_size + (n-1)%block_size
+ * exactly as pa_cache_append writes them (FP8: with scale kv_scale), and then
+ * out is computed exactly as pa_decode computes it over the n tokens,
+ * including the new one ("PagedAttention Mechanics": append, then attend).
+ * slot_mapping (optional, int32 [num_seqs], may be NULL) receives the slots
+ * (-1 for empty sequences).  The appended token's block must not be shared
+ * with another sequence.  Workspace as for pa_decode.  The append is done by
+ * the attention kernel's CTA that owns the token's partition, before it
+ * reads that page.
+ */
+pa_status pa_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                         void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *context_lens, int num_seqs, int num_q_heads,
+                         int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                         pa_kv_dtype kv_dtype, float kv_scale, float softmax_scale,
+                         int partition_size, void *workspace, size_t workspace_bytes,
+                         int32_t *slot_mapping, void *out, cudaStream_t stream);
+
+/*
  * pa_decode_static_workspace -- pa_decode with partition_size > 0, without
  * the caller's workspace.
  * The source pages have no counterpart to this entry point.  It exists for

@@ -39,6 +39,8 @@ SIGNATURES = {
     "pa_decode_reduce": (_I, [_P, _SZ, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pa_decode": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F, _I, _P, _SZ,
                        _P, _P]),
+    "pa_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F,
+                            _I, _P, _SZ, _P, _P, _P]),
     "pa_decode_static_workspace": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                         _F, _I, _P, _P]),
     "pa_device_errors": (_I, [ctypes.POINTER(ctypes.c_uint), _I]),
@@ -50,10 +52,12 @@ _lib = None
 
 
 def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libpa.so (``PA_LIBRARY`` in the environment selects another build
+    of the same library, e.g. a launch-shape variant)."""
     global _lib
     if _lib is not None and path is None:
         return _lib
-    p = path or LIB_PATH
+    p = path or os.environ.get("PA_LIBRARY") or LIB_PATH
     if not os.path.exists(p):
         raise ImportError(
             f"{p} not found: build the CUDA library first "

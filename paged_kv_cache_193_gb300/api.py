@@ -155,6 +155,38 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     return out
 
 
+def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                softmax_scale: float | None = None, kv_scale: float = 1.0, partition_size: int = 0,
+                workspace: torch.Tensor | None = None, slot_mapping: torch.Tensor | None = None,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One fused decode step: append each sequence's new K/V row at position
+    ctx - 1, then attend over the ctx tokens.  Returns bf16 [S, Hq, D]."""
+    kv_dtype, S, Hq, D, NB, Hkv, B = _decode_common(q, k_cache, v_cache, block_tables, context_lens)
+    _need(k_new, "k_new", (torch.bfloat16,), 3)
+    _need(v_new, "v_new", (torch.bfloat16,), 3)
+    if tuple(k_new.shape) != (S, Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [num_seqs, num_kv_heads, head_dim]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", (torch.bfloat16,), 3)
+    if slot_mapping is not None:
+        _need(slot_mapping, "slot_mapping", (torch.int32,), 1)
+    if partition_size and workspace is None:
+        workspace = alloc_workspace(q, block_tables, B, partition_size)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib_handle().pa_decode_step(
+        q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), S, Hq, Hkv, D, NB,
+        B, kv_dtype, float(kv_scale), float(softmax_scale), int(partition_size), ws_ptr, ws_bytes,
+        slot_mapping.data_ptr() if slot_mapping is not None else None, out.data_ptr(),
+        _stream(stream)))
+    return out
+
+
 def decode_partitions(q, k_cache, v_cache, block_tables, context_lens, softmax_scale, kv_scale,
                       partition_size, workspace, stream=None) -> None:
     """Per-partition (o, m, l) into ``workspace`` (layout in include/pa.h)."""
@@ -203,10 +235,13 @@ class DecodeStep:
     """One decode step of one attention layer over a paged cache, with every
     buffer allocated up front: slot mapping of the newest tokens, append of
     their K/V, partitioned attention and (when split) the merge.  Calling it
-    launches 3 or 4 kernels on the current stream and allocates nothing."""
+    allocates nothing.  ``fused`` (default) runs ``pa_decode_step``: 1 kernel,
+    2 when split; otherwise the separate entry points: 3 kernels, 4 when
+    split."""
 
     def __init__(self, k_cache, v_cache, block_tables, context_lens, num_q_heads,
-                 softmax_scale=None, kv_scale=1.0, partition_size=0):
+                 softmax_scale=None, kv_scale=1.0, partition_size=0, fused=True):
+        self.fused = fused
         self.k_cache, self.v_cache = k_cache, v_cache
         self.block_tables, self.context_lens = block_tables, context_lens
         NB, self.Hkv, self.B, self.D = k_cache.shape
@@ -238,6 +273,14 @@ class DecodeStep:
                    self.softmax_scale, self.kv_scale, 0, None, self.out, stream=stream)
         return self.out
 
+    def launches(self) -> int:
+        """Kernels one call launches."""
+        return (1 if self.fused else 3) + (1 if self.partition_size else 0)
+
     def __call__(self, q, k_new, v_new, stream=None):
+        if self.fused:
+            return decode_step(q, k_new, v_new, self.k_cache, self.v_cache, self.block_tables,
+                               self.context_lens, self.softmax_scale, self.kv_scale,
+                               self.partition_size, self.workspace, self.slots, self.out, stream)
         self.append(k_new, v_new, stream)
         return self.attend(q, stream)

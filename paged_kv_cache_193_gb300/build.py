@@ -52,16 +52,21 @@ def compile_flags(verbose_ptxas: bool = False) -> list[str]:
     return flags
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile and link if any source is newer than the library; return its path."""
-    if not force and not _stale():
+def build(force: bool = False, verbose_ptxas: bool = False, out: str | None = None,
+          defines: tuple[str, ...] = ()) -> str:
+    """Compile and link if any source is newer than the library; return its
+    path.  ``out`` and ``defines`` (e.g. ``("PA_DECODE_WARPS=2",)``) build a
+    variant of the library elsewhere, for launch-shape tuning."""
+    lib = out or LIB
+    if not force and not defines and out is None and not _stale():
         return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+    obj_dir = os.path.join(os.path.dirname(lib), os.path.basename(lib) + ".objs") if out else OUT_DIR
+    os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
-    flags = compile_flags(verbose_ptxas)
+    flags = compile_flags(verbose_ptxas) + ["-D" + d for d in defines]
 
     def one(src: str) -> tuple[str, str]:
-        obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         cmd = [cc, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -74,13 +79,13 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if verbose_ptxas:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -54,6 +54,15 @@ struct DecodeArgs {
     float *ws_m;
     float *ws_l;
     unsigned int *err;
+    // fused append (pa_decode_step): the CTA whose partition holds a
+    // sequence's newest token first writes that token's K/V row of its KV
+    // head into the cache; null k_new = no append
+    const uint4 *k_new;  // bf16 [num_seqs][num_kv_heads][head_dim]
+    const uint4 *v_new;
+    uint8_t *k_cache_w;
+    uint8_t *v_cache_w;
+    int32_t *slot_out;   // optional: slot of each sequence's newest token
+    float append_scale;  // E4M3 scale of the append (cache dtype FP8)
 };
 
 // Give up on a page copy after this long (normal waits are microseconds).
@@ -96,7 +105,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int t, int b) {
 }
 
 template <int D, int BS, bool FP8, int NT, int NW, int SPW>
-__global__ void __launch_bounds__(NW * 32, 2)
+__global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeArgs a) {
     using C = Cfg<D, BS, FP8, NT, NW, SPW>;
@@ -111,18 +120,88 @@ __global__ void __launch_bounds__(NW * 32, 2)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = lane >> 2, c = lane & 3;
 
-    int n = a.context_lens[s];
+    // let a dependent merge kernel launch now; it waits for our results
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    // Block-table entries and the query do not depend on the context length:
+    // load them first so their latency overlaps the context-length load.
+    const int t_begin = part * a.partition_size;
+    const int page0 = t_begin / BS;
+    const int lim = min(a.max_blocks - page0, a.partition_size / BS) - warp;  // table entries left
+    const int32_t *bt = a.block_tables + static_cast<int64_t>(s) * a.max_blocks + page0 + warp;
+    int ent_cur = lane * NW < lim ? __ldg(bt + lane * NW) : -1;
+    int ent_next = (32 + lane) * NW < lim ? __ldg(bt + (32 + lane) * NW) : -1;
+
+    // query fragments (B operand of S^T = K Q^T), resident in registers
+    uint32_t qf[C::KSTEPS][NT][2];
+    {
+        const __nv_bfloat16 *qh = a.q + (static_cast<int64_t>(s) * a.num_q_heads + h * a.group) * D;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int g = nt * 8 + r;
+            const bool live = g < a.group;
+            const __nv_bfloat16 *qg = qh + g * D;
+#pragma unroll
+            for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                if constexpr (!FP8) {
+                    // logical k = 2c, 2c+1 and 2c+8, 2c+9 of this 16-dim step
+                    qf[kk][nt][0] = live ? __ldg(reinterpret_cast<const uint32_t *>(qg + kk * 16 + 2 * c)) : 0u;
+                    qf[kk][nt][1] = live ? __ldg(reinterpret_cast<const uint32_t *>(qg + kk * 16 + 8 + 2 * c)) : 0u;
+                } else {
+                    // permuted order: this thread's dims are c*16*CPT + 4*kk + {0,1,2,3}
+                    uint2 w = live ? __ldg(reinterpret_cast<const uint2 *>(qg + c * 16 * C::CPT + 4 * kk))
+                                   : make_uint2(0u, 0u);
+                    float2 f0 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w.x));
+                    float2 f1 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w.y));
+                    qf[kk][nt][0] = pack2<true>(f0.x, f0.y);
+                    qf[kk][nt][1] = pack2<true>(f1.x, f1.y);
+                }
+            }
+        }
+    }
+
+    const int n_raw = a.context_lens[s];
+    int n = n_raw;
     const int cap = a.max_blocks * BS;
     if (n > cap) {
         if (tid == 0 && part == 0 && h == 0) set_device_error(a.err, PA_DEVERR_BAD_CONTEXT);
         n = cap;
     }
     if (n < 0) n = 0;
-    const int t_begin = part * a.partition_size;
+    if (a.k_new && a.slot_out && n == 0 && part == 0 && h == 0 && tid == 0) a.slot_out[s] = -1;
     if (a.split && t_begin >= n) return;  // past this sequence's end: nothing to write
     const int t_end = min(t_begin + a.partition_size, n);
-    const int page0 = t_begin / BS;
     const int npages = t_end > t_begin ? (t_end - t_begin + BS - 1) / BS : 0;
+
+    if (a.k_new && n > 0 && n_raw <= cap && n - 1 >= t_begin && n - 1 < t_end) {
+        // Append the newest token of sequence s (position n - 1, which this
+        // partition holds) for KV head h, before any page copy is issued.
+        const int pos = n - 1;
+        const int32_t blk = a.block_tables[static_cast<int64_t>(s) * a.max_blocks + pos / BS];
+        if (blk >= 0 && blk < a.num_blocks) {
+            if (tid < D / 8) {
+                const int64_t src = (static_cast<int64_t>(s) * a.num_kv_heads + h) * (D / 8) + tid;
+                const int64_t dst =
+                    ((static_cast<int64_t>(blk) * a.num_kv_heads + h) * BS + pos % BS) * D + tid * 8;
+                const uint4 kv = a.k_new[src], vv = a.v_new[src];
+                if constexpr (!FP8) {
+                    *reinterpret_cast<uint4 *>(a.k_cache_w + dst * 2) = kv;
+                    *reinterpret_cast<uint4 *>(a.v_cache_w + dst * 2) = vv;
+                } else {
+                    *reinterpret_cast<uint2 *>(a.k_cache_w + dst) = quantize8_e4m3(kv, a.append_scale);
+                    *reinterpret_cast<uint2 *>(a.v_cache_w + dst) = quantize8_e4m3(vv, a.append_scale);
+                }
+                // the row is read back below by this CTA's TMA (async proxy)
+                fence_proxy_async_global();
+            }
+            if (h == 0 && tid == 0 && a.slot_out) a.slot_out[s] = blk * BS + pos % BS;
+        } else {
+            if (tid == 0) set_device_error(a.err, PA_DEVERR_BAD_BLOCK);
+            if (h == 0 && tid == 0 && a.slot_out) a.slot_out[s] = -1;
+        }
+    } else if (a.k_new && a.slot_out && n_raw > cap && part == 0 && h == 0 && tid == 0) {
+        a.slot_out[s] = -1;
+    }
 
     if (tid == 0) {
 #pragma unroll
@@ -133,11 +212,8 @@ __global__ void __launch_bounds__(NW * 32, 2)
     }
     __syncthreads();
 
-    // ---- this warp's pages and their block-table entries -----------------
+    // ---- this warp's pages ----------------------------------------------------
     const int my_pages = npages > warp ? (npages - warp + NW - 1) / NW : 0;
-    const int32_t *bt = a.block_tables + static_cast<int64_t>(s) * a.max_blocks + page0 + warp;
-    int ent_cur = lane < my_pages ? bt[lane * NW] : -1;
-    int ent_next = 32 + lane < my_pages ? bt[(32 + lane) * NW] : -1;
     int chunk_cur = 0;
     const uint64_t policy = l2_evict_first_policy();
     const int rows_total = a.num_blocks * a.num_kv_heads * BS;
@@ -149,7 +225,7 @@ __global__ void __launch_bounds__(NW * 32, 2)
             ent_cur = ent_next;
             chunk_cur = ck;
             const int kk = (ck + 1) * 32 + lane;
-            ent_next = kk < my_pages ? bt[kk * NW] : -1;
+            ent_next = kk < my_pages ? __ldg(bt + kk * NW) : -1;
         }
         return __shfl_sync(0xffffffffu, ent_cur, k & 31);
     };
@@ -178,34 +254,6 @@ __global__ void __launch_bounds__(NW * 32, 2)
     for (int k = 0; k < prolog; ++k) {
         const int blk = entry(k);
         if (lane == 0) issue(k, blk);
-    }
-
-    // ---- query fragments (B operand of S^T = K Q^T), resident in registers
-    uint32_t qf[C::KSTEPS][NT][2];
-    {
-        const __nv_bfloat16 *qh = a.q + (static_cast<int64_t>(s) * a.num_q_heads + h * a.group) * D;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int g = nt * 8 + r;
-            const bool live = g < a.group;
-            const __nv_bfloat16 *qg = qh + g * D;
-#pragma unroll
-            for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                if constexpr (!FP8) {
-                    // logical k = 2c, 2c+1 and 2c+8, 2c+9 of this 16-dim step
-                    qf[kk][nt][0] = live ? *reinterpret_cast<const uint32_t *>(qg + kk * 16 + 2 * c) : 0u;
-                    qf[kk][nt][1] = live ? *reinterpret_cast<const uint32_t *>(qg + kk * 16 + 8 + 2 * c) : 0u;
-                } else {
-                    // permuted order: this thread's dims are c*16*CPT + 4*kk + {0,1,2,3}
-                    uint2 w = live ? *reinterpret_cast<const uint2 *>(qg + c * 16 * C::CPT + 4 * kk)
-                                   : make_uint2(0u, 0u);
-                    float2 f0 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w.x));
-                    float2 f1 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w.y));
-                    qf[kk][nt][0] = pack2<true>(f0.x, f0.y);
-                    qf[kk][nt][1] = pack2<true>(f1.x, f1.y);
-                }
-            }
-        }
     }
 
     float o[C::DT][NT][4];
@@ -541,14 +589,30 @@ static pa_status make_map(CUtensorMap *map, const void *cache, bool fp8, int hea
     return PA_OK;
 }
 
-constexpr int kWarps = 4;
-constexpr int kStagesPerWarp = 2;
+// Launch shape (build-time): warps per CTA, and the shared-memory budget of
+// the page ring, from which the pages in flight per warp follow.
+#ifndef PA_DECODE_WARPS
+#define PA_DECODE_WARPS 4
+#endif
+#ifndef PA_DECODE_RING_KB
+#define PA_DECODE_RING_KB 64
+#endif
+constexpr int kWarps = PA_DECODE_WARPS;
+constexpr int kRingBytes = PA_DECODE_RING_KB * 1024;
+
+template <int D, int BS, bool FP8>
+constexpr int stages_per_warp() {
+    constexpr int stage = 2 * BS * D * (FP8 ? 1 : 2);
+    constexpr int spw = kRingBytes / (kWarps * stage);
+    return spw < 1 ? 1 : spw;
+}
 
 template <int D, int BS, bool FP8, int NT>
 static pa_status launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
                                dim3 grid, cudaStream_t stream) {
-    using C = Cfg<D, BS, FP8, NT, kWarps, kStagesPerWarp>;
-    auto kern = decode_kernel<D, BS, FP8, NT, kWarps, kStagesPerWarp>;
+    constexpr int SPW = stages_per_warp<D, BS, FP8>();
+    using C = Cfg<D, BS, FP8, NT, kWarps, SPW>;
+    auto kern = decode_kernel<D, BS, FP8, NT, kWarps, SPW>;
     pa_status st = cuda_check(
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM),
         "cudaFuncSetAttribute(decode)");
@@ -623,11 +687,19 @@ static size_t workspace_bytes_of(int num_seqs, int num_q_heads, int head_dim, in
     return static_cast<size_t>(num_seqs) * num_q_heads * parts * (head_dim + 2) * sizeof(float);
 }
 
+// New-token rows appended by the decode kernel itself (pa_decode_step).
+struct StepAppend {
+    const void *k_new;
+    const void *v_new;
+    int32_t *slot_out;
+};
+
 // Launch the per-partition (split) or whole-context (unsplit) kernel.
 static pa_status run_decode(const void *q, const void *k_cache, const void *v_cache,
                             const int32_t *block_tables, const int32_t *context_lens,
                             const DecodeShape &sh, float kv_scale, float softmax_scale,
-                            void *workspace, void *out, cudaStream_t stream) {
+                            void *workspace, void *out, cudaStream_t stream,
+                            const StepAppend *app = nullptr) {
     const bool split = sh.partition_size > 0;
     const int64_t parts = max_partitions_of(sh.max_blocks, sh.block_size, sh.partition_size);
     const bool fp8 = sh.kv_dtype == PA_KV_FP8_E4M3;
@@ -661,6 +733,12 @@ static pa_status run_decode(const void *q, const void *k_cache, const void *v_ca
     a.ws_m = split ? a.ws_o + wrows * parts * sh.head_dim : nullptr;
     a.ws_l = split ? a.ws_m + wrows * parts : nullptr;
     a.err = err;
+    a.k_new = app ? static_cast<const uint4 *>(app->k_new) : nullptr;
+    a.v_new = app ? static_cast<const uint4 *>(app->v_new) : nullptr;
+    a.k_cache_w = app ? static_cast<uint8_t *>(const_cast<void *>(k_cache)) : nullptr;
+    a.v_cache_w = app ? static_cast<uint8_t *>(const_cast<void *>(v_cache)) : nullptr;
+    a.slot_out = app ? app->slot_out : nullptr;
+    a.append_scale = kv_scale;
 
     if (parts > 0x7fffffffLL) return fail(PA_ERR_UNSUPPORTED, "too many partitions");
     dim3 grid(static_cast<unsigned>(split ? parts : 1), sh.num_kv_heads, sh.num_seqs);
@@ -746,9 +824,6 @@ pa_status pa_decode_reduce(const void *workspace, size_t workspace_bytes,
     if (!context_lens || !out) return fail(PA_ERR_INVALID_ARG, "null pointer");
     if (!aligned16(out)) return fail(PA_ERR_INVALID_ARG, "out must be 16-byte aligned");
     int64_t parts = max_partitions_of(max_blocks_per_seq, block_size, partition_size);
-    if (parts * 4 > 200 * 1024)
-        return fail(PA_ERR_UNSUPPORTED, "%lld partitions exceed the merge kernel's shared memory",
-                    static_cast<long long>(parts));
     size_t need = workspace_bytes_of(num_seqs, num_q_heads, head_dim, parts);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need)
         return fail(PA_ERR_WORKSPACE, "workspace %p of %zu bytes (need %zu, 16-byte aligned)",
@@ -777,15 +852,47 @@ pa_status pa_decode(const void *q, const void *k_cache, const void *v_cache,
         return run_decode(q, k_cache, v_cache, block_tables, context_lens, sh, kv_scale,
                           softmax_scale, nullptr, out, stream);
     int64_t parts = max_partitions_of(max_blocks_per_seq, block_size, partition_size);
-    if (parts * 4 > 200 * 1024)
-        return fail(PA_ERR_UNSUPPORTED, "%lld partitions exceed the merge kernel's shared memory",
-                    static_cast<long long>(parts));
     size_t need = workspace_bytes_of(num_seqs, num_q_heads, head_dim, parts);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need)
         return fail(PA_ERR_WORKSPACE, "workspace %p of %zu bytes (need %zu, 16-byte aligned)",
                     workspace, workspace_bytes, need);
     st = run_decode(q, k_cache, v_cache, block_tables, context_lens, sh, kv_scale, softmax_scale,
                     workspace, nullptr, stream);
+    if (st != PA_OK) return st;
+    return launch_reduce(workspace, context_lens, num_seqs, num_q_heads, head_dim, partition_size,
+                         static_cast<int>(parts), out, stream);
+}
+
+pa_status pa_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                         void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *context_lens, int num_seqs, int num_q_heads,
+                         int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                         pa_kv_dtype kv_dtype, float kv_scale, float softmax_scale,
+                         int partition_size, void *workspace, size_t workspace_bytes,
+                         int32_t *slot_mapping, void *out, cudaStream_t stream) {
+    clear_error();
+    DecodeShape sh{num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                   max_blocks_per_seq, partition_size, kv_dtype};
+    pa_status st = check_shape(sh, kv_scale, softmax_scale);
+    if (st != PA_OK) return st;
+    if (num_seqs == 0) return PA_OK;
+    st = check_pointers(q, k_cache, v_cache, block_tables, context_lens);
+    if (st != PA_OK) return st;
+    if (!k_new || !v_new) return fail(PA_ERR_INVALID_ARG, "null pointer (k_new / v_new)");
+    if (!aligned16(k_new) || !aligned16(v_new))
+        return fail(PA_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    if (!out || !aligned16(out)) return fail(PA_ERR_INVALID_ARG, "out must be non-null and 16-byte aligned");
+    StepAppend app{k_new, v_new, slot_mapping};
+    if (partition_size == 0)
+        return run_decode(q, k_cache, v_cache, block_tables, context_lens, sh, kv_scale,
+                          softmax_scale, nullptr, out, stream, &app);
+    int64_t parts = max_partitions_of(max_blocks_per_seq, block_size, partition_size);
+    size_t need = workspace_bytes_of(num_seqs, num_q_heads, head_dim, parts);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need)
+        return fail(PA_ERR_WORKSPACE, "workspace %p of %zu bytes (need %zu, 16-byte aligned)",
+                    workspace, workspace_bytes, need);
+    st = run_decode(q, k_cache, v_cache, block_tables, context_lens, sh, kv_scale, softmax_scale,
+                    workspace, nullptr, stream, &app);
     if (st != PA_OK) return st;
     return launch_reduce(workspace, context_lens, num_seqs, num_q_heads, head_dim, partition_size,
                          static_cast<int>(parts), out, stream);
@@ -816,9 +923,6 @@ pa_status decode_split_into(const void *q, const void *k_cache, const void *v_ca
     if (st != PA_OK) return st;
     if (!out || !aligned16(out)) return fail(PA_ERR_INVALID_ARG, "out must be non-null and 16-byte aligned");
     int64_t parts = max_partitions_of(max_blocks_per_seq, block_size, partition_size);
-    if (parts * 4 > 200 * 1024)
-        return fail(PA_ERR_UNSUPPORTED, "%lld partitions exceed the merge kernel's shared memory",
-                    static_cast<long long>(parts));
     size_t need = workspace_bytes_of(num_seqs, num_q_heads, head_dim, parts);
     if (need > capacity)
         return fail(PA_ERR_WORKSPACE,

@@ -56,6 +56,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's generic-proxy global writes before later async-proxy
+// (TMA) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                  "r"(bytes)
@@ -206,6 +212,26 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 __device__ __forceinline__ void set_device_error(unsigned int *err, unsigned int bits) {
     if (err) atomicOr(err, bits);
+}
+
+// Eight bf16 values -> eight E4M3 codes of x / scale: IEEE fp32 division,
+// round to nearest even, saturating to +-448 (the append's FP8 encoding).
+__device__ __forceinline__ uint2 quantize8_e4m3(const uint4 &bf16x8, float scale) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&bf16x8);
+    uint32_t words[2];
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float2 f = __bfloat1622float2(h[w * 2 + j]);
+            float2 q = make_float2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+            __nv_fp8x2_storage_t two = __nv_cvt_float2_to_fp8x2(q, __NV_SATFINITE, __NV_E4M3);
+            packed |= static_cast<uint32_t>(two) << (16 * j);
+        }
+        words[w] = packed;
+    }
+    return make_uint2(words[0], words[1]);
 }
 
 }  // namespace pa

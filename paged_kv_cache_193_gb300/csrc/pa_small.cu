@@ -106,122 +106,127 @@ __global__ void append_kernel(const uint4 *__restrict__ k, const uint4 *__restri
         *reinterpret_cast<uint4 *>(k_cache + dst * 2) = kv;
         *reinterpret_cast<uint4 *>(v_cache + dst * 2) = vv;
     } else {
-        const uint4 *src[2] = {&kv, &vv};
-        uint8_t *cache[2] = {k_cache, v_cache};
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
-            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(src[which]);
-            uint32_t words[2];
-#pragma unroll
-            for (int w = 0; w < 2; ++w) {
-                uint32_t packed = 0;
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    float2 f = __bfloat1622float2(h[w * 2 + j]);
-                    float2 q = make_float2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
-                    __nv_fp8x2_storage_t two = __nv_cvt_float2_to_fp8x2(q, __NV_SATFINITE, __NV_E4M3);
-                    packed |= static_cast<uint32_t>(two) << (16 * j);
-                }
-                words[w] = packed;
-            }
-            *reinterpret_cast<uint2 *>(cache[which] + dst) = make_uint2(words[0], words[1]);
-        }
+        *reinterpret_cast<uint2 *>(k_cache + dst) = quantize8_e4m3(kv, scale);
+        *reinterpret_cast<uint2 *>(v_cache + dst) = quantize8_e4m3(vv, scale);
     }
 }
 
 // ---------------------------------------------------------------------------
-// partition merge: one CTA of 128 threads per (sequence, query head)
+// partition merge: WPR warps per (sequence, query head), 128 threads per CTA
 // ---------------------------------------------------------------------------
 
 constexpr int kReduceThreads = 128;
 
-template <int D>
-__global__ void __launch_bounds__(kReduceThreads)
-    reduce_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_m,
-                  const float *__restrict__ ws_l, const int32_t *__restrict__ context_lens,
-                  int num_q_heads, int partition_size, int max_partitions,
-                  __nv_bfloat16 *__restrict__ out) {
-    constexpr int VEC = D / 32;  // floats per lane across one warp
-    constexpr int NWARP = kReduceThreads / 32;
-    extern __shared__ float w_s[];  // [max_partitions] weights
-    __shared__ float red[NWARP];
-    __shared__ float acc_s[NWARP][D];
+// Wait until the grid this one depends on (programmatic dependent launch)
+// has finished and its writes are visible; a no-op otherwise.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
-    const int hq = blockIdx.x, s = blockIdx.y;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t row = static_cast<int64_t>(s) * num_q_heads + hq;
-    __nv_bfloat16 *dst = out + row * D;
-    int n = context_lens[s];
-    n = n > 0 ? (n + partition_size - 1) / partition_size : 0;
-    if (n > max_partitions) n = max_partitions;
-    if (n == 0) {
-        for (int d = tid; d < D; d += kReduceThreads) dst[d] = __float2bfloat16_rn(0.f);
-        return;
-    }
-    const float *m = ws_m + row * max_partitions;
-    const float *l = ws_l + row * max_partitions;
-
-    // M = max_p m_p
-    float mx = -INFINITY;
-    for (int p = tid; p < n; p += kReduceThreads) mx = fmaxf(mx, m[p]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) red[warp] = mx;
-    __syncthreads();
-    mx = red[0];
-#pragma unroll
-    for (int w = 1; w < NWARP; ++w) mx = fmaxf(mx, red[w]);
-    __syncthreads();
-
-    // w_p = l_p exp(m_p - M), W = sum_p w_p
-    float sum = 0.f;
-    for (int p = tid; p < n; p += kReduceThreads) {
-        float w = l[p] * __expf(m[p] - mx);
-        w_s[p] = w;
-        sum += w;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) red[warp] = sum;
-    __syncthreads();
-    float total = 0.f;
-#pragma unroll
-    for (int w = 0; w < NWARP; ++w) total += red[w];
-
-    // out = sum_p w_p o_p / W; warp w takes partitions p = w, w + 4, ...
-    float acc[VEC];
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
-    const float *o = ws_o + row * max_partitions * D + lane * VEC;
-    for (int p = warp; p < n; p += NWARP) {
-        float w = w_s[p];
-        const float *src = o + static_cast<int64_t>(p) * D;
-        if constexpr (VEC == 4) {
-            float4 x = *reinterpret_cast<const float4 *>(src);
-            acc[0] += w * x.x;
-            acc[1] += w * x.y;
-            acc[2] += w * x.z;
-            acc[3] += w * x.w;
-        } else {
-            float2 x = *reinterpret_cast<const float2 *>(src);
-            acc[0] += w * x.x;
-            acc[1] += w * x.y;
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) acc_s[warp][lane * VEC + j] = acc[j];
-    __syncthreads();
-    float inv = 1.f / total;
-    for (int d = tid; d < D; d += kReduceThreads) {
-        float a = 0.f;
-#pragma unroll
-        for (int w = 0; w < NWARP; ++w) a += acc_s[w][d];
-        dst[d] = __float2bfloat16_rn(a * inv);
+template <int VEC>
+__device__ __forceinline__ void fma_vec(float (&acc)[VEC], float w, const float *src) {
+    if constexpr (VEC == 4) {
+        const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
+        acc[0] += w * x.x;
+        acc[1] += w * x.y;
+        acc[2] += w * x.z;
+        acc[3] += w * x.w;
+    } else {
+        const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
+        acc[0] += w * x.x;
+        acc[1] += w * x.y;
     }
 }
 
-// Shared by pa_decode (split path) and pa_decode_reduce; arguments checked
-// by the caller.
+// Each warp covers all D dims of its row (VEC per lane); the WPR warps of a
+// row take partitions p = sub, sub + WPR, ... with four independent
+// accumulators so four partition loads are in flight per warp.
+template <int D, int WPR>
+__global__ void __launch_bounds__(kReduceThreads)
+    reduce_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_m,
+                  const float *__restrict__ ws_l, const int32_t *__restrict__ context_lens,
+                  int num_rows, int num_q_heads, int partition_size, int max_partitions,
+                  __nv_bfloat16 *__restrict__ out) {
+    constexpr int VEC = D / 32;
+    constexpr int ROWS = kReduceThreads / 32 / WPR;
+    __shared__ float part_s[WPR > 1 ? ROWS * WPR : 1][WPR > 1 ? D : 1];
+    grid_dependency_wait();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = warp % WPR;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * ROWS + warp / WPR;
+    const bool live = row < num_rows;
+    int n = 0;
+    if (live) {
+        const int ctx = context_lens[row / num_q_heads];
+        n = ctx > 0 ? (ctx + partition_size - 1) / partition_size : 0;
+        if (n > max_partitions) n = max_partitions;
+    }
+    float acc[4][VEC];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) acc[u][j] = 0.f;
+    float total = 0.f;
+    if (n > 0) {
+        const float *m = ws_m + row * max_partitions;
+        const float *l = ws_l + row * max_partitions;
+        float mx = -INFINITY;
+        for (int p = lane; p < n; p += 32) mx = fmaxf(mx, __ldcg(m + p));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        for (int p = lane; p < n; p += 32) total += __ldcg(l + p) * __expf(__ldcg(m + p) - mx);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+        const float *o = ws_o + row * max_partitions * D + lane * VEC;
+        int p = sub;
+        for (; p + 3 * WPR < n; p += 4 * WPR) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int q = p + u * WPR;
+                const float w = __ldcg(l + q) * __expf(__ldcg(m + q) - mx);
+                fma_vec<VEC>(acc[u], w, o + static_cast<int64_t>(q) * D);
+            }
+        }
+        for (; p < n; p += WPR) {
+            const float w = __ldcg(l + p) * __expf(__ldcg(m + p) - mx);
+            fma_vec<VEC>(acc[0], w, o + static_cast<int64_t>(p) * D);
+        }
+    }
+    float res[VEC];
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) res[j] = acc[0][j] + acc[1][j] + acc[2][j] + acc[3][j];
+    if constexpr (WPR > 1) {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) part_s[warp][lane * VEC + j] = res[j];
+        __syncthreads();
+        if (sub != 0) return;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+            float a = 0.f;
+#pragma unroll
+            for (int w = 0; w < WPR; ++w) a += part_s[warp + w][lane * VEC + j];
+            res[j] = a;
+        }
+    }
+    if (!live) return;
+    const float inv = total > 0.f ? 1.f / total : 0.f;
+    __nv_bfloat16 *dst = out + row * D + lane * VEC;
+    if constexpr (VEC == 4) {
+        __nv_bfloat162 a = __floats2bfloat162_rn(res[0] * inv, res[1] * inv);
+        __nv_bfloat162 b = __floats2bfloat162_rn(res[2] * inv, res[3] * inv);
+        uint2 v;
+        v.x = *reinterpret_cast<uint32_t *>(&a);
+        v.y = *reinterpret_cast<uint32_t *>(&b);
+        *reinterpret_cast<uint2 *>(dst) = v;
+    } else {
+        *reinterpret_cast<__nv_bfloat162 *>(dst) = __floats2bfloat162_rn(res[0] * inv, res[1] * inv);
+    }
+}
+
+// Shared by pa_decode (split path), pa_decode_step and pa_decode_reduce;
+// arguments checked by the caller.  Launched as a programmatic dependent of
+// the kernel before it on the stream, so its launch overlaps that kernel's
+// tail; the kernel itself waits for the predecessor's results.
 pa_status launch_reduce(const void *workspace, const int32_t *context_lens, int num_seqs,
                         int num_q_heads, int head_dim, int partition_size, int max_partitions,
                         void *out, cudaStream_t stream) {
@@ -229,32 +234,33 @@ pa_status launch_reduce(const void *workspace, const int32_t *context_lens, int 
     const int64_t rows = static_cast<int64_t>(num_seqs) * num_q_heads;
     const float *ws_m = ws_o + rows * max_partitions * head_dim;
     const float *ws_l = ws_m + rows * max_partitions;
-    dim3 grid(num_q_heads, num_seqs);
-    size_t smem = static_cast<size_t>(max_partitions) * sizeof(float);
-    if (head_dim == 128) {
-        if (smem > 48 * 1024) {
-            pa_status st = cuda_check(cudaFuncSetAttribute(reduce_kernel<128>,
-                                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                           static_cast<int>(smem)),
-                                      "cudaFuncSetAttribute(reduce)");
-            if (st != PA_OK) return st;
-        }
-        reduce_kernel<128><<<grid, kReduceThreads, smem, stream>>>(
-            ws_o, ws_m, ws_l, context_lens, num_q_heads, partition_size, max_partitions,
-            static_cast<__nv_bfloat16 *>(out));
-    } else {
-        if (smem > 48 * 1024) {
-            pa_status st = cuda_check(cudaFuncSetAttribute(reduce_kernel<64>,
-                                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                           static_cast<int>(smem)),
-                                      "cudaFuncSetAttribute(reduce)");
-            if (st != PA_OK) return st;
-        }
-        reduce_kernel<64><<<grid, kReduceThreads, smem, stream>>>(
-            ws_o, ws_m, ws_l, context_lens, num_q_heads, partition_size, max_partitions,
-            static_cast<__nv_bfloat16 *>(out));
-    }
-    return cuda_check(cudaGetLastError(), "reduce launch");
+    // one warp per row while partitions are few, four when there are many
+    const int wpr = max_partitions > 16 ? 4 : 1;
+    const int rows_per_cta = kReduceThreads / 32 / wpr;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta));
+    cfg.blockDim = dim3(kReduceThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int nrows = static_cast<int>(rows);
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(out);
+    cudaError_t e;
+    if (head_dim == 128)
+        e = wpr == 4 ? cudaLaunchKernelEx(&cfg, reduce_kernel<128, 4>, ws_o, ws_m, ws_l, context_lens,
+                                          nrows, num_q_heads, partition_size, max_partitions, o)
+                     : cudaLaunchKernelEx(&cfg, reduce_kernel<128, 1>, ws_o, ws_m, ws_l, context_lens,
+                                          nrows, num_q_heads, partition_size, max_partitions, o);
+    else
+        e = wpr == 4 ? cudaLaunchKernelEx(&cfg, reduce_kernel<64, 4>, ws_o, ws_m, ws_l, context_lens,
+                                          nrows, num_q_heads, partition_size, max_partitions, o)
+                     : cudaLaunchKernelEx(&cfg, reduce_kernel<64, 1>, ws_o, ws_m, ws_l, context_lens,
+                                          nrows, num_q_heads, partition_size, max_partitions, o);
+    return cuda_check(e, "reduce launch");
 }
 
 }  // namespace pa

@@ -27,6 +27,14 @@ CONFIGS = [
 ]
 
 
+def _bench_launches():
+    import bench
+    return [(name, bs, ps) for name, (bs, ps) in bench.DEFAULT_LAUNCH.items() if name != "tiny"]
+
+
+CONFIGS += [c for c in _bench_launches() if c not in CONFIGS]
+
+
 @pytest.fixture(scope="module")
 def api(cuda_device):
     from paged_kv_cache_193_gb300 import api as a

@@ -50,22 +50,23 @@ def _oracle_step(oracle, wl, partition_size=0):
     return slots, kc, vc, out
 
 
-def _gpu_step(api, wl, partition_size):
+def _gpu_step(api, wl, partition_size, fused=True):
     bt, cl = device_tables(wl, wl.k_cache.device)
     step = api.DecodeStep(wl.k_cache, wl.v_cache, bt, cl, wl.shape.num_q_heads,
-                          wl.softmax_scale, wl.kv_scale, partition_size)
+                          wl.softmax_scale, wl.kv_scale, partition_size, fused=fused)
     out = step(wl.q, wl.k_new, wl.v_new).clone()
     torch.cuda.synchronize()
     return step.slots.cpu().numpy(), out
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "separate"])
 @pytest.mark.parametrize("partition_size", [0, 16, 32, 64, 512])
-def test_tiny_step_matches_oracle(api, oracle, cuda_device, partition_size):
+def test_tiny_step_matches_oracle(api, oracle, cuda_device, partition_size, fused):
     wl = W.make("tiny", device=cuda_device)
     W.poison(wl, pending=True)
     api.device_errors(clear=True)
     slots_ref, kc_ref, vc_ref, out_ref = _oracle_step(oracle, wl)
-    slots, out = _gpu_step(api, wl, partition_size)
+    slots, out = _gpu_step(api, wl, partition_size, fused)
     assert np.array_equal(slots, slots_ref)
     assert np.array_equal(W.bits(wl.k_cache), kc_ref)
     assert np.array_equal(W.bits(wl.v_cache), vc_ref)
@@ -88,8 +89,10 @@ def test_shapes_match_oracle(api, oracle, cuda_device, D, B, G, Hkv, kv):
                       cuda_device)
     W.poison(wl, pending=True)
     slots_ref, kc_ref, vc_ref, out_ref = _oracle_step(oracle, wl)
-    for ps in (0, 4 * B, 256):
-        slots, out = _gpu_step(api, wl, ps)
+    for ps, fused in ((0, True), (4 * B, True), (256, False), (0, False)):
+        # poison the pending slots again so each call's append is checked
+        W.poison(wl, pending=True)
+        slots, out = _gpu_step(api, wl, ps, fused)
         assert np.array_equal(slots, slots_ref)
         assert np.array_equal(W.bits(wl.k_cache), kc_ref)
         assert np.array_equal(W.bits(wl.v_cache), vc_ref)
