@@ -69,6 +69,8 @@ def parse():
     ap.add_argument("--block-size", type=int, default=None)
     ap.add_argument("--partition-size", type=int, default=None)
     ap.add_argument("--num-seqs", type=int, default=None, help="shrink the workload (profiling)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="store the workload's KV cache as E4M3 (one per-tensor scale)")
     ap.add_argument("--separate", action="store_true",
                     help="time the unfused entry points (3-4 kernels per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -180,6 +182,9 @@ def build_workload(args, device):
     bs = args.block_size or bs
     ps = ps if args.partition_size is None else args.partition_size
     wl = W.make(args.config, device=device, block_size=bs, num_seqs=args.num_seqs)
+    if args.fp8 and wl.shape.kv_dtype != W.KV_FP8_E4M3:
+        wl.shape.kv_dtype = W.KV_FP8_E4M3
+        wl.kv_scale = W.fp8_scale_from(wl.k_cache, wl.v_cache, wl.k_new, wl.v_new)
     return wl, ps
 
 

@@ -336,10 +336,9 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
                     const uint4 &B = rb[kk / 4];
                     const uint32_t wa = (kk % 4 == 0) ? A.x : (kk % 4 == 1) ? A.y : (kk % 4 == 2) ? A.z : A.w;
                     const uint32_t wb = (kk % 4 == 0) ? B.x : (kk % 4 == 1) ? B.y : (kk % 4 == 2) ? B.z : B.w;
-                    const uint32_t a0 = e4m3x2_to_f16x2(wa & 0xFFFFu);
-                    const uint32_t a1 = e4m3x2_to_f16x2(wb & 0xFFFFu);
-                    const uint32_t a2 = e4m3x2_to_f16x2(wa >> 16);
-                    const uint32_t a3 = e4m3x2_to_f16x2(wb >> 16);
+                    uint32_t a0, a1, a2, a3;
+                    e4m3x4_to_f16x2x2(wa, a0, a2);  // row t0: k = 2c,2c+1 | 2c+8,2c+9
+                    e4m3x4_to_f16x2x2(wb, a1, a3);  // row t1
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
                         mma16816<true>(sc[mt][nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
@@ -424,12 +423,9 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
 #pragma unroll
                     for (int mu = 0; mu < 2; ++mu) {
                         const uint32_t sel = mu ? 0x7362u : 0x5140u;
-                        const uint32_t lo = __byte_perm(w0, w1, sel);
-                        const uint32_t hi = __byte_perm(w2, w3, sel);
-                        const uint32_t a0 = e4m3x2_to_f16x2(lo & 0xFFFFu);
-                        const uint32_t a1 = e4m3x2_to_f16x2(lo >> 16);
-                        const uint32_t a2 = e4m3x2_to_f16x2(hi & 0xFFFFu);
-                        const uint32_t a3 = e4m3x2_to_f16x2(hi >> 16);
+                        uint32_t a0, a1, a2, a3;
+                        e4m3x4_to_f16x2x2(__byte_perm(w0, w1, sel), a0, a1);
+                        e4m3x4_to_f16x2x2(__byte_perm(w2, w3, sel), a2, a3);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
                             mma16816<true>(o[gi * 2 + mu][nt], a0, a1, a2, a3, pb[mt][nt][0],

@@ -186,11 +186,17 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
     }
 }
 
-// Two E4M3 bytes (low byte first) -> two fp16 in one register (exact).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-        static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xFFFFu), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Four E4M3 bytes b0..b3 of a word (b0 lowest) -> two fp16x2 registers:
+// lo = {b0, b1}, hi = {b2, b3}, low half first.  Exact (every E4M3 value is
+// an fp16 value).  The conversion reads the two 16-bit halves of the word
+// directly, so no masking or shifting is needed.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 template <bool F16>
