@@ -71,6 +71,10 @@ def parse():
     ap.add_argument("--num-seqs", type=int, default=None, help="shrink the workload (profiling)")
     ap.add_argument("--fp8", action="store_true",
                     help="store the workload's KV cache as E4M3 (one per-tensor scale)")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay the step(s) from one CUDA graph instead of launching eagerly")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="attention layers per step, each with its own KV cache")
     ap.add_argument("--separate", action="store_true",
                     help="time the unfused entry points (3-4 kernels per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -177,11 +181,12 @@ class ClockSampler:
 # workload
 # --------------------------------------------------------------------------
 
-def build_workload(args, device):
+def build_workload(args, device, data_seed=None):
     bs, ps = DEFAULT_LAUNCH[args.config]
     bs = args.block_size or bs
     ps = ps if args.partition_size is None else args.partition_size
-    wl = W.make(args.config, device=device, block_size=bs, num_seqs=args.num_seqs)
+    wl = W.make(args.config, device=device, block_size=bs, num_seqs=args.num_seqs,
+                data_seed=data_seed)
     if args.fp8 and wl.shape.kv_dtype != W.KV_FP8_E4M3:
         wl.shape.kv_dtype = W.KV_FP8_E4M3
         wl.kv_scale = W.fp8_scale_from(wl.k_cache, wl.v_cache, wl.k_new, wl.v_new)
@@ -215,7 +220,7 @@ def config_of(wl, ps, args):
         "kv_dtype": "bf16" if sh.kv_dtype == W.KV_BF16 else "fp8_e4m3",
         "mean_context": float(np.mean(wl.context_lens)), "num_blocks": wl.num_blocks,
         "kv_bytes_per_step": wl.kv_bytes(), "unique_kv_bytes_per_step": wl.unique_kv_bytes(),
-        "seed": wl.seed, "parallelism": "replicas",
+        "seed": wl.seed, "parallelism": "replicas", "layers": args.layers,
         "l2": f"inputs larger than L2: KV pool {pool_gb:.2f} GB vs 129 MB L2"
               + ("; the shared prefix is L2-resident by design" if wl.name == "prefix_fp8" else ""),
     }
@@ -333,15 +338,31 @@ def run_ours(args):
     from paged_kv_cache_193_gb300 import api
 
     wl, ps = build_workload(args, device)
-    if wl.shape.kv_dtype == W.KV_FP8_E4M3:
-        quantize_fp8_pool(api, wl)
+    # further layers share the contexts and block tables, with their own values
+    layers = [wl] + [build_workload(args, device, data_seed=wl.seed + 1000 * i)[0]
+                     for i in range(1, args.layers)]
+    steps, inputs = [], []
+    for lw in layers:
+        if lw.shape.kv_dtype == W.KV_FP8_E4M3:
+            quantize_fp8_pool(api, lw)
+        lbt = torch.from_numpy(lw.block_tables).to(device)
+        lcl = torch.from_numpy(lw.context_lens).to(device)
+        steps.append(api.DecodeStep(lw.k_cache, lw.v_cache, lbt, lcl, lw.shape.num_q_heads,
+                                    lw.softmax_scale, lw.kv_scale, ps, fused=not args.separate))
+        inputs.append((lw.q, lw.k_new, lw.v_new))
     sh = wl.shape
-    bt = torch.from_numpy(wl.block_tables).to(device)
-    cl = torch.from_numpy(wl.context_lens).to(device)
-    step = api.DecodeStep(wl.k_cache, wl.v_cache, bt, cl, sh.num_q_heads, wl.softmax_scale,
-                          wl.kv_scale, ps, fused=not args.separate)
+    step = steps[0]
+    bt, cl = step.block_tables, step.context_lens
     stream = torch.cuda.current_stream()
-    launches_per_step = step.launches()
+    if args.graph:
+        graph = api.StepGraph(steps, inputs)
+        run_step = graph.replay
+        launches_per_step = graph.launches()
+    else:
+        def run_step():
+            for st, (q, k, v) in zip(steps, inputs):
+                st(q, k, v)
+        launches_per_step = sum(st.launches() for st in steps)
 
     # warm-up: at least W steps and at least --min-warmup-seconds of load
     clocks = ClockSampler(local)
@@ -350,7 +371,7 @@ def run_ours(args):
     t_w = time.time()
     done = 0
     while done < args.warmup or time.time() - t_w < args.min_warmup_seconds:
-        step(wl.q, wl.k_new, wl.v_new)
+        run_step()
         done += 1
         if done % 50 == 0:
             torch.cuda.synchronize()
@@ -368,7 +389,7 @@ def run_ours(args):
     start.record(stream)
     for i in range(K):
         ev[i][0].record(stream)
-        step(wl.q, wl.k_new, wl.v_new)
+        run_step()
         ev[i][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
@@ -384,14 +405,16 @@ def run_ours(args):
     # merge one launch each with events between them (this breaks the
     # overlap of the merge's launch with the attention tail, so it is kept
     # out of the timed steps).
-    if ps == 0 and step.fused:
+    if ps == 0 and step.fused and len(steps) == 1:
         dec_ms, red_ms, kname = float(np.mean(t_step)), 0.0, "decode_kernel (fused step)"
     else:
         n2 = min(K, 200)
         e = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n2)]
         for i in range(n2):
             e[i][0].record(stream)
-            if ps:
+            if ps == 0 and step.fused:
+                step(wl.q, wl.k_new, wl.v_new)
+            elif ps:
                 api.decode_partitions(wl.q, wl.k_cache, wl.v_cache, bt, cl, wl.softmax_scale,
                                       wl.kv_scale, ps, step.workspace)
             else:
@@ -408,12 +431,12 @@ def run_ours(args):
         kname = "decode_kernel (per-partition attention)" if ps else "decode_kernel"
     clocks.stop()
 
-    kv = wl.kv_bytes()
+    kv = sum(lw.kv_bytes() for lw in layers)
     ms_per_step = total_ms / K
     value = world * kv * K / (total_ms / 1e3) / 1e9
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", 6800.0))
-    achieved = kv / (dec_ms / 1e3) / 1e9
+    achieved = wl.kv_bytes() / (dec_ms / 1e3) / 1e9
     traffic = recorded_traffic(wl, ps)
 
     result = {
@@ -424,6 +447,7 @@ def run_ours(args):
         "data": "synthetic (seeded N(0,1) bf16, shuffled block tables)",
         "config": config_of(wl, ps, args),
         "tokens_per_s": round(world * sh.num_seqs * K / (total_ms / 1e3), 1),
+        "layers_per_step": len(layers), "launch": "one CUDA graph per step" if args.graph else "eager",
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         f"pct_of_{peak_kind}_hbm": round(100 * value / world / hbm, 2),
         "breakdown_ms": {"step_median": round(float(np.median(t_step)), 5),
@@ -438,11 +462,11 @@ def run_ours(args):
                      "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "algorithmic_bytes_per_launch": kv, "traffic": traffic},
+                     "algorithmic_bytes_per_launch": wl.kv_bytes(), "traffic": traffic},
     }
     result["clocks"] = clocks.summary(t_wall0 - 1.0, t_wall1)
 
-    if not args.no_e2e:
+    if not args.no_e2e and len(layers) == 1:
         result["e2e"] = run_e2e(api, wl, step, ps, K, world, device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)

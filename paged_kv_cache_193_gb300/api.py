@@ -284,3 +284,41 @@ class DecodeStep:
                                self.partition_size, self.workspace, self.slots, self.out, stream)
         self.append(k_new, v_new, stream)
         return self.attend(q, stream)
+
+
+class StepGraph:
+    """Several layers' decode steps captured into one CUDA graph.
+
+    ``steps`` are ``DecodeStep`` objects (one per attention layer, each with
+    its own cache) and ``inputs`` the matching ``(q, k_new, v_new)`` device
+    buffers.  ``replay()`` re-runs every step with whatever those buffers, the
+    context lengths and the block tables hold at that moment; nothing is
+    re-encoded on the host, so the per-step host cost is one graph launch.
+    One eager pass runs first (outside the capture) so that the library's
+    once-per-device set-up never happens while a stream is being captured.
+    """
+
+    def __init__(self, steps, inputs):
+        if len(steps) != len(inputs):
+            raise ValueError("one (q, k_new, v_new) triple per step")
+        self.steps = list(steps)
+        self.inputs = list(inputs)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self._run()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._run()
+
+    def _run(self):
+        for step, (q, k, v) in zip(self.steps, self.inputs):
+            step(q, k, v)
+
+    def launches(self) -> int:
+        return sum(s.launches() for s in self.steps)
+
+    def replay(self) -> None:
+        self.graph.replay()

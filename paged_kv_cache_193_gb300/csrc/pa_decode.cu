@@ -31,6 +31,8 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "pa_device.cuh"
 
 namespace pa {
@@ -609,10 +611,19 @@ static pa_status launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, con
     constexpr int SPW = stages_per_warp<D, BS, FP8>();
     using C = Cfg<D, BS, FP8, NT, kWarps, SPW>;
     auto kern = decode_kernel<D, BS, FP8, NT, kWarps, SPW>;
-    pa_status st = cuda_check(
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM),
-        "cudaFuncSetAttribute(decode)");
+    // Raise the kernel's shared-memory limit once per device (the first call
+    // on a device should precede any stream capture).
+    static std::atomic<uint64_t> raised{0};
+    int dev = 0;
+    pa_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
     if (st != PA_OK) return st;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+    if (!bit || !(raised.load(std::memory_order_acquire) & bit)) {
+        st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM),
+                        "cudaFuncSetAttribute(decode)");
+        if (st != PA_OK) return st;
+        raised.fetch_or(bit, std::memory_order_release);
+    }
     kern<<<grid, kWarps * 32, C::SMEM, stream>>>(tk, tv, a);
     return cuda_check(cudaGetLastError(), "decode launch");
 }

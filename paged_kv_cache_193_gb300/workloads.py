@@ -259,28 +259,32 @@ def _finish(name, shape, ctx, tables, nb, device, seed, gen_device=None, kv_scal
 
 
 def make(name: str, device="cpu", seed: int | None = None, block_size: int | None = None,
-         num_seqs: int | None = None, fill_cache: bool = True, extra_steps: int = 0) -> Workload:
+         num_seqs: int | None = None, fill_cache: bool = True, extra_steps: int = 0,
+         data_seed: int | None = None) -> Workload:
     """Build workload ``name`` (see the module docstring).  ``num_seqs``
     shrinks a workload (same distributions) for quick tests or profiling;
     ``extra_steps`` reserves table capacity and pool blocks for that many more
-    appended tokens per sequence (the long-context step workload)."""
+    appended tokens per sequence (the long-context step workload).
+    ``data_seed`` (default: ``seed``) seeds the values only, so several
+    layers can share one set of contexts and block tables."""
     idx = NAMES.index(name)
     seed = idx if seed is None else seed
     rng = np.random.default_rng(seed)
+    vseed = seed if data_seed is None else data_seed
     if name == "tiny":
         shape = Shape(num_seqs or 4, 8, 2, 64, block_size or 16)
         ctx = np.array([1, 17, 100, 255], np.int64)[: shape.num_seqs]
         nb = 64
         tables, _ = build_tables(ctx, shape.block_size, nb, rng)
-        return _finish(name, shape, ctx, tables, nb, device, seed, fill_cache=fill_cache)
+        return _finish(name, shape, ctx, tables, nb, device, vseed, fill_cache=fill_cache)
     if name == "llama8b":
         shape = Shape(num_seqs or 256, 32, 8, 128, block_size or 16)
         ctx = rng.integers(512, 2048, size=shape.num_seqs, endpoint=True)
-        mb = _blocks_for(2048, shape.block_size)
+        mb = _blocks_for(2048 + extra_steps, shape.block_size)
     elif name == "long70b":
         shape = Shape(num_seqs or 64, 64, 8, 128, block_size or 16, partition_size=512)
         ctx = rng.integers(4096, 32768, size=shape.num_seqs, endpoint=True)
-        mb = _blocks_for(32768, shape.block_size)
+        mb = _blocks_for(32768 + extra_steps, shape.block_size)
     elif name == "prefix_fp8":
         shape = Shape(num_seqs or 256, 32, 8, 128, block_size or 16, kv_dtype=KV_FP8_E4M3)
         prefix = 2048
@@ -291,7 +295,7 @@ def make(name: str, device="cpu", seed: int | None = None, block_size: int | Non
         need = pb + sum(_blocks_for(int(c), shape.block_size) - pb for c in ctx)
         nb = math.ceil(1.2 * need)
         tables, _ = build_tables(ctx, shape.block_size, nb, rng, mb, shared_prefix_blocks=pb)
-        wl = _finish(name, shape, ctx, tables, nb, device, seed, gen_device=device,
+        wl = _finish(name, shape, ctx, tables, nb, device, vseed, gen_device=device,
                      fill_cache=fill_cache)
         wl.notes["shared_prefix_tokens"] = prefix
         return wl
@@ -304,7 +308,7 @@ def make(name: str, device="cpu", seed: int | None = None, block_size: int | Non
     need = sum(_blocks_for(int(c) + extra_steps, shape.block_size) for c in ctx)
     nb = math.ceil(1.2 * need)
     tables, alloc = build_tables(ctx, shape.block_size, nb, rng, mb)
-    wl = _finish(name, shape, ctx, tables, nb, device, seed, fill_cache=fill_cache)
+    wl = _finish(name, shape, ctx, tables, nb, device, vseed, fill_cache=fill_cache)
     wl.notes["allocator"] = alloc
     return wl
 
