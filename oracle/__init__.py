@@ -57,6 +57,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
                                                 I, I, P, P, P]
     lib.pa_oracle_merge_partitions.restype = None
     lib.pa_oracle_merge_partitions.argtypes = [P, P, P, P, I, I, I, I, I, P]
+    lib.pa_oracle_cache_append_scaled.restype = None
+    lib.pa_oracle_cache_append_scaled.argtypes = [P, P, P, I, P, P, I, I, I, P, P]
+    lib.pa_oracle_decode_scaled.restype = None
+    lib.pa_oracle_decode_scaled.argtypes = [P, P, P, P, I, P, I, I, I, I, I, D, P, P, P, I, P]
     lib.pa_oracle_set_threads.restype = None
     lib.pa_oracle_set_threads.argtypes = [I]
     lib.pa_oracle_get_threads.restype = I
@@ -181,6 +185,47 @@ class Oracle:
         out = np.zeros((S, Hq, D), np.float64)
         self.lib.pa_oracle_merge_partitions(_p(o), _p(m), _p(l), _p(cl), S, Hq, D,
                                             partition_size, P, _p(out))
+        return out
+
+    # -- E4M3 with per-head K and V scales ---------------------------------------
+    def cache_append_scaled(self, k_bits, v_bits, slot_mapping, k_cache, v_cache, block_size,
+                            k_scales, v_scales) -> None:
+        """In-place E4M3 append with scale k_scales[h] / v_scales[h] per KV head."""
+        k = _c(k_bits, np.uint16)
+        v = _c(v_bits, np.uint16)
+        sm = _c(slot_mapping, np.int32)
+        ks = _c(k_scales, np.float32)
+        vs = _c(v_scales, np.float32)
+        assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+        assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+        T, Hkv, D = k.shape
+        assert ks.shape == (Hkv,) and vs.shape == (Hkv,)
+        self.lib.pa_oracle_cache_append_scaled(_p(k), _p(v), _p(sm), T, _p(k_cache), _p(v_cache),
+                                               Hkv, D, block_size, _p(ks), _p(vs))
+
+    def decode_scaled(self, q_bits, k_cache, v_cache, block_tables, context_lens, num_kv_heads,
+                      block_size, softmax_scale, k_scales, v_scales, pairs=None) -> np.ndarray:
+        """fp64 attention over an E4M3 cache with per-head scales: [S, Hq, D],
+        or [n, D] for the given (sequence, query head) pairs."""
+        q = _c(q_bits, np.uint16)
+        bt = _c(block_tables, np.int32)
+        cl = _c(context_lens, np.int32)
+        kc = np.ascontiguousarray(k_cache, dtype=np.uint8)
+        vc = np.ascontiguousarray(v_cache, dtype=np.uint8)
+        ks = _c(k_scales, np.float32)
+        vs = _c(v_scales, np.float32)
+        S, Hq, D = q.shape
+        if pairs is None:
+            out = np.zeros((S, Hq, D), np.float64)
+            self.lib.pa_oracle_decode_scaled(_p(q), _p(kc), _p(vc), _p(bt), bt.shape[1], _p(cl), S,
+                                             Hq, num_kv_heads, D, block_size, float(softmax_scale),
+                                             _p(ks), _p(vs), None, 0, _p(out))
+            return out
+        pr = _c(pairs, np.int32).reshape(-1, 2)
+        out = np.zeros((pr.shape[0], D), np.float64)
+        self.lib.pa_oracle_decode_scaled(_p(q), _p(kc), _p(vc), _p(bt), bt.shape[1], _p(cl), S, Hq,
+                                         num_kv_heads, D, block_size, float(softmax_scale), _p(ks),
+                                         _p(vs), _p(pr), pr.shape[0], _p(out))
         return out
 
     # -- threads -------------------------------------------------------------

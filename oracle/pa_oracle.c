@@ -205,7 +205,7 @@ static int64_t token_index(const int32_t *block_tables, int max_blocks_per_seq,
 static void attend_range(const uint16_t *q_row, const void *k_cache, const void *v_cache,
                          const int32_t *block_tables, int max_blocks_per_seq, int s, int kvh,
                          int t_begin, int t_end, int num_kv_heads, int head_dim, int block_size,
-                         double softmax_scale, int kv_dtype, double kv_scale,
+                         double softmax_scale, int kv_dtype, double k_scale, double v_scale,
                          double *x, double *o, double *m_out, double *l_out)
 {
     int n = t_end - t_begin;
@@ -223,7 +223,7 @@ static void attend_range(const uint16_t *q_row, const void *k_cache, const void 
         for (int d = 0; d < head_dim; ++d) {
             int64_t idx = token_index(block_tables, max_blocks_per_seq, s, t, kvh, d,
                                       num_kv_heads, head_dim, block_size);
-            dot += pa_oracle_bf16_to_double(q_row[d]) * cache_value(k_cache, idx, kv_dtype, kv_scale);
+            dot += pa_oracle_bf16_to_double(q_row[d]) * cache_value(k_cache, idx, kv_dtype, k_scale);
         }
         x[i] = softmax_scale * dot;
     }
@@ -244,7 +244,7 @@ static void attend_range(const uint16_t *q_row, const void *k_cache, const void 
         for (int d = 0; d < head_dim; ++d) {
             int64_t idx = token_index(block_tables, max_blocks_per_seq, s, t, kvh, d,
                                       num_kv_heads, head_dim, block_size);
-            o[d] += p * cache_value(v_cache, idx, kv_dtype, kv_scale);
+            o[d] += p * cache_value(v_cache, idx, kv_dtype, v_scale);
         }
     }
     *m_out = m;
@@ -281,7 +281,8 @@ void pa_oracle_decode(const uint16_t *q, const void *k_cache, const void *v_cach
                 attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,
                              block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s],
                              num_kv_heads, head_dim, block_size, softmax_scale, kv_dtype,
-                             kv_scale, x, out + ((int64_t)s * num_q_heads + hq) * head_dim, &m, &l);
+                             kv_scale, kv_scale, x, out + ((int64_t)s * num_q_heads + hq) * head_dim,
+                             &m, &l);
             }
         }
         free(x);
@@ -307,7 +308,7 @@ void pa_oracle_decode_pairs(const uint16_t *q, const void *k_cache, const void *
         double m, l;
         attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,
                      block_tables, max_blocks_per_seq, s, hq / group, 0, n, num_kv_heads,
-                     head_dim, block_size, softmax_scale, kv_dtype, kv_scale, x,
+                     head_dim, block_size, softmax_scale, kv_dtype, kv_scale, kv_scale, x,
                      out + (int64_t)i * head_dim, &m, &l);
         free(x);
     }
@@ -341,7 +342,8 @@ void pa_oracle_decode_partitions(const uint16_t *q, const void *k_cache, const v
                     attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache,
                                  v_cache, block_tables, max_blocks_per_seq, s, hq / group, t0,
                                  t1, num_kv_heads, head_dim, block_size, softmax_scale,
-                                 kv_dtype, kv_scale, x, o + row * head_dim, &m[row], &l[row]);
+                                 kv_dtype, kv_scale, kv_scale, x, o + row * head_dim, &m[row],
+                                 &l[row]);
                 }
             }
         }
@@ -382,6 +384,68 @@ void pa_oracle_merge_partitions(const float *o, const float *m, const float *l,
                     dst[d] += w * (double)o[(base + p) * head_dim + d];
             }
         }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* E4M3 cache with a scale per KV head for K and for V                        */
+/* ------------------------------------------------------------------------ */
+
+/* The tuning guide's FP8 KV passage (Step 3) fixes no scale granularity.
+ * This variant gives every KV head h its own scales: K elements of head h
+ * are stored as e4m3(float(x) / k_scales[h]) and read back as
+ * e4m3(b) * k_scales[h]; V likewise with v_scales[h].  One scale for the
+ * whole cache is the case where every entry is equal. */
+void pa_oracle_cache_append_scaled(const uint16_t *k, const uint16_t *v,
+                                   const int32_t *slot_mapping, int num_tokens,
+                                   uint8_t *k_cache, uint8_t *v_cache, int num_kv_heads,
+                                   int head_dim, int block_size, const float *k_scales,
+                                   const float *v_scales)
+{
+    for (int i = 0; i < num_tokens; ++i) {
+        int32_t slot = slot_mapping[i];
+        if (slot < 0)
+            continue;
+        int64_t block = slot / block_size;
+        int64_t off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            for (int d = 0; d < head_dim; ++d) {
+                int64_t src = ((int64_t)i * num_kv_heads + h) * head_dim + d;
+                int64_t dst = ((block * num_kv_heads + h) * block_size + off) * head_dim + d;
+                float kf = (float)pa_oracle_bf16_to_double(k[src]);
+                float vf = (float)pa_oracle_bf16_to_double(v[src]);
+                k_cache[dst] = pa_oracle_e4m3_from_float(kf / k_scales[h]);
+                v_cache[dst] = pa_oracle_e4m3_from_float(vf / v_scales[h]);
+            }
+        }
+    }
+}
+
+/* Decode attention over an E4M3 cache with per-head K and V scales, for the
+ * listed (sequence, query head) pairs (all pairs when pairs is NULL, in
+ * [S][Hq] order).  out is fp64 [n][D]. */
+void pa_oracle_decode_scaled(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                             const int32_t *block_tables, int max_blocks_per_seq,
+                             const int32_t *context_lens, int num_seqs, int num_q_heads,
+                             int num_kv_heads, int head_dim, int block_size,
+                             double softmax_scale, const float *k_scales, const float *v_scales,
+                             const int32_t *pairs, int n_pairs, double *out)
+{
+    int group = num_q_heads / num_kv_heads;
+    int n = pairs ? n_pairs : num_seqs * num_q_heads;
+#pragma omp parallel for schedule(dynamic)
+    for (int i = 0; i < n; ++i) {
+        int s = pairs ? pairs[2 * i] : i / num_q_heads;
+        int hq = pairs ? pairs[2 * i + 1] : i % num_q_heads;
+        int kvh = hq / group;
+        int len = context_lens[s];
+        double *x = (double *)malloc(sizeof(double) * (size_t)(len > 0 ? len : 1));
+        double m, l;
+        attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,
+                     block_tables, max_blocks_per_seq, s, kvh, 0, len, num_kv_heads, head_dim,
+                     block_size, softmax_scale, 1, (double)k_scales[kvh], (double)v_scales[kvh],
+                     x, out + (int64_t)i * head_dim, &m, &l);
+        free(x);
     }
 }
 

@@ -271,7 +271,55 @@ def pin_partition_merge(o):
             assert np.array_equal(po[:, :, 0, :], full)
 
 
+def pin_fp8_per_head_scales(o):
+    """E4M3 cache with a different scale per KV head and for K vs V: the
+    oracle's attention equals torch SDPA over values decoded by torch's
+    float8_e4m3fn and multiplied by each head's own scale; the appended codes
+    are the per-head encodings, and equal scales reduce to the one-scale
+    append."""
+    rng = np.random.default_rng(14)
+    c = _case(Hq=12, Hkv=3, seed=41)
+    B = 16
+    tables, _, _ = c.paged(B, 30, rng)
+    ks = np.array([0.011, 0.023, 0.007], np.float32)
+    vs = np.array([0.019, 0.005, 0.031], np.float32)
+    kc = np.full((30, c.Hkv, B, c.D), 0x7F, np.uint8)
+    vc = np.full_like(kc, 0x7F)
+    for s_, n in enumerate(c.ctx):
+        slots = np.array([tables[s_, t // B] * B + t % B for t in range(n)], np.int32)
+        o.cache_append_scaled(c.k[s_].transpose(1, 0, 2), c.v[s_].transpose(1, 0, 2), slots,
+                              kc, vc, B, ks, vs)
+    codes_k, codes_v = [], []
+    for s_, n in enumerate(c.ctx):
+        ck = np.zeros((c.Hkv, n, c.D), np.uint8)
+        cv = np.zeros_like(ck)
+        for t in range(n):
+            ck[:, t] = kc[tables[s_, t // B], :, t % B]
+            cv[:, t] = vc[tables[s_, t // B], :, t % B]
+        for h in range(c.Hkv):
+            for d in (0, 5, c.D - 1):
+                assert ck[h, 0, d] == _byte(o, c.k[s_][h, 0, d], ks[h])
+                assert cv[h, 0, d] == _byte(o, c.v[s_][h, 0, d], vs[h])
+        codes_k.append(ck)
+        codes_v.append(cv)
+    out = o.decode_scaled(c.q, kc, vc, tables, np.array(c.ctx), c.Hkv, B, 0.21, ks, vs)
+    c.k, c.v = codes_k, codes_v
+    ref = c.sdpa(0.21, deq_k=lambda a: _e4m3_torch(a) * ks[:, None, None].astype(np.float64),
+                 deq_v=lambda a: _e4m3_torch(a) * vs[:, None, None].astype(np.float64))
+    assert np.abs(out - ref).max() < 1e-12, np.abs(out - ref).max()
+    # one scale everywhere: the per-head functions agree with the one-scale ones
+    same = np.full(c.Hkv, 0.013, np.float32)
+    k1 = np.zeros((8, c.Hkv, B, c.D), np.uint8)
+    v1, k2, v2 = k1.copy(), k1.copy(), k1.copy()
+    kb = (np.arange(3 * c.Hkv * c.D, dtype=np.uint32) * 2654435761 % 65535).astype(np.uint16)
+    kb = kb.reshape(3, c.Hkv, c.D) & 0x7FFF  # finite patterns only
+    sl = np.array([1, 17, 40], np.int32)
+    o.cache_append_scaled(kb, kb, sl, k1, v1, B, same, same)
+    o.cache_append(kb, kb, sl, k2, v2, B, 1, float(same[0]))
+    assert np.array_equal(k1, k2) and np.array_equal(v1, v2)
+
+
 ALL = [pin_kv_formula, pin_e4m3_decode, pin_e4m3_encode, pin_e4m3_roundtrip, pin_attention_sdpa,
        pin_attention_fp8, pin_extreme_scores, pin_permutation, pin_prefix_sharing, pin_context_one,
        pin_identical_keys, pin_empty_context, pin_slot_mapping, pin_append_readback,
-       pin_partition_merge]
+       pin_partition_merge, pin_fp8_per_head_scales]

@@ -27,6 +27,10 @@ MUTANTS = {
     "append_block_offset_swapped": ("int64_t block = slot / block_size;\n        int64_t off = slot % block_size;",
                                     "int64_t block = slot % block_size;\n        int64_t off = slot / block_size;"),
     "merge_drops_l": ("total += (double)l[base + p] * exp(", "total += exp("),
+    "scaled_kv_swapped": ("(double)k_scales[kvh], (double)v_scales[kvh]",
+                          "(double)v_scales[kvh], (double)k_scales[kvh]"),
+    "scaled_head_ignored": ("k_cache[dst] = pa_oracle_e4m3_from_float(kf / k_scales[h]);",
+                            "k_cache[dst] = pa_oracle_e4m3_from_float(kf / k_scales[0]);"),
     "partition_short": ("int t1 = t0 + partition_size;", "int t1 = t0 + partition_size - 1;"),
     "last_token_dropped": ("attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s],",
                            "attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s] - (context_lens[s] > 1),"),
