@@ -75,6 +75,8 @@ def parse():
                     help="replay the step(s) from one CUDA graph instead of launching eagerly")
     ap.add_argument("--layers", type=int, default=1,
                     help="attention layers per step, each with its own KV cache")
+    ap.add_argument("--per-head-scales", action="store_true",
+                    help="E4M3 cache with its own K and V scale per KV head")
     ap.add_argument("--separate", action="store_true",
                     help="time the unfused entry points (3-4 kernels per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -210,6 +212,22 @@ def quantize_fp8_pool(api, wl):
     wl.k_cache, wl.v_cache = kc, vc
 
 
+def quantize_fp8_pool_scaled(api, wl, k_scales, v_scales):
+    """As quantize_fp8_pool, with the library's per-head-scale append."""
+    NB, Hkv, B, D = wl.k_cache.shape
+    wl.notes["bf16_pool"] = (wl.k_cache, wl.v_cache)
+    kc = torch.empty((NB, Hkv, B, D), dtype=torch.uint8, device=wl.k_cache.device)
+    vc = torch.empty_like(kc)
+    chunk = max(1, (1 << 20) // B)
+    for b0 in range(0, NB, chunk):
+        b1 = min(NB, b0 + chunk)
+        ksrc = wl.k_cache[b0:b1].permute(0, 2, 1, 3).reshape(-1, Hkv, D).contiguous()
+        vsrc = wl.v_cache[b0:b1].permute(0, 2, 1, 3).reshape(-1, Hkv, D).contiguous()
+        slots = torch.arange(b0 * B, b1 * B, dtype=torch.int32, device=kc.device)
+        api.cache_append_scaled(ksrc, vsrc, slots, kc, vc, k_scales, v_scales)
+    wl.k_cache, wl.v_cache = kc, vc
+
+
 def config_of(wl, ps, args):
     sh = wl.shape
     pool_gb = (wl.k_cache.numel() * wl.k_cache.element_size() * 2) / 1e9
@@ -217,7 +235,9 @@ def config_of(wl, ps, args):
         "workload": f"{wl.name}: {DESCRIPTION[wl.name]}",
         "num_seqs": sh.num_seqs, "num_q_heads": sh.num_q_heads, "num_kv_heads": sh.num_kv_heads,
         "head_dim": sh.head_dim, "block_size": sh.block_size, "partition_size": ps,
-        "kv_dtype": "bf16" if sh.kv_dtype == W.KV_BF16 else "fp8_e4m3",
+        "kv_dtype": "bf16" if sh.kv_dtype == W.KV_BF16 else
+                    ("fp8_e4m3, K and V scale per KV head" if args.per_head_scales else
+                     "fp8_e4m3, one scale"),
         "mean_context": float(np.mean(wl.context_lens)), "num_blocks": wl.num_blocks,
         "kv_bytes_per_step": wl.kv_bytes(), "unique_kv_bytes_per_step": wl.unique_kv_bytes(),
         "seed": wl.seed, "parallelism": "replicas", "layers": args.layers,
@@ -343,12 +363,21 @@ def run_ours(args):
                      for i in range(1, args.layers)]
     steps, inputs = [], []
     for lw in layers:
-        if lw.shape.kv_dtype == W.KV_FP8_E4M3:
+        ks = vs = None
+        if args.per_head_scales:
+            if lw.shape.kv_dtype != W.KV_FP8_E4M3:
+                raise SystemExit("--per-head-scales needs an E4M3 cache (--fp8 or prefix_fp8)")
+            # amax / 448 per KV head, for K and V separately
+            ks = (lw.k_cache.float().abs().amax(dim=(0, 2, 3)) / 448.0).contiguous()
+            vs = (lw.v_cache.float().abs().amax(dim=(0, 2, 3)) / 448.0).contiguous()
+            quantize_fp8_pool_scaled(api, lw, ks, vs)
+        elif lw.shape.kv_dtype == W.KV_FP8_E4M3:
             quantize_fp8_pool(api, lw)
         lbt = torch.from_numpy(lw.block_tables).to(device)
         lcl = torch.from_numpy(lw.context_lens).to(device)
         steps.append(api.DecodeStep(lw.k_cache, lw.v_cache, lbt, lcl, lw.shape.num_q_heads,
-                                    lw.softmax_scale, lw.kv_scale, ps, fused=not args.separate))
+                                    lw.softmax_scale, lw.kv_scale, ps, fused=not args.separate,
+                                    k_scales=ks, v_scales=vs))
         inputs.append((lw.q, lw.k_new, lw.v_new))
     sh = wl.shape
     step = steps[0]

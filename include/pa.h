@@ -218,6 +218,33 @@ pa_status pa_decode_step(const void *q, const void *k_new, const void *v_new, vo
                          int32_t *slot_mapping, void *out, cudaStream_t stream);
 
 /*
+ * pa_cache_append_scaled / pa_decode_step_scaled -- the E4M3 cache with its
+ * own scale per KV head for K and for V.
+ * The tuning guide's FP8 KV passage (Step 3) fixes no scale granularity;
+ * these entry points take the per-head reading: K elements of KV head h
+ * are stored as e4m3_rn_satfinite((float)x / k_scales[h]) and read back as
+ * e4m3(b) * k_scales[h]; V likewise with v_scales[h].  k_scales and
+ * v_scales are DEVICE float arrays [num_kv_heads] of positive finite values
+ * (not checked); equal entries give the one-scale behaviour of
+ * pa_cache_append / pa_decode_step.  The cache dtype is E4M3.
+ * pa_decode_step_scaled: as pa_decode_step; k_new and v_new may both be NULL
+ * for attention without an append (slot_mapping is then not written).
+ */
+pa_status pa_cache_append_scaled(const void *k, const void *v, const int32_t *slot_mapping,
+                                 int num_tokens, void *k_cache, void *v_cache, int num_blocks,
+                                 int num_kv_heads, int head_dim, int block_size,
+                                 const float *k_scales, const float *v_scales,
+                                 cudaStream_t stream);
+pa_status pa_decode_step_scaled(const void *q, const void *k_new, const void *v_new,
+                                void *k_cache, void *v_cache, const int32_t *block_tables,
+                                int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+                                int block_size, const float *k_scales, const float *v_scales,
+                                float softmax_scale, int partition_size, void *workspace,
+                                size_t workspace_bytes, int32_t *slot_mapping, void *out,
+                                cudaStream_t stream);
+
+/*
  * pa_decode_static_workspace -- pa_decode with partition_size > 0, without
  * the caller's workspace.
  * The source pages have no counterpart to this entry point.  It exists for

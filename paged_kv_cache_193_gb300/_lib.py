@@ -41,6 +41,9 @@ SIGNATURES = {
                        _P, _P]),
     "pa_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F,
                             _I, _P, _SZ, _P, _P, _P]),
+    "pa_cache_append_scaled": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
+    "pa_decode_step_scaled": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P,
+                                   _P, _F, _I, _P, _SZ, _P, _P, _P]),
     "pa_decode_static_workspace": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                         _F, _I, _P, _P]),
     "pa_device_errors": (_I, [ctypes.POINTER(ctypes.c_uint), _I]),

@@ -187,6 +187,59 @@ def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cac
     return out
 
 
+def cache_append_scaled(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                        k_cache: torch.Tensor, v_cache: torch.Tensor, k_scales: torch.Tensor,
+                        v_scales: torch.Tensor, stream=None) -> None:
+    """E4M3 append with a scale per KV head for K (``k_scales``) and for V
+    (``v_scales``), float32 device tensors [num_kv_heads]; in place."""
+    _need(k, "k", (torch.bfloat16,), 3)
+    _need(v, "v", (torch.bfloat16,), 3)
+    _need(slot_mapping, "slot_mapping", (torch.int32,), 1)
+    _need(k_cache, "k_cache", _CACHE_DTYPES[PA_KV_FP8_E4M3], 4)
+    _need(v_cache, "v_cache", _CACHE_DTYPES[PA_KV_FP8_E4M3], 4)
+    T, Hkv, D = k.shape
+    NB, Hkv2, B, D2 = k_cache.shape
+    _need(k_scales, "k_scales", (torch.float32,), 1)
+    _need(v_scales, "v_scales", (torch.float32,), 1)
+    if (Hkv2, D2) != (Hkv, D) or k_scales.shape[0] != Hkv or v_scales.shape[0] != Hkv:
+        raise ValueError("inconsistent shapes")
+    _check(_lib_handle().pa_cache_append_scaled(
+        k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T, k_cache.data_ptr(),
+        v_cache.data_ptr(), NB, Hkv, D, B, k_scales.data_ptr(), v_scales.data_ptr(),
+        _stream(stream)))
+
+
+def decode_step_scaled(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, k_scales,
+                       v_scales, softmax_scale=None, partition_size=0, workspace=None,
+                       slot_mapping=None, out=None, stream=None) -> torch.Tensor:
+    """Fused decode step over an E4M3 cache with per-KV-head K and V scales.
+    ``k_new``/``v_new`` may both be None: attention without an append."""
+    kv_dtype, S, Hq, D, NB, Hkv, B = _decode_common(q, k_cache, v_cache, block_tables, context_lens)
+    if kv_dtype != PA_KV_FP8_E4M3:
+        raise TypeError("per-head scales need an E4M3 cache")
+    _need(k_scales, "k_scales", (torch.float32,), 1)
+    _need(v_scales, "v_scales", (torch.float32,), 1)
+    if k_new is not None:
+        _need(k_new, "k_new", (torch.bfloat16,), 3)
+        _need(v_new, "v_new", (torch.bfloat16,), 3)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if partition_size and workspace is None:
+        workspace = alloc_workspace(q, block_tables, B, partition_size)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib_handle().pa_decode_step_scaled(
+        q.data_ptr(), k_new.data_ptr() if k_new is not None else None,
+        v_new.data_ptr() if v_new is not None else None, k_cache.data_ptr(), v_cache.data_ptr(),
+        block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), S, Hq, Hkv, D, NB,
+        B, k_scales.data_ptr(), v_scales.data_ptr(), float(softmax_scale), int(partition_size),
+        ws_ptr, ws_bytes, slot_mapping.data_ptr() if slot_mapping is not None else None,
+        out.data_ptr(), _stream(stream)))
+    return out
+
+
 def decode_partitions(q, k_cache, v_cache, block_tables, context_lens, softmax_scale, kv_scale,
                       partition_size, workspace, stream=None) -> None:
     """Per-partition (o, m, l) into ``workspace`` (layout in include/pa.h)."""
@@ -240,8 +293,13 @@ class DecodeStep:
     split."""
 
     def __init__(self, k_cache, v_cache, block_tables, context_lens, num_q_heads,
-                 softmax_scale=None, kv_scale=1.0, partition_size=0, fused=True):
+                 softmax_scale=None, kv_scale=1.0, partition_size=0, fused=True,
+                 k_scales=None, v_scales=None):
         self.fused = fused
+        # per-KV-head E4M3 scales (device float32 [Hkv]); fused path only
+        self.k_scales, self.v_scales = k_scales, v_scales
+        if k_scales is not None and not fused:
+            raise ValueError("per-head scales run through the fused step")
         self.k_cache, self.v_cache = k_cache, v_cache
         self.block_tables, self.context_lens = block_tables, context_lens
         NB, self.Hkv, self.B, self.D = k_cache.shape
@@ -278,6 +336,11 @@ class DecodeStep:
         return (1 if self.fused else 3) + (1 if self.partition_size else 0)
 
     def __call__(self, q, k_new, v_new, stream=None):
+        if self.fused and self.k_scales is not None:
+            return decode_step_scaled(q, k_new, v_new, self.k_cache, self.v_cache,
+                                      self.block_tables, self.context_lens, self.k_scales,
+                                      self.v_scales, self.softmax_scale, self.partition_size,
+                                      self.workspace, self.slots, self.out, stream)
         if self.fused:
             return decode_step(q, k_new, v_new, self.k_cache, self.v_cache, self.block_tables,
                                self.context_lens, self.softmax_scale, self.kv_scale,

@@ -65,6 +65,10 @@ struct DecodeArgs {
     uint8_t *v_cache_w;
     int32_t *slot_out;   // optional: slot of each sequence's newest token
     float append_scale;  // E4M3 scale of the append (cache dtype FP8)
+    // optional per-KV-head E4M3 scales (override the single scale above)
+    const float *k_scales;
+    const float *v_scales;
+    float softmax_log2;  // softmax_scale * log2(e)
 };
 
 // Give up on a page copy after this long (normal waits are microseconds).
@@ -121,6 +125,16 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
     const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = lane >> 2, c = lane & 3;
+
+    // scales of this KV head: one for the whole cache, or K and V per head
+    float score_scale = a.score_scale, v_scale = a.v_scale;
+    float append_k_scale = a.append_scale, append_v_scale = a.append_scale;
+    if (a.k_scales) {
+        append_k_scale = __ldg(a.k_scales + h);
+        append_v_scale = __ldg(a.v_scales + h);
+        score_scale = a.softmax_log2 * append_k_scale;
+        v_scale = append_v_scale;
+    }
 
     // let a dependent merge kernel launch now; it waits for our results
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -190,8 +204,8 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
                     *reinterpret_cast<uint4 *>(a.k_cache_w + dst * 2) = kv;
                     *reinterpret_cast<uint4 *>(a.v_cache_w + dst * 2) = vv;
                 } else {
-                    *reinterpret_cast<uint2 *>(a.k_cache_w + dst) = quantize8_e4m3(kv, a.append_scale);
-                    *reinterpret_cast<uint2 *>(a.v_cache_w + dst) = quantize8_e4m3(vv, a.append_scale);
+                    *reinterpret_cast<uint2 *>(a.k_cache_w + dst) = quantize8_e4m3(kv, append_k_scale);
+                    *reinterpret_cast<uint2 *>(a.v_cache_w + dst) = quantize8_e4m3(vv, append_v_scale);
                 }
                 // the row is read back below by this CTA's TMA (async proxy)
                 fence_proxy_async_global();
@@ -360,7 +374,7 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
 #pragma unroll
                     for (int hi = 0; hi < 2; ++hi) {
                         const int row = mt * 16 + r + hi * 8;
-                        float x = sc[mt][nt][hi * 2 + j] * a.score_scale;
+                        float x = sc[mt][nt][hi * 2 + j] * score_scale;
                         x = row < valid ? x : -INFINITY;
                         sc[mt][nt][hi * 2 + j] = x;
                         mx = fmaxf(mx, x);
@@ -514,7 +528,7 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
 #pragma unroll
             for (int w = 0; w < NW; ++w) L += lsm[w * C::NP + g] * fast_exp2(msm[w * C::NP + g] - M);
         }
-        const float inv = L > 0.f ? a.v_scale / L : 0.f;
+        const float inv = L > 0.f ? v_scale / L : 0.f;
 #pragma unroll
         for (int w = 0; w < NW; ++w)
             wsm[w * C::NP + g] = L > 0.f ? fast_exp2(msm[w * C::NP + g] - M) * inv : 0.f;
@@ -696,9 +710,11 @@ static size_t workspace_bytes_of(int num_seqs, int num_q_heads, int head_dim, in
 
 // New-token rows appended by the decode kernel itself (pa_decode_step).
 struct StepAppend {
-    const void *k_new;
+    const void *k_new;  // null: attention only
     const void *v_new;
     int32_t *slot_out;
+    const float *k_scales;  // optional per-KV-head E4M3 scales
+    const float *v_scales;
 };
 
 // Launch the per-partition (split) or whole-context (unsplit) kernel.
@@ -742,10 +758,13 @@ static pa_status run_decode(const void *q, const void *k_cache, const void *v_ca
     a.err = err;
     a.k_new = app ? static_cast<const uint4 *>(app->k_new) : nullptr;
     a.v_new = app ? static_cast<const uint4 *>(app->v_new) : nullptr;
-    a.k_cache_w = app ? static_cast<uint8_t *>(const_cast<void *>(k_cache)) : nullptr;
-    a.v_cache_w = app ? static_cast<uint8_t *>(const_cast<void *>(v_cache)) : nullptr;
-    a.slot_out = app ? app->slot_out : nullptr;
+    a.k_cache_w = a.k_new ? static_cast<uint8_t *>(const_cast<void *>(k_cache)) : nullptr;
+    a.v_cache_w = a.k_new ? static_cast<uint8_t *>(const_cast<void *>(v_cache)) : nullptr;
+    a.slot_out = a.k_new ? app->slot_out : nullptr;
     a.append_scale = kv_scale;
+    a.k_scales = app ? app->k_scales : nullptr;
+    a.v_scales = app ? app->v_scales : nullptr;
+    a.softmax_log2 = softmax_scale * 1.4426950408889634f;
 
     if (parts > 0x7fffffffLL) return fail(PA_ERR_UNSUPPORTED, "too many partitions");
     dim3 grid(static_cast<unsigned>(split ? parts : 1), sh.num_kv_heads, sh.num_seqs);
@@ -889,7 +908,7 @@ pa_status pa_decode_step(const void *q, const void *k_new, const void *v_new, vo
     if (!aligned16(k_new) || !aligned16(v_new))
         return fail(PA_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
     if (!out || !aligned16(out)) return fail(PA_ERR_INVALID_ARG, "out must be non-null and 16-byte aligned");
-    StepAppend app{k_new, v_new, slot_mapping};
+    StepAppend app{k_new, v_new, slot_mapping, nullptr, nullptr};
     if (partition_size == 0)
         return run_decode(q, k_cache, v_cache, block_tables, context_lens, sh, kv_scale,
                           softmax_scale, nullptr, out, stream, &app);
@@ -899,6 +918,44 @@ pa_status pa_decode_step(const void *q, const void *k_new, const void *v_new, vo
         return fail(PA_ERR_WORKSPACE, "workspace %p of %zu bytes (need %zu, 16-byte aligned)",
                     workspace, workspace_bytes, need);
     st = run_decode(q, k_cache, v_cache, block_tables, context_lens, sh, kv_scale, softmax_scale,
+                    workspace, nullptr, stream, &app);
+    if (st != PA_OK) return st;
+    return launch_reduce(workspace, context_lens, num_seqs, num_q_heads, head_dim, partition_size,
+                         static_cast<int>(parts), out, stream);
+}
+
+pa_status pa_decode_step_scaled(const void *q, const void *k_new, const void *v_new,
+                                void *k_cache, void *v_cache, const int32_t *block_tables,
+                                int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+                                int block_size, const float *k_scales, const float *v_scales,
+                                float softmax_scale, int partition_size, void *workspace,
+                                size_t workspace_bytes, int32_t *slot_mapping, void *out,
+                                cudaStream_t stream) {
+    clear_error();
+    DecodeShape sh{num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                   max_blocks_per_seq, partition_size, PA_KV_FP8_E4M3};
+    pa_status st = check_shape(sh, 1.f, softmax_scale);
+    if (st != PA_OK) return st;
+    if (!k_scales || !v_scales) return fail(PA_ERR_INVALID_ARG, "null scale array");
+    if (num_seqs == 0) return PA_OK;
+    st = check_pointers(q, k_cache, v_cache, block_tables, context_lens);
+    if (st != PA_OK) return st;
+    if ((k_new == nullptr) != (v_new == nullptr))
+        return fail(PA_ERR_INVALID_ARG, "k_new and v_new must both be given or both be NULL");
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new)))
+        return fail(PA_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    if (!out || !aligned16(out)) return fail(PA_ERR_INVALID_ARG, "out must be non-null and 16-byte aligned");
+    StepAppend app{k_new, v_new, slot_mapping, k_scales, v_scales};
+    if (partition_size == 0)
+        return run_decode(q, k_cache, v_cache, block_tables, context_lens, sh, 1.f, softmax_scale,
+                          nullptr, out, stream, &app);
+    int64_t parts = max_partitions_of(max_blocks_per_seq, block_size, partition_size);
+    size_t need = workspace_bytes_of(num_seqs, num_q_heads, head_dim, parts);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need)
+        return fail(PA_ERR_WORKSPACE, "workspace %p of %zu bytes (need %zu, 16-byte aligned)",
+                    workspace, workspace_bytes, need);
+    st = run_decode(q, k_cache, v_cache, block_tables, context_lens, sh, 1.f, softmax_scale,
                     workspace, nullptr, stream, &app);
     if (st != PA_OK) return st;
     return launch_reduce(workspace, context_lens, num_seqs, num_q_heads, head_dim, partition_size,

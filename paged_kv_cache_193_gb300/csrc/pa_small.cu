@@ -82,7 +82,8 @@ __global__ void append_kernel(const uint4 *__restrict__ k, const uint4 *__restri
                               const int32_t *__restrict__ slot_mapping, int num_tokens,
                               uint8_t *__restrict__ k_cache, uint8_t *__restrict__ v_cache,
                               int64_t num_slots, int num_kv_heads, int head_dim, int block_size,
-                              float scale, unsigned int *err) {
+                              float scale, const float *__restrict__ k_scales,
+                              const float *__restrict__ v_scales, unsigned int *err) {
     const int vec_per_row = head_dim / 8;
     int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     int64_t total = static_cast<int64_t>(num_tokens) * num_kv_heads * vec_per_row;
@@ -106,8 +107,11 @@ __global__ void append_kernel(const uint4 *__restrict__ k, const uint4 *__restri
         *reinterpret_cast<uint4 *>(k_cache + dst * 2) = kv;
         *reinterpret_cast<uint4 *>(v_cache + dst * 2) = vv;
     } else {
-        *reinterpret_cast<uint2 *>(k_cache + dst) = quantize8_e4m3(kv, scale);
-        *reinterpret_cast<uint2 *>(v_cache + dst) = quantize8_e4m3(vv, scale);
+        // one scale for the whole cache, or one per KV head for K and for V
+        const float ks = k_scales ? k_scales[head] : scale;
+        const float vs = v_scales ? v_scales[head] : scale;
+        *reinterpret_cast<uint2 *>(k_cache + dst) = quantize8_e4m3(kv, ks);
+        *reinterpret_cast<uint2 *>(v_cache + dst) = quantize8_e4m3(vv, vs);
     }
 }
 
@@ -314,11 +318,11 @@ pa_status pa_slot_mapping(const int32_t *block_tables, int max_blocks_per_seq,
     return cuda_check(cudaGetLastError(), "slot mapping launch");
 }
 
-pa_status pa_cache_append(const void *k, const void *v, const int32_t *slot_mapping,
-                          int num_tokens, void *k_cache, void *v_cache, int num_blocks,
-                          int num_kv_heads, int head_dim, int block_size,
-                          pa_kv_dtype kv_dtype, float scale, cudaStream_t stream) {
-    clear_error();
+static pa_status append_impl(const void *k, const void *v, const int32_t *slot_mapping,
+                             int num_tokens, void *k_cache, void *v_cache, int num_blocks,
+                             int num_kv_heads, int head_dim, int block_size, pa_kv_dtype kv_dtype,
+                             float scale, const float *k_scales, const float *v_scales,
+                             cudaStream_t stream) {
     if (num_tokens < 0 || num_blocks < 0 || num_kv_heads <= 0)
         return fail(PA_ERR_INVALID_ARG, "bad size (num_tokens=%d, num_blocks=%d, num_kv_heads=%d)",
                     num_tokens, num_blocks, num_kv_heads);
@@ -328,7 +332,7 @@ pa_status pa_cache_append(const void *k, const void *v, const int32_t *slot_mapp
         return fail(PA_ERR_UNSUPPORTED, "block_size %d (supported: 16, 32)", block_size);
     if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_FP8_E4M3)
         return fail(PA_ERR_UNSUPPORTED, "kv_dtype %d", static_cast<int>(kv_dtype));
-    if (kv_dtype == PA_KV_FP8_E4M3 && !(scale > 0.f && scale <= 3.4e38f))
+    if (kv_dtype == PA_KV_FP8_E4M3 && !k_scales && !(scale > 0.f && scale <= 3.4e38f))
         return fail(PA_ERR_INVALID_ARG, "fp8 scale must be positive and finite");
     if (num_tokens == 0) return PA_OK;
     if (!k || !v || !slot_mapping || !k_cache || !v_cache)
@@ -346,13 +350,33 @@ pa_status pa_cache_append(const void *k, const void *v, const int32_t *slot_mapp
         append_kernel<false><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
             static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, num_tokens,
             static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), num_slots,
-            num_kv_heads, head_dim, block_size, scale, err);
+            num_kv_heads, head_dim, block_size, scale, nullptr, nullptr, err);
     else
         append_kernel<true><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
             static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, num_tokens,
             static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), num_slots,
-            num_kv_heads, head_dim, block_size, scale, err);
+            num_kv_heads, head_dim, block_size, scale, k_scales, v_scales, err);
     return cuda_check(cudaGetLastError(), "append launch");
+}
+
+pa_status pa_cache_append(const void *k, const void *v, const int32_t *slot_mapping,
+                          int num_tokens, void *k_cache, void *v_cache, int num_blocks,
+                          int num_kv_heads, int head_dim, int block_size,
+                          pa_kv_dtype kv_dtype, float scale, cudaStream_t stream) {
+    clear_error();
+    return append_impl(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, num_kv_heads,
+                       head_dim, block_size, kv_dtype, scale, nullptr, nullptr, stream);
+}
+
+pa_status pa_cache_append_scaled(const void *k, const void *v, const int32_t *slot_mapping,
+                                 int num_tokens, void *k_cache, void *v_cache, int num_blocks,
+                                 int num_kv_heads, int head_dim, int block_size,
+                                 const float *k_scales, const float *v_scales,
+                                 cudaStream_t stream) {
+    clear_error();
+    if (!k_scales || !v_scales) return fail(PA_ERR_INVALID_ARG, "null scale array");
+    return append_impl(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, num_kv_heads,
+                       head_dim, block_size, PA_KV_FP8_E4M3, 1.f, k_scales, v_scales, stream);
 }
 
 }  // extern "C"
