@@ -61,6 +61,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.pa_oracle_cache_append_scaled.argtypes = [P, P, P, I, P, P, I, I, I, P, P]
     lib.pa_oracle_decode_scaled.restype = None
     lib.pa_oracle_decode_scaled.argtypes = [P, P, P, P, I, P, I, I, I, I, I, D, P, P, P, I, P]
+    lib.pa_oracle_block_alloc.restype = I
+    lib.pa_oracle_block_alloc.argtypes = [P, I, P, I, I, P, P, P, I, P, P, I, I, I, P]
     lib.pa_oracle_set_threads.restype = None
     lib.pa_oracle_set_threads.argtypes = [I]
     lib.pa_oracle_get_threads.restype = I
@@ -227,6 +229,27 @@ class Oracle:
                                          num_kv_heads, D, block_size, float(softmax_scale), _p(ks),
                                          _p(vs), _p(pr), pr.shape[0], _p(out))
         return out
+
+    # -- block allocation with copy-on-write ------------------------------------
+    def block_alloc(self, block_tables, context_lens, block_size, free_blocks, free_count,
+                    refcounts, k_cache, v_cache):
+        """In place on every array: fresh blocks for tokens that open a block,
+        copy-on-write for tokens written into a shared block.  Returns
+        (status, free_count, cow_src)."""
+        for a, dt in ((block_tables, np.int32), (free_blocks, np.int32), (refcounts, np.int32)):
+            assert a.dtype == dt and a.flags.c_contiguous
+        assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+        cl = _c(context_lens, np.int32)
+        S, MB = block_tables.shape
+        NB, Hkv, B, D = k_cache.shape
+        elem = k_cache.dtype.itemsize
+        fc = np.array([free_count], np.int32)
+        cow = np.empty(S, np.int32)
+        st = self.lib.pa_oracle_block_alloc(_p(block_tables), MB, _p(cl), S, block_size,
+                                            _p(free_blocks), _p(fc), _p(refcounts), NB,
+                                            _p(k_cache.view(np.uint8)), _p(v_cache.view(np.uint8)),
+                                            Hkv, D, elem, _p(cow))
+        return int(st), int(fc[0]), cow
 
     # -- threads -------------------------------------------------------------
     def set_threads(self, n: int) -> None:

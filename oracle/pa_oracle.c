@@ -450,6 +450,115 @@ void pa_oracle_decode_scaled(const uint16_t *q, const uint8_t *k_cache, const ui
 }
 
 /* ------------------------------------------------------------------------ */
+/* block allocation for the newest tokens, with copy-on-write                */
+/* ------------------------------------------------------------------------ */
+
+/* "When a new token arrives, [the engine] appends to the logical sequence
+ * and allocates a fresh physical page only if needed" (first page,
+ * "PagedAttention Mechanics"), and sequences may share the physical blocks of
+ * a common prompt (fourth page, section 2).  Reading for a shared block that
+ * is about to be written (the pages are silent): the writer first gets its
+ * own copy (copy-on-write).
+ *
+ * For every sequence s with n = context_lens[s] > 0 (n counts the token
+ * being appended, at position pos = n - 1, logical block j = pos / B):
+ *   - pos % B == 0: the token opens block j: it gets a fresh block;
+ *   - otherwise, if the block table[s][j] is referenced by more than one
+ *     sequence (refcounts[block] > 1, counted before this call): it gets a
+ *     fresh block, the rows [0, pos % B) of every KV head of K and V are
+ *     copied into it, and the old block loses one reference;
+ *   - otherwise nothing changes (the sole owner appends in place).
+ * Fresh blocks are taken from the top of the free stack
+ * free_blocks[0 .. *free_count) in sequence order (the first sequence that
+ * needs one takes free_blocks[*free_count - 1]); each gets refcount 1.
+ * Blocks whose count drops to zero are pushed back afterwards, in the order
+ * of the last sequence (by index) that copied out of them.  If the stack
+ * holds fewer blocks than needed, nothing changes and the call returns 1
+ * (else 0).  cow_src[s] receives the block copied from, or -1.
+ * Caches are bf16 (elem_bytes 2) or E4M3 (1); layout as elsewhere. */
+int pa_oracle_block_alloc(int32_t *block_tables, int max_blocks_per_seq,
+                          const int32_t *context_lens, int num_seqs, int block_size,
+                          int32_t *free_blocks, int32_t *free_count, int32_t *refcounts,
+                          int num_blocks, uint8_t *k_cache, uint8_t *v_cache, int num_kv_heads,
+                          int head_dim, int elem_bytes, int32_t *cow_src)
+{
+    int need = 0;
+    int *action = (int *)malloc(sizeof(int) * (size_t)(num_seqs > 0 ? num_seqs : 1));
+    /* decide, from the state before the call */
+    for (int s = 0; s < num_seqs; ++s) {
+        int n = context_lens[s];
+        action[s] = 0; /* 0 none, 1 fresh, 2 copy */
+        cow_src[s] = -1;
+        if (n <= 0)
+            continue;
+        int pos = n - 1;
+        int j = pos / block_size;
+        if (j >= max_blocks_per_seq)
+            continue;
+        if (pos % block_size == 0) {
+            action[s] = 1;
+        } else {
+            int32_t cur = block_tables[(int64_t)s * max_blocks_per_seq + j];
+            if (cur < 0 || cur >= num_blocks)
+                continue;
+            if (refcounts[cur] > 1)
+                action[s] = 2;
+        }
+        if (action[s])
+            ++need;
+    }
+    if (need > *free_count) {
+        free(action);
+        return 1;
+    }
+    int top = *free_count;
+    int taken = 0;
+    int32_t *freed = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_seqs > 0 ? num_seqs : 1));
+    int nfreed = 0;
+    int64_t row_bytes = (int64_t)head_dim * elem_bytes;
+    for (int s = 0; s < num_seqs; ++s) {
+        if (!action[s])
+            continue;
+        int pos = context_lens[s] - 1;
+        int j = pos / block_size;
+        int64_t entry = (int64_t)s * max_blocks_per_seq + j;
+        int32_t fresh = free_blocks[top - 1 - taken];
+        ++taken;
+        if (action[s] == 2) {
+            int32_t old = block_tables[entry];
+            int rows = pos % block_size;
+            for (int h = 0; h < num_kv_heads; ++h) {
+                int64_t src = (((int64_t)old * num_kv_heads + h) * block_size) * row_bytes;
+                int64_t dst = (((int64_t)fresh * num_kv_heads + h) * block_size) * row_bytes;
+                memcpy(k_cache + dst, k_cache + src, (size_t)(rows * row_bytes));
+                memcpy(v_cache + dst, v_cache + src, (size_t)(rows * row_bytes));
+            }
+            refcounts[old] -= 1;
+            cow_src[s] = old;
+        }
+        block_tables[entry] = fresh;
+        refcounts[fresh] = 1;
+    }
+    /* push blocks left without references, in order of their last copier */
+    for (int s = 0; s < num_seqs; ++s) {
+        if (action[s] != 2 || refcounts[cow_src[s]] != 0)
+            continue;
+        int last = 1;
+        for (int t = s + 1; t < num_seqs; ++t)
+            if (action[t] == 2 && cow_src[t] == cow_src[s])
+                last = 0;
+        if (last)
+            freed[nfreed++] = cow_src[s];
+    }
+    *free_count = top - taken;
+    for (int i = 0; i < nfreed; ++i)
+        free_blocks[(*free_count)++] = freed[i];
+    free(freed);
+    free(action);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* threads                                                                   */
 /* ------------------------------------------------------------------------ */
 

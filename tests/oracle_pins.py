@@ -319,7 +319,73 @@ def pin_fp8_per_head_scales(o):
     assert np.array_equal(k1, k2) and np.array_equal(v1, v2)
 
 
+def pin_block_alloc(o):
+    """Allocation for the newest tokens: checked against invariants that any
+    correct allocator with these rules keeps (conservation of blocks,
+    reference counts equal to the references in the tables, exclusive
+    ownership of every block about to be written, untouched sole owners,
+    unchanged logical contents, fresh blocks from the top of the stack in
+    sequence order, all-or-nothing when the stack is short)."""
+    from alloc_cases import gather_rows, make_state
+    for seed in (1, 2, 3):
+        st = make_state(seed)
+        B, NB = st["B"], st["NB"]
+        t0, r0, f0 = st["tables"].copy(), st["refc"].copy(), st["free"].copy()
+        k0, v0 = st["k"].copy(), st["v"].copy()
+        tables, refc, free = st["tables"], st["refc"], np.concatenate([st["free"], np.zeros(NB, np.int32)])
+        status, fc, cow = o.block_alloc(tables, st["ctx"], B, free, st["free_count"], refc,
+                                        st["k"], st["v"])
+        assert status == 0
+        ctx = st["ctx"]
+        S = len(ctx)
+        # reference counts equal the references in the tables
+        recount = np.zeros(NB, np.int32)
+        for s_ in range(S):
+            for j in range((ctx[s_] + B - 1) // B):
+                assert 0 <= tables[s_, j] < NB
+                recount[tables[s_, j]] += 1
+        assert np.array_equal(recount, refc)
+        # conservation: every block is either free or referenced, never both
+        free_now = free[:fc]
+        assert len(set(free_now.tolist())) == fc
+        assert not (set(free_now.tolist()) & set(np.flatnonzero(recount).tolist()))
+        assert fc + np.count_nonzero(recount) == NB
+        need = 0
+        for s_ in range(S):
+            n = int(ctx[s_])
+            if n <= 0:
+                assert np.array_equal(tables[s_], t0[s_])
+                continue
+            pos, j = n - 1, (n - 1) // B
+            # only entry j may change
+            mask = np.ones(tables.shape[1], bool)
+            mask[j] = False
+            assert np.array_equal(tables[s_][mask], t0[s_][mask])
+            assert refc[tables[s_, j]] == 1  # exclusive before the write
+            shared_before = pos % B != 0 and r0[t0[s_, j]] > 1
+            if pos % B != 0 and not shared_before:
+                assert tables[s_, j] == t0[s_, j] and cow[s_] == -1  # sole owner: in place
+            if pos % B == 0 or shared_before:
+                assert tables[s_, j] == f0[st["free_count"] - 1 - need]  # stack top, in order
+                need += 1
+            assert cow[s_] == (t0[s_, j] if shared_before else -1)
+            # the logical rows before the new token are unchanged
+            for old, new in ((k0, st["k"]), (v0, st["v"])):
+                a = gather_rows(t0, pos, s_, old, B)
+                b = gather_rows(tables, pos, s_, new, B)
+                assert (a is None and b is None) or np.array_equal(a, b)
+        assert fc == st["free_count"] - need + len(set(int(c) for c in cow if c >= 0 and refc[c] == 0))
+    # a short stack changes nothing
+    st = make_state(4, extra_free=2)
+    t0, r0 = st["tables"].copy(), st["refc"].copy()
+    free = st["free"].copy()
+    status, fc, cow = o.block_alloc(st["tables"], st["ctx"], st["B"], free, st["free_count"],
+                                    st["refc"], st["k"], st["v"])
+    assert status == 1 and fc == st["free_count"]
+    assert np.array_equal(st["tables"], t0) and np.array_equal(st["refc"], r0)
+
+
 ALL = [pin_kv_formula, pin_e4m3_decode, pin_e4m3_encode, pin_e4m3_roundtrip, pin_attention_sdpa,
        pin_attention_fp8, pin_extreme_scores, pin_permutation, pin_prefix_sharing, pin_context_one,
        pin_identical_keys, pin_empty_context, pin_slot_mapping, pin_append_readback,
-       pin_partition_merge, pin_fp8_per_head_scales]
+       pin_partition_merge, pin_fp8_per_head_scales, pin_block_alloc]

@@ -31,6 +31,12 @@ MUTANTS = {
                           "(double)v_scales[kvh], (double)k_scales[kvh]"),
     "scaled_head_ignored": ("k_cache[dst] = pa_oracle_e4m3_from_float(kf / k_scales[h]);",
                             "k_cache[dst] = pa_oracle_e4m3_from_float(kf / k_scales[0]);"),
+    "alloc_copies_sole_owner": ("if (refcounts[cur] > 1)\n                action[s] = 2;",
+                                "if (refcounts[cur] > 0)\n                action[s] = 2;"),
+    "alloc_copy_short": ("int rows = pos % block_size;", "int rows = pos % block_size - (pos % block_size > 0);"),
+    "alloc_stack_bottom": ("int32_t fresh = free_blocks[top - 1 - taken];", "int32_t fresh = free_blocks[taken];"),
+    "alloc_no_release": ("refcounts[old] -= 1;", "refcounts[old] -= 0;"),
+    "alloc_no_push": ("freed[nfreed++] = cow_src[s];", "(void)0;"),
     "partition_short": ("int t1 = t0 + partition_size;", "int t1 = t0 + partition_size - 1;"),
     "last_token_dropped": ("attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s],",
                            "attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s] - (context_lens[s] > 1),"),
