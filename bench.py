@@ -77,6 +77,9 @@ def parse():
                     help="attention layers per step, each with its own KV cache")
     ap.add_argument("--per-head-scales", action="store_true",
                     help="E4M3 cache with its own K and V scale per KV head")
+    ap.add_argument("--device-alloc", action="store_true",
+                    help="each step first advances every context by one token and allocates "
+                         "blocks on the device (pa_block_alloc), then runs the step")
     ap.add_argument("--separate", action="store_true",
                     help="time the unfused entry points (3-4 kernels per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -187,8 +190,9 @@ def build_workload(args, device, data_seed=None):
     bs, ps = DEFAULT_LAUNCH[args.config]
     bs = args.block_size or bs
     ps = ps if args.partition_size is None else args.partition_size
+    extra = args.warmup + args.steps + 1 if args.device_alloc else 0
     wl = W.make(args.config, device=device, block_size=bs, num_seqs=args.num_seqs,
-                data_seed=data_seed)
+                data_seed=data_seed, extra_steps=extra)
     if args.fp8 and wl.shape.kv_dtype != W.KV_FP8_E4M3:
         wl.shape.kv_dtype = W.KV_FP8_E4M3
         wl.kv_scale = W.fp8_scale_from(wl.k_cache, wl.v_cache, wl.k_new, wl.v_new)
@@ -383,7 +387,26 @@ def run_ours(args):
     step = steps[0]
     bt, cl = step.block_tables, step.context_lens
     stream = torch.cuda.current_stream()
-    if args.graph:
+    if args.device_alloc:
+        if len(steps) != 1 or args.graph:
+            raise SystemExit("--device-alloc runs one eager layer")
+        args.min_warmup_seconds = 0.0
+        alloc = wl.notes["allocator"]
+        pool = api.DeviceBlockPool(alloc._free, alloc.refcount, device)
+        # contexts currently include the token appended at step 0: start one lower
+        cl.sub_(1)
+        kv0 = wl.kv_bytes() - sh.num_seqs * sh.num_kv_heads * sh.head_dim * 2 * (
+            2 if sh.kv_dtype == W.KV_BF16 else 1)
+        per_token = sh.num_kv_heads * sh.head_dim * 2 * (2 if sh.kv_dtype == W.KV_BF16 else 1)
+        cow = torch.empty(sh.num_seqs, dtype=torch.int32, device=device)
+        calls = [0]
+
+        def run_step():
+            pool.allocate(bt, cl, wl.k_cache, wl.v_cache, advance=True, cow_src=cow)
+            step(wl.q, wl.k_new, wl.v_new)
+            calls[0] += 1
+        launches_per_step = step.launches() + 2
+    elif args.graph:
         graph = api.StepGraph(steps, inputs)
         run_step = graph.replay
         launches_per_step = graph.launches()
@@ -434,7 +457,7 @@ def run_ours(args):
     # merge one launch each with events between them (this breaks the
     # overlap of the merge's launch with the attention tail, so it is kept
     # out of the timed steps).
-    if ps == 0 and step.fused and len(steps) == 1:
+    if ps == 0 and step.fused and len(steps) == 1 and not args.device_alloc:
         dec_ms, red_ms, kname = float(np.mean(t_step)), 0.0, "decode_kernel (fused step)"
     else:
         n2 = min(K, 200)
@@ -461,11 +484,19 @@ def run_ours(args):
     clocks.stop()
 
     kv = sum(lw.kv_bytes() for lw in layers)
+    if args.device_alloc:
+        # the timed steps saw contexts growing by one token per step
+        first = calls[0] - K
+        kv = kv0 + per_token * sh.num_seqs * (first + (K + 1) / 2.0)
+        assert api.device_errors() == 0, "device errors during the allocating steps"
     ms_per_step = total_ms / K
     value = world * kv * K / (total_ms / 1e3) / 1e9
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", 6800.0))
-    achieved = wl.kv_bytes() / (dec_ms / 1e3) / 1e9
+    kv_launch = wl.kv_bytes()
+    if args.device_alloc:  # the kernel-only launches ran at the final contexts
+        kv_launch = kv0 + per_token * sh.num_seqs * calls[0]
+    achieved = kv_launch / (dec_ms / 1e3) / 1e9
     traffic = recorded_traffic(wl, ps)
 
     result = {
@@ -477,6 +508,7 @@ def run_ours(args):
         "config": config_of(wl, ps, args),
         "tokens_per_s": round(world * sh.num_seqs * K / (total_ms / 1e3), 1),
         "layers_per_step": len(layers), "launch": "one CUDA graph per step" if args.graph else "eager",
+        "device_alloc": bool(args.device_alloc),
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         f"pct_of_{peak_kind}_hbm": round(100 * value / world / hbm, 2),
         "breakdown_ms": {"step_median": round(float(np.median(t_step)), 5),
@@ -491,13 +523,13 @@ def run_ours(args):
                      "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "algorithmic_bytes_per_launch": wl.kv_bytes(), "traffic": traffic},
+                     "algorithmic_bytes_per_launch": kv_launch, "traffic": traffic},
     }
     result["clocks"] = clocks.summary(t_wall0 - 1.0, t_wall1)
 
-    if not args.no_e2e and len(layers) == 1:
+    if not args.no_e2e and len(layers) == 1 and not args.device_alloc:
         result["e2e"] = run_e2e(api, wl, step, ps, K, world, device)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.device_alloc:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(result), flush=True)

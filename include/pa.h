@@ -80,6 +80,7 @@ typedef enum pa_kv_dtype {
 #define PA_DEVERR_BAD_CONTEXT 0x2u /* context_lens[s] > max_blocks_per_seq * block_size: clamped */
 #define PA_DEVERR_TIMEOUT     0x4u /* a wait for a page copy exceeded its time limit; output invalid */
 #define PA_DEVERR_BAD_SLOT    0x8u /* slot_mapping entry >= num_blocks * block_size: token skipped */
+#define PA_DEVERR_OUT_OF_BLOCKS 0x10u /* pa_block_alloc: free stack too short; nothing changed */
 
 /*
  * pa_slot_mapping -- slot of each sequence's newest token.
@@ -243,6 +244,42 @@ pa_status pa_decode_step_scaled(const void *q, const void *k_new, const void *v_
                                 float softmax_scale, int partition_size, void *workspace,
                                 size_t workspace_bytes, int32_t *slot_mapping, void *out,
                                 cudaStream_t stream);
+
+/*
+ * pa_block_alloc -- device-side block allocation for the newest tokens, with
+ * copy-on-write of shared blocks.
+ * Source: "a fresh physical page only if needed" ("PagedAttention
+ * Mechanics", first page) and blocks shared between requests (fourth page,
+ * section 2).  Reading for writes into a shared block (the pages are
+ * silent): the writer first gets a private copy.
+ *   context_lens int32 [num_seqs] (device, in/out): the length including the
+ *                token being appended; with advance != 0 every entry > 0 is
+ *                first increased by one (one new token per active sequence)
+ *                and written back.
+ *   For each sequence with n > 0, pos = n - 1, j = pos / block_size:
+ *     pos % block_size == 0: block_tables[s][j] = a fresh block;
+ *     else if refcounts[block_tables[s][j]] > 1 (counted before the call):
+ *       block_tables[s][j] = a fresh block holding a copy of rows
+ *       [0, pos % block_size) of the old block (every KV head, K and V), and
+ *       the old block loses one reference;
+ *     else nothing (the sole owner appends in place).
+ *   free_blocks int32 [num_blocks] (device, in/out): a stack whose first
+ *                *free_count entries are the free blocks; fresh blocks come
+ *                off its top in sequence order (refcount set to 1); blocks
+ *                whose count reaches 0 are pushed back afterwards in the
+ *                order of the last sequence that copied out of them.
+ *   free_count   int32 scalar (device, in/out).
+ *   refcounts    int32 [num_blocks] (device, in/out): references per block.
+ *   cow_src      int32 [num_seqs] (device, out): block copied from, or -1.
+ * If the stack holds fewer blocks than needed nothing changes and the device
+ * error word gets PA_DEVERR_OUT_OF_BLOCKS.  Deterministic (one CTA decides
+ * in sequence order).  num_seqs <= 16384.  Two kernels (decide, copy).
+ */
+pa_status pa_block_alloc(int32_t *block_tables, int max_blocks_per_seq, int32_t *context_lens,
+                         int num_seqs, int block_size, int advance, int32_t *free_blocks,
+                         int32_t *free_count, int32_t *refcounts, int num_blocks, void *k_cache,
+                         void *v_cache, int num_kv_heads, int head_dim, pa_kv_dtype kv_dtype,
+                         int32_t *cow_src, cudaStream_t stream);
 
 /*
  * pa_decode_static_workspace -- pa_decode with partition_size > 0, without

@@ -26,6 +26,7 @@ PA_DEVERR_BAD_BLOCK = 0x1
 PA_DEVERR_BAD_CONTEXT = 0x2
 PA_DEVERR_TIMEOUT = 0x4
 PA_DEVERR_BAD_SLOT = 0x8
+PA_DEVERR_OUT_OF_BLOCKS = 0x10
 
 # name -> (restype, argtypes); the order matches include/pa.h
 _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -44,6 +45,7 @@ SIGNATURES = {
     "pa_cache_append_scaled": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "pa_decode_step_scaled": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P,
                                    _P, _F, _I, _P, _SZ, _P, _P, _P]),
+    "pa_block_alloc": (_I, [_P, _I, _P, _I, _I, _I, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P]),
     "pa_decode_static_workspace": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                         _F, _I, _P, _P]),
     "pa_device_errors": (_I, [ctypes.POINTER(ctypes.c_uint), _I]),

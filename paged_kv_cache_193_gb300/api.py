@@ -240,6 +240,39 @@ def decode_step_scaled(q, k_new, v_new, k_cache, v_cache, block_tables, context_
     return out
 
 
+class DeviceBlockPool:
+    """Device-side free stack and reference counts of a paged cache's blocks,
+    driven by ``pa_block_alloc``.  Build it from the host state once
+    (``free`` = the free block ids in stack order, ``refcounts`` per block);
+    afterwards every step allocates on the device."""
+
+    def __init__(self, free, refcounts, device):
+        NB = len(refcounts)
+        self.free_blocks = torch.zeros(NB, dtype=torch.int32, device=device)
+        self.free_blocks[: len(free)] = torch.as_tensor(free, dtype=torch.int32)
+        self.free_count = torch.tensor([len(free)], dtype=torch.int32, device=device)
+        self.refcounts = torch.as_tensor(refcounts, dtype=torch.int32).to(device).contiguous()
+        self.num_blocks = NB
+
+    def allocate(self, block_tables, context_lens, k_cache, v_cache, advance=False, cow_src=None,
+                 stream=None) -> torch.Tensor:
+        """Fresh blocks / copy-on-write for each sequence's newest token (see
+        pa_block_alloc); returns cow_src (int32 [S])."""
+        _need(block_tables, "block_tables", (torch.int32,), 2)
+        _need(context_lens, "context_lens", (torch.int32,), 1)
+        kv_dtype = cache_dtype_of(k_cache)
+        NB, Hkv, B, D = k_cache.shape
+        S, MB = block_tables.shape
+        if cow_src is None:
+            cow_src = torch.empty(S, dtype=torch.int32, device=block_tables.device)
+        _check(_lib_handle().pa_block_alloc(
+            block_tables.data_ptr(), MB, context_lens.data_ptr(), S, B, 1 if advance else 0,
+            self.free_blocks.data_ptr(), self.free_count.data_ptr(), self.refcounts.data_ptr(), NB,
+            k_cache.data_ptr(), v_cache.data_ptr(), Hkv, D, kv_dtype, cow_src.data_ptr(),
+            _stream(stream)))
+        return cow_src
+
+
 def decode_partitions(q, k_cache, v_cache, block_tables, context_lens, softmax_scale, kv_scale,
                       partition_size, workspace, stream=None) -> None:
     """Per-partition (o, m, l) into ``workspace`` (layout in include/pa.h)."""

@@ -274,9 +274,12 @@ def make(name: str, device="cpu", seed: int | None = None, block_size: int | Non
     if name == "tiny":
         shape = Shape(num_seqs or 4, 8, 2, 64, block_size or 16)
         ctx = np.array([1, 17, 100, 255], np.int64)[: shape.num_seqs]
-        nb = 64
-        tables, _ = build_tables(ctx, shape.block_size, nb, rng)
-        return _finish(name, shape, ctx, tables, nb, device, vseed, fill_cache=fill_cache)
+        nb = 64 + extra_steps * shape.num_seqs
+        tables, alloc = build_tables(ctx, shape.block_size, nb, rng,
+                                     _blocks_for(255 + extra_steps, shape.block_size))
+        wl = _finish(name, shape, ctx, tables, nb, device, vseed, fill_cache=fill_cache)
+        wl.notes["allocator"] = alloc
+        return wl
     if name == "llama8b":
         shape = Shape(num_seqs or 256, 32, 8, 128, block_size or 16)
         ctx = rng.integers(512, 2048, size=shape.num_seqs, endpoint=True)
@@ -290,14 +293,15 @@ def make(name: str, device="cpu", seed: int | None = None, block_size: int | Non
         prefix = 2048
         suffix = rng.integers(64, 512, size=shape.num_seqs, endpoint=True)
         ctx = prefix + suffix
-        mb = _blocks_for(prefix + 512, shape.block_size)
+        mb = _blocks_for(prefix + 512 + extra_steps, shape.block_size)
         pb = prefix // shape.block_size
-        need = pb + sum(_blocks_for(int(c), shape.block_size) - pb for c in ctx)
+        need = pb + sum(_blocks_for(int(c) + extra_steps, shape.block_size) - pb for c in ctx)
         nb = math.ceil(1.2 * need)
-        tables, _ = build_tables(ctx, shape.block_size, nb, rng, mb, shared_prefix_blocks=pb)
+        tables, alloc = build_tables(ctx, shape.block_size, nb, rng, mb, shared_prefix_blocks=pb)
         wl = _finish(name, shape, ctx, tables, nb, device, vseed, gen_device=device,
                      fill_cache=fill_cache)
         wl.notes["shared_prefix_tokens"] = prefix
+        wl.notes["allocator"] = alloc
         return wl
     elif name == "ctx128k":
         shape = Shape(num_seqs or 8, 128, 8, 128, block_size or 16, partition_size=512)

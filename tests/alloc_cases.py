@@ -9,20 +9,22 @@ import numpy as np
 
 def make_state(seed: int, B: int = 4, NB: int = 64, Hkv: int = 2, D: int = 8, elem=np.uint16,
                extra_free: int | None = None):
+    """Lengths are set relative to the block size B, so the same situations
+    arise for any B >= 4."""
     rng = np.random.default_rng(seed)
     order = list(rng.permutation(NB))
-    seqs = []  # (pre_len, shared prompt blocks)
-    # group A: share a 6-token prompt (blocks: one full, one holding 2 rows),
-    # each about to append its first own token into the partial block
+    seqs = []  # (tokens already cached, shared prompt blocks)
+    # group A: share a prompt of one full and one partial block, each about to
+    # append its first own token into the partial (shared) block
     prompt_a = [order.pop(), order.pop()]
     for _ in range(3):
-        seqs.append((6, list(prompt_a)))
-    # group B: share an 8-token prompt (two full blocks) plus private suffixes
+        seqs.append((B + B // 2, list(prompt_a)))
+    # group B: share a prompt of two full blocks plus private suffixes
     prompt_b = [order.pop(), order.pop()]
-    for extra in (0, 1, 3, 5):
-        seqs.append((8 + extra, list(prompt_b)))
+    for extra in (0, 1, 3, B + 1):
+        seqs.append((2 * B + extra, list(prompt_b)))
     # private sequences of assorted lengths, and an empty one
-    for n in (1, 3, 4, 7, 12, 0):
+    for n in (1, 3, B, B + 3, 3 * B, 0):
         seqs.append((n, []))
     S = len(seqs)
     MB = 8
@@ -40,9 +42,8 @@ def make_state(seed: int, B: int = 4, NB: int = 64, Hkv: int = 2, D: int = 8, el
     free = np.array(order, np.int32)
     if extra_free is not None:
         free = free[:extra_free]
-    # the new token of every non-empty sequence is appended this step
-    ctx = np.array([pre + 1 if pre > 0 or s == S - 2 else 0 for s, (pre, _) in enumerate(seqs)],
-                   np.int32)
+    # every non-empty sequence appends one token this step
+    ctx = np.array([pre + 1 if pre > 0 else 0 for pre, _ in seqs], np.int32)
     g = np.random.default_rng(seed + 1)
     kc = g.integers(0, 2**15, size=(NB, Hkv, B, D)).astype(elem)
     vc = g.integers(0, 2**15, size=(NB, Hkv, B, D)).astype(elem)
