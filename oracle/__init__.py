@@ -63,6 +63,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.pa_oracle_decode_scaled.argtypes = [P, P, P, P, I, P, I, I, I, I, I, D, P, P, P, I, P]
     lib.pa_oracle_block_alloc.restype = I
     lib.pa_oracle_block_alloc.argtypes = [P, I, P, I, I, P, P, P, I, P, P, I, I, I, P]
+    lib.pa_oracle_chunk_slot_mapping.restype = None
+    lib.pa_oracle_chunk_slot_mapping.argtypes = [P, I, P, P, I, I, P]
+    lib.pa_oracle_prefill.restype = None
+    lib.pa_oracle_prefill.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, D, I, D, P]
     lib.pa_oracle_set_threads.restype = None
     lib.pa_oracle_set_threads.argtypes = [I]
     lib.pa_oracle_get_threads.restype = I
@@ -228,6 +232,34 @@ class Oracle:
         self.lib.pa_oracle_decode_scaled(_p(q), _p(kc), _p(vc), _p(bt), bt.shape[1], _p(cl), S, Hq,
                                          num_kv_heads, D, block_size, float(softmax_scale), _p(ks),
                                          _p(vs), _p(pr), pr.shape[0], _p(out))
+        return out
+
+    # -- chunked prefill ------------------------------------------------------
+    def chunk_slot_mapping(self, block_tables, context_lens, query_start, block_size):
+        """int32 [Tq] slots of every chunk token (the chunk ends the context)."""
+        bt = _c(block_tables, np.int32)
+        cl = _c(context_lens, np.int32)
+        qs = _c(query_start, np.int32)
+        out = np.empty(int(qs[-1]), np.int32)
+        self.lib.pa_oracle_chunk_slot_mapping(_p(bt), bt.shape[1], _p(cl), _p(qs), cl.shape[0],
+                                              block_size, _p(out))
+        return out
+
+    def prefill(self, q_bits, k_cache, v_cache, block_tables, context_lens, query_start,
+                num_kv_heads, block_size, softmax_scale, kv_dtype=0, kv_scale=1.0) -> np.ndarray:
+        """fp64 [Tq, Hq, D]: causal attention of every chunk token over its
+        sequence's cached tokens up to and including itself."""
+        q = _c(q_bits, np.uint16)
+        bt = _c(block_tables, np.int32)
+        cl = _c(context_lens, np.int32)
+        qs = _c(query_start, np.int32)
+        kc = np.ascontiguousarray(k_cache)
+        vc = np.ascontiguousarray(v_cache)
+        T, Hq, D = q.shape
+        out = np.zeros((T, Hq, D), np.float64)
+        self.lib.pa_oracle_prefill(_p(q), _p(kc), _p(vc), _p(bt), bt.shape[1], _p(cl), _p(qs),
+                                   cl.shape[0], Hq, num_kv_heads, D, block_size,
+                                   float(softmax_scale), kv_dtype, float(kv_scale), _p(out))
         return out
 
     # -- block allocation with copy-on-write ------------------------------------

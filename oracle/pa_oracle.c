@@ -450,6 +450,61 @@ void pa_oracle_decode_scaled(const uint16_t *q, const uint8_t *k_cache, const ui
 }
 
 /* ------------------------------------------------------------------------ */
+/* chunked prefill: many new tokens per sequence                             */
+/* ------------------------------------------------------------------------ */
+
+/* Slots of a chunk of new tokens.  Sequence s brings the
+ * C = query_start[s+1] - query_start[s] tokens at the end of its context
+ * (context_lens[s] counts them): row i of the chunk is logical position
+ * context_lens[s] - C + (i - query_start[s]); its slot is found through the
+ * block table as for a single token ("PagedAttention Mechanics"). */
+void pa_oracle_chunk_slot_mapping(const int32_t *block_tables, int max_blocks_per_seq,
+                                  const int32_t *context_lens, const int32_t *query_start,
+                                  int num_seqs, int block_size, int32_t *slot_mapping)
+{
+    for (int s = 0; s < num_seqs; ++s) {
+        int c = query_start[s + 1] - query_start[s];
+        for (int i = query_start[s]; i < query_start[s + 1]; ++i) {
+            int pos = context_lens[s] - c + (i - query_start[s]);
+            int32_t block = block_tables[(int64_t)s * max_blocks_per_seq + pos / block_size];
+            slot_mapping[i] = block * block_size + pos % block_size;
+        }
+    }
+}
+
+/* Chunked prefill attention: each new token attends to every token at or
+ * before its own position -- the cached prefix and the chunk's earlier
+ * tokens -- read through the block table (the chunk's own K/V are already
+ * in the cache).  q and out are [Tq][Hq][D] with the rows of sequence s at
+ * [query_start[s], query_start[s+1]); out is fp64. */
+void pa_oracle_prefill(const uint16_t *q, const void *k_cache, const void *v_cache,
+                       const int32_t *block_tables, int max_blocks_per_seq,
+                       const int32_t *context_lens, const int32_t *query_start, int num_seqs,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       double softmax_scale, int kv_dtype, double kv_scale, double *out)
+{
+    int group = num_q_heads / num_kv_heads;
+    int total = query_start[num_seqs];
+#pragma omp parallel for schedule(dynamic)
+    for (int i = 0; i < total; ++i) {
+        int s = 0;
+        while (query_start[s + 1] <= i)
+            ++s;
+        int c = query_start[s + 1] - query_start[s];
+        int pos = context_lens[s] - c + (i - query_start[s]);
+        double *x = (double *)malloc(sizeof(double) * (size_t)(context_lens[s] > 0 ? context_lens[s] : 1));
+        for (int hq = 0; hq < num_q_heads; ++hq) {
+            double m, l;
+            attend_range(q + ((int64_t)i * num_q_heads + hq) * head_dim, k_cache, v_cache,
+                         block_tables, max_blocks_per_seq, s, hq / group, 0, pos + 1,
+                         num_kv_heads, head_dim, block_size, softmax_scale, kv_dtype, kv_scale,
+                         kv_scale, x, out + ((int64_t)i * num_q_heads + hq) * head_dim, &m, &l);
+        }
+        free(x);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* block allocation for the newest tokens, with copy-on-write                */
 /* ------------------------------------------------------------------------ */
 

@@ -385,7 +385,51 @@ def pin_block_alloc(o):
     assert np.array_equal(st["tables"], t0) and np.array_equal(st["refc"], r0)
 
 
+def pin_prefill(o):
+    """Chunked prefill: a chunk covering the whole sequence is causal
+    attention (torch SDPA, is_causal); a chunk after a cached prefix is SDPA
+    with the mask 'key position <= query position'; the last token of every
+    chunk equals decode attention; chunk slots equal brute-force enumeration
+    and their last entry equals the newest-token slot."""
+    import torch.nn.functional as F
+    rng = np.random.default_rng(15)
+    for B, (Hq, Hkv) in ((16, (8, 2)), (4, (6, 3))):
+        ctx = [5, 40, 33, 17]
+        chunk = [5, 7, 1, 17]  # whole, after prefix, single token, whole (17 > B)
+        c = LogicalCase(ctx, Hq, Hkv, 16, seed=B + Hq)
+        tables, kc, vc = c.paged(B, 40, rng)
+        qs = np.concatenate([[0], np.cumsum(chunk)]).astype(np.int32)
+        g = torch.Generator().manual_seed(3)
+        q = torch.randn(int(qs[-1]), Hq, 16, generator=g).to(torch.bfloat16)
+        qb = q.view(torch.int16).numpy().view(np.uint16)
+        out = o.prefill(qb, kc, vc, tables, np.array(ctx), qs, Hkv, B, 0.3)
+        G = Hq // Hkv
+        for s_, (n, ch) in enumerate(zip(ctx, chunk)):
+            rows = slice(qs[s_], qs[s_ + 1])
+            qq = torch.from_numpy(bits_to_f64(qb[rows])).permute(1, 0, 2)[None]   # [1, Hq, ch, D]
+            k = torch.from_numpy(bits_to_f64(c.k[s_])).repeat_interleave(G, 0)[None]
+            v = torch.from_numpy(bits_to_f64(c.v[s_])).repeat_interleave(G, 0)[None]
+            qpos = torch.arange(n - ch, n)[:, None]
+            mask = torch.arange(n)[None, :] <= qpos
+            ref = F.scaled_dot_product_attention(qq, k, v, attn_mask=mask, scale=0.3)
+            if ch == n:
+                causal = F.scaled_dot_product_attention(qq, k, v, is_causal=True, scale=0.3)
+                assert torch.allclose(ref, causal, atol=1e-12)
+            got = out[rows].transpose(1, 0, 2)[None]
+            assert np.abs(got - ref.numpy()).max() < 1e-12
+        # the last chunk token is the decode token
+        last = qs[1:] - 1
+        dec = o.decode(qb[last], kc, vc, tables, np.array(ctx), Hkv, B, 0.3)
+        assert np.array_equal(out[last], dec)
+        # slots
+        slots = o.chunk_slot_mapping(tables, np.array(ctx), qs, B)
+        for s_, (n, ch) in enumerate(zip(ctx, chunk)):
+            allslots = [int(b) * B + off for b in tables[s_] if b >= 0 for off in range(B)][:n]
+            assert slots[qs[s_]:qs[s_ + 1]].tolist() == allslots[n - ch:]
+        assert np.array_equal(slots[last], o.slot_mapping(tables, np.array(ctx), B))
+
+
 ALL = [pin_kv_formula, pin_e4m3_decode, pin_e4m3_encode, pin_e4m3_roundtrip, pin_attention_sdpa,
        pin_attention_fp8, pin_extreme_scores, pin_permutation, pin_prefix_sharing, pin_context_one,
        pin_identical_keys, pin_empty_context, pin_slot_mapping, pin_append_readback,
-       pin_partition_merge, pin_fp8_per_head_scales, pin_block_alloc]
+       pin_partition_merge, pin_fp8_per_head_scales, pin_block_alloc, pin_prefill]

@@ -37,6 +37,12 @@ MUTANTS = {
     "alloc_stack_bottom": ("int32_t fresh = free_blocks[top - 1 - taken];", "int32_t fresh = free_blocks[taken];"),
     "alloc_no_release": ("refcounts[old] -= 1;", "refcounts[old] -= 0;"),
     "alloc_no_push": ("freed[nfreed++] = cow_src[s];", "(void)0;"),
+    "prefill_not_causal": ("s, hq / group, 0, pos + 1,", "s, hq / group, 0, context_lens[s],"),
+    "prefill_strict_causal": ("s, hq / group, 0, pos + 1,", "s, hq / group, 0, pos + (pos > 0),"),
+    "prefill_chunk_offset": ("int pos = context_lens[s] - c + (i - query_start[s]);\n        double *x",
+                             "int pos = context_lens[s] - c + (i - query_start[s]) - (c > 1);\n        double *x"),
+    "chunk_slots_shifted": ("int pos = context_lens[s] - c + (i - query_start[s]);\n            int32_t block",
+                            "int pos = context_lens[s] - c + (i - query_start[s]) + 1 - (i == query_start[s + 1] - 1);\n            int32_t block"),
     "partition_short": ("int t1 = t0 + partition_size;", "int t1 = t0 + partition_size - 1;"),
     "last_token_dropped": ("attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s],",
                            "attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s] - (context_lens[s] > 1),"),
