@@ -80,6 +80,8 @@ def parse():
     ap.add_argument("--device-alloc", action="store_true",
                     help="each step first advances every context by one token and allocates "
                          "blocks on the device (pa_block_alloc), then runs the step")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time chunked prefill (16 sequences x 512-token chunks) instead of decode")
     ap.add_argument("--separate", action="store_true",
                     help="time the unfused entry points (3-4 kernels per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -616,10 +618,96 @@ def run_reference(args):
     print(json.dumps(result), flush=True)
 
 
+def run_prefill(args):
+    """Chunked prefill step: chunk slots, append of the chunk's K/V, causal
+    attention over the paged cache.  value = attention TFLOP/s (QK^T and PV
+    over the (query, key) pairs the causal mask keeps)."""
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    from paged_kv_cache_193_gb300 import api
+    wl = W.make_prefill(device, num_seqs=args.num_seqs or 16)
+    sh = wl.shape
+    bt = torch.from_numpy(wl.block_tables).to(device)
+    cl = torch.from_numpy(wl.context_lens).to(device)
+    qs = torch.from_numpy(wl.query_start).to(device)
+    T = int(wl.query_start[-1])
+    slots = torch.empty(T, dtype=torch.int32, device=device)
+    out = torch.empty_like(wl.q)
+    mq = wl.max_query_len
+    stream = torch.cuda.current_stream()
+
+    def step():
+        api.chunk_slot_mapping(bt, cl, qs, sh.block_size, out=slots)
+        api.cache_append(wl.k_new, wl.v_new, slots, wl.k_cache, wl.v_cache)
+        api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, mq, wl.softmax_scale, out=out)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_w = time.time()
+    done = 0
+    while done < args.warmup or time.time() - t_w < args.min_warmup_seconds:
+        step()
+        done += 1
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(K):
+        ev[i][0].record(stream)
+        api.chunk_slot_mapping(bt, cl, qs, sh.block_size, out=slots)
+        api.cache_append(wl.k_new, wl.v_new, slots, wl.k_cache, wl.v_cache)
+        kev[i][0].record(stream)
+        api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, mq, wl.softmax_scale, out=out)
+        kev[i][1].record(stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    clocks.stop()
+    assert api.device_errors() == 0
+    step_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev])), world, device)
+    kern_ms = float(np.mean([a.elapsed_time(b) for a, b in kev]))
+    flops = wl.attention_flops()
+    peaks, kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    achieved = flops / (kern_ms / 1e3) / 1e12
+    res = {
+        "metric": "paged chunked-prefill attention TFLOP/s", "value": round(world * flops / (step_ms / 1e3) / 1e12, 2),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled block tables)",
+        "config": {"workload": f"chunked prefill: {sh.num_seqs} seqs x {mq}-token chunks after "
+                               f"cached prefixes U[0,2048], {sh.num_q_heads}q/{sh.num_kv_heads}kv heads, "
+                               f"head_dim {sh.head_dim}, block {sh.block_size}, bf16",
+                   "chunk_tokens": T, "attention_flops_per_step": flops, "seed": wl.seed,
+                   "l2": f"KV pool {2 * wl.k_cache.numel() * 2 / 1e9:.2f} GB"},
+        "tokens_per_s": round(world * T / (step_ms / 1e3), 1),
+        "breakdown_ms": {"prefill_kernel": round(kern_ms, 5),
+                         "slots+append": round(step_ms - kern_ms, 5)},
+        "gpu_launches": 3 * K,
+        "roofline": {"bound": "tensor", "kernel": "prefill_kernel (mma.sync m16n8k16)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4),
+                     "peak_kind": f"{kind} cuBLAS bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
+                     "traffic": None},
+        "clocks": clocks.summary(t0 - 1.0, t1),
+    }
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.prefill:
+        run_prefill(args)
     else:
         run_ours(args)
 

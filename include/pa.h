@@ -282,6 +282,39 @@ pa_status pa_block_alloc(int32_t *block_tables, int max_blocks_per_seq, int32_t 
                          int32_t *cow_src, cudaStream_t stream);
 
 /*
+ * pa_chunk_slot_mapping / pa_prefill -- chunked prefill over the paged cache.
+ * Chunked prefill is named in the first page's "Production Checklist" and in
+ * Step 2 of the tuning guide; the attention walks the block table as the
+ * decode does (fourth page, section 2).
+ * Sequence s brings C_s = query_start[s+1] - query_start[s] new tokens at the
+ * END of its context: context_lens[s] >= C_s counts them, and chunk row i
+ * (query_start[s] <= i < query_start[s+1]) is logical position
+ * p_i = context_lens[s] - C_s + (i - query_start[s]).
+ *   query_start  int32 [num_seqs + 1] (device), query_start[0] = 0.
+ * pa_chunk_slot_mapping: slot_mapping[i] = slot of position p_i (int32
+ *   [query_start[num_seqs]] output), for pa_cache_append of the chunk's K/V.
+ * pa_prefill: for every chunk row i and query head hq,
+ *   out[i][hq] = bf16_rn( softmax_{t <= p_i}(softmax_scale * q[i][hq] . K[t])
+ *                         . V ),  K/V of KV head hq / group, t over the
+ *   sequence's logical tokens 0..p_i through the block table (the chunk's
+ *   own K/V must already be in the cache).
+ *   q, out bf16 [query_start[num_seqs]][num_q_heads][head_dim].
+ *   max_query_len >= every C_s (host-side bound used for the grid).
+ *   Supported: bf16 cache, group 1, 2, 4, 8 or 16, head_dim 64/128, block 16/32.
+ *   One kernel (tensor-core MMA, TMA page loads).  kv_scale is unused.
+ */
+pa_status pa_chunk_slot_mapping(const int32_t *block_tables, int max_blocks_per_seq,
+                                const int32_t *context_lens, const int32_t *query_start,
+                                int num_seqs, int block_size, int32_t *slot_mapping,
+                                cudaStream_t stream);
+pa_status pa_prefill(const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_tables, int max_blocks_per_seq,
+                     const int32_t *context_lens, const int32_t *query_start, int num_seqs,
+                     int max_query_len, int num_q_heads, int num_kv_heads, int head_dim,
+                     int num_blocks, int block_size, pa_kv_dtype kv_dtype, float kv_scale,
+                     float softmax_scale, void *out, cudaStream_t stream);
+
+/*
  * pa_decode_static_workspace -- pa_decode with partition_size > 0, without
  * the caller's workspace.
  * The source pages have no counterpart to this entry point.  It exists for

@@ -240,6 +240,46 @@ def decode_step_scaled(q, k_new, v_new, k_cache, v_cache, block_tables, context_
     return out
 
 
+def chunk_slot_mapping(block_tables, context_lens, query_start, block_size, out=None,
+                       stream=None) -> torch.Tensor:
+    """int32 slots of every chunk token (chunks end their contexts)."""
+    _need(block_tables, "block_tables", (torch.int32,), 2)
+    _need(context_lens, "context_lens", (torch.int32,), 1)
+    _need(query_start, "query_start", (torch.int32,), 1)
+    S, MB = block_tables.shape
+    if out is None:
+        out = torch.empty(int(query_start[-1].item()), dtype=torch.int32, device=block_tables.device)
+    _check(_lib_handle().pa_chunk_slot_mapping(block_tables.data_ptr(), MB, context_lens.data_ptr(),
+                                               query_start.data_ptr(), S, block_size,
+                                               out.data_ptr(), _stream(stream)))
+    return out
+
+
+def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, max_query_len,
+            softmax_scale=None, out=None, stream=None) -> torch.Tensor:
+    """Chunked prefill attention: bf16 [T, Hq, D] for the chunk rows q."""
+    _need(q, "q", (torch.bfloat16,), 3)
+    _need(query_start, "query_start", (torch.int32,), 1)
+    kv_dtype = cache_dtype_of(k_cache)
+    _need(k_cache, "k_cache", _CACHE_DTYPES[kv_dtype], 4)
+    _need(v_cache, "v_cache", _CACHE_DTYPES[kv_dtype], 4)
+    _need(block_tables, "block_tables", (torch.int32,), 2)
+    _need(context_lens, "context_lens", (torch.int32,), 1)
+    T, Hq, D = q.shape
+    NB, Hkv, B, _ = k_cache.shape
+    S = context_lens.shape[0]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(_lib_handle().pa_prefill(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                    block_tables.data_ptr(), block_tables.shape[1],
+                                    context_lens.data_ptr(), query_start.data_ptr(), S,
+                                    int(max_query_len), Hq, Hkv, D, NB, B, kv_dtype, 1.0,
+                                    float(softmax_scale), out.data_ptr(), _stream(stream)))
+    return out
+
+
 class DeviceBlockPool:
     """Device-side free stack and reference counts of a paged cache's blocks,
     driven by ``pa_block_alloc``.  Build it from the host state once

@@ -582,8 +582,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // Tensor map over a cache viewed as [num_blocks * num_kv_heads * block_size
 // rows][head_dim], one box = [block_size rows][min(row bytes, 128) bytes].
-static pa_status make_map(CUtensorMap *map, const void *cache, bool fp8, int head_dim,
-                          int64_t rows, int block_size) {
+pa_status make_map(CUtensorMap *map, const void *cache, bool fp8, int head_dim, int64_t rows,
+                   int block_size) {
     auto fn = encode_fn();
     if (!fn) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const int elem = fp8 ? 1 : 2;

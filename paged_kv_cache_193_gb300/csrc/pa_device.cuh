@@ -31,6 +31,12 @@ pa_status launch_reduce(const void *workspace, const int32_t *context_lens, int 
                         int num_q_heads, int head_dim, int partition_size, int max_partitions,
                         void *out, cudaStream_t stream);
 
+// Tensor map over a KV cache viewed as [num_blocks * num_kv_heads *
+// block_size rows][head_dim]; one box is [block_size rows][min(row bytes,
+// 128) bytes] with the hardware swizzle matching that width.
+pa_status make_map(CUtensorMap *map, const void *cache, bool fp8, int head_dim, int64_t rows,
+                   int block_size);
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ---------------------------------------------------------------------------
@@ -214,6 +220,20 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Shared-memory address of byte b of token row t in a page tile laid down
+// by the TMA with the swizzle matching SLAB (the box width in bytes): the
+// 16-byte chunk c of a 128-byte row lands at c ^ (t & 7), of a 64-byte row
+// at c ^ ((t >> 1) & 3); wider rows are split into SLAB-wide column slabs
+// of BS rows each.
+template <int SLAB, int BS>
+__device__ __forceinline__ uint32_t swz_addr(uint32_t base, int t, int b) {
+    const int slab = b / SLAB;
+    const int within = b % SLAB;
+    const int chunk = within >> 4;
+    const int phys = SLAB == 128 ? (chunk ^ (t & 7)) : (chunk ^ ((t >> 1) & 3));
+    return base + slab * (BS * SLAB) + t * SLAB + (phys << 4) + (within & 15);
 }
 
 __device__ __forceinline__ void set_device_error(unsigned int *err, unsigned int bits) {

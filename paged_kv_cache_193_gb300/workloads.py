@@ -328,3 +328,88 @@ def sample_pairs(wl: Workload, n: int, seed: int = 1234) -> np.ndarray:
         picks.add(int(rng.integers(0, total)))
     flat = np.array(sorted(picks), np.int64)
     return np.stack([flat // Hq, flat % Hq], axis=1).astype(np.int32)
+
+
+@dataclass
+class PrefillWorkload:
+    """One chunked-prefill step: sequence s brings the chunk rows
+    [query_start[s], query_start[s+1]) at the end of its context; the cache
+    holds the prefix, the chunk's own K/V are ``k_new``/``v_new``."""
+
+    shape: Shape
+    num_blocks: int
+    context_lens: np.ndarray      # int32 [S], prefix + chunk
+    query_start: np.ndarray       # int32 [S + 1]
+    block_tables: np.ndarray      # int32 [S, MB]
+    q: torch.Tensor               # bf16 [T, Hq, D]
+    k_new: torch.Tensor           # bf16 [T, Hkv, D]
+    v_new: torch.Tensor
+    k_cache: torch.Tensor         # bf16 [NB, Hkv, B, D]
+    v_cache: torch.Tensor
+    softmax_scale: float
+    seed: int = 0
+
+    @property
+    def max_query_len(self) -> int:
+        return int(np.diff(self.query_start).max()) if len(self.context_lens) else 0
+
+    def attention_flops(self) -> int:
+        """Multiply-adds x2 of QK^T and PV over the (query, key) pairs the
+        causal mask keeps: 4 * D * Hq per pair."""
+        sh = self.shape
+        pairs = 0
+        for s in range(sh.num_seqs):
+            n = int(self.context_lens[s])
+            c = int(self.query_start[s + 1] - self.query_start[s])
+            pairs += sum(n - c + i + 1 for i in range(c))
+        return 4 * sh.head_dim * sh.num_q_heads * pairs
+
+
+def make_prefill(device="cpu", seed: int = 5, num_seqs: int = 16, chunk: int | list = 512,
+                 max_prefix: int = 2048, num_q_heads: int = 32, num_kv_heads: int = 8,
+                 head_dim: int = 128, block_size: int = 16, prefixes=None) -> PrefillWorkload:
+    """Chunked prefill of a Llama-3-8B-shaped layer: ``num_seqs`` sequences
+    with cached prefixes uniform on [0, max_prefix] each bring a chunk of
+    ``chunk`` new tokens (16 x 512 = 8192 tokens per step, the batched-token
+    budget the pages suggest as a starting point)."""
+    rng = np.random.default_rng(seed)
+    S = num_seqs
+    chunks = np.array(chunk if isinstance(chunk, (list, tuple)) else [chunk] * S, np.int64)
+    pre = (np.array(prefixes, np.int64) if prefixes is not None
+           else rng.integers(0, max_prefix, size=S, endpoint=True))
+    ctx = pre + chunks
+    B = block_size
+    need = sum(_blocks_for(int(c), B) for c in ctx)
+    nb = math.ceil(1.2 * need) + 4
+    tables, _ = build_tables(ctx, B, nb, rng)
+    shape = Shape(S, num_q_heads, num_kv_heads, head_dim, B)
+    g = _generator(seed, device)
+    T = int(chunks.sum())
+    q = _randn_bf16((T, num_q_heads, head_dim), g, device)
+    k_new = _randn_bf16((T, num_kv_heads, head_dim), g, device)
+    v_new = _randn_bf16((T, num_kv_heads, head_dim), g, device)
+    kc = _randn_bf16((nb, num_kv_heads, B, head_dim), g, device)
+    vc = _randn_bf16((nb, num_kv_heads, B, head_dim), g, device)
+    qs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    return PrefillWorkload(shape=shape, num_blocks=nb, context_lens=ctx.astype(np.int32),
+                           query_start=qs, block_tables=tables, q=q, k_new=k_new, v_new=v_new,
+                           k_cache=kc, v_cache=vc, softmax_scale=1.0 / math.sqrt(head_dim),
+                           seed=seed)
+
+
+def poison_prefill(wl: PrefillWorkload) -> None:
+    """NaN in every cache row outside the sequences' contexts, and in the
+    chunk rows (which the step's append must write first)."""
+    sh = wl.shape
+    B = sh.block_size
+    live = np.zeros((wl.num_blocks, B), bool)
+    for s in range(sh.num_seqs):
+        n = int(wl.context_lens[s])
+        c = int(wl.query_start[s + 1] - wl.query_start[s])
+        for t in range(n - c):
+            live[wl.block_tables[s, t // B], t % B] = True
+    dead = torch.from_numpy(~live).to(wl.k_cache.device)
+    mask = dead[:, None, :, None].expand(-1, sh.num_kv_heads, -1, sh.head_dim)
+    fill = torch.tensor(np.int16(np.uint16(BF16_NAN_BITS).view(np.int16)), device=wl.k_cache.device)
+    for c_ in (wl.k_cache, wl.v_cache):
+        c_.view(torch.int16).masked_fill_(mask, fill)

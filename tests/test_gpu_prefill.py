@@ -1,0 +1,103 @@
+"""Chunked prefill through the C ABI: chunk slots and the chunk's append bit
+for bit, attention within tolerance of the oracle's causal definition."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import compare
+from paged_kv_cache_193_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api(cuda_device):
+    from paged_kv_cache_193_gb300 import api as a
+    a._lib_handle()
+    return a
+
+
+def _dev(wl, device):
+    return (torch.from_numpy(wl.block_tables).to(device), torch.from_numpy(wl.context_lens).to(device),
+            torch.from_numpy(wl.query_start).to(device))
+
+
+def _oracle_step(oracle, wl):
+    kc, vc = W.bits(wl.k_cache).copy(), W.bits(wl.v_cache).copy()
+    slots = oracle.chunk_slot_mapping(wl.block_tables, wl.context_lens, wl.query_start,
+                                      wl.shape.block_size)
+    oracle.cache_append(W.bits(wl.k_new), W.bits(wl.v_new), slots, kc, vc, wl.shape.block_size, 0, 1.0)
+    out = oracle.prefill(W.bits(wl.q), kc, vc, wl.block_tables, wl.context_lens, wl.query_start,
+                         wl.shape.num_kv_heads, wl.shape.block_size, wl.softmax_scale)
+    return slots, kc, vc, out
+
+
+def _gpu_step(api, wl, device):
+    bt, cl, qs = _dev(wl, device)
+    slots = api.chunk_slot_mapping(bt, cl, qs, wl.shape.block_size)
+    api.cache_append(wl.k_new, wl.v_new, slots, wl.k_cache, wl.v_cache)
+    out = api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, wl.max_query_len, wl.softmax_scale)
+    torch.cuda.synchronize()
+    return slots.cpu().numpy(), out
+
+
+@pytest.mark.parametrize("D,B,G,Hkv", [(128, 16, 4, 2), (128, 32, 8, 1), (64, 16, 16, 1),
+                                       (64, 32, 1, 3), (128, 16, 2, 2)])
+def test_prefill_matches_oracle(api, oracle, cuda_device, D, B, G, Hkv):
+    wl = W.make_prefill(cuda_device, seed=D + B + G, num_seqs=5, chunk=[1, 7, 64, 100, 33],
+                        prefixes=[0, 5, 33, 300, 16], num_q_heads=G * Hkv, num_kv_heads=Hkv,
+                        head_dim=D, block_size=B)
+    W.poison_prefill(wl)
+    api.device_errors(clear=True)
+    slots_ref, kc_ref, vc_ref, ref = _oracle_step(oracle, wl)
+    slots, out = _gpu_step(api, wl, cuda_device)
+    assert np.array_equal(slots, slots_ref)
+    assert np.array_equal(W.bits(wl.k_cache), kc_ref) and np.array_equal(W.bits(wl.v_cache), vc_ref)
+    compare(out, ref, what=f"prefill D{D} B{B} G{G}")
+    assert api.device_errors() == 0
+
+
+def test_prefill_last_row_is_decode(api, cuda_device):
+    """The last chunk token of every sequence computes what the decode
+    kernel computes for that context."""
+    wl = W.make_prefill(cuda_device, seed=2, num_seqs=6, chunk=48, max_prefix=700)
+    bt, cl, qs = _dev(wl, cuda_device)
+    slots = api.chunk_slot_mapping(bt, cl, qs, 16)
+    api.cache_append(wl.k_new, wl.v_new, slots, wl.k_cache, wl.v_cache)
+    out = api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, wl.max_query_len)
+    last = torch.from_numpy(wl.query_start[1:] - 1).long().to(cuda_device)
+    dec = api.decode(wl.q[last].contiguous(), wl.k_cache, wl.v_cache, bt, cl)
+    diff = (out[last].float() - dec.float()).abs().max().item()
+    assert diff <= 1e-2
+
+
+@pytest.mark.slow
+def test_prefill_workload_sampled(api, oracle, cuda_device):
+    """The 8192-token chunked-prefill workload: every row of three sequences
+    against the oracle."""
+    wl = W.make_prefill(cuda_device)
+    W.poison_prefill(wl)
+    pick = [0, 7, 15]
+    # oracle on those sequences only (compacted), before the GPU append
+    B = wl.shape.block_size
+    rows = [wl.block_tables[s, : (int(wl.context_lens[s]) + B - 1) // B] for s in pick]
+    used = np.unique(np.concatenate(rows))
+    remap = {int(b): i for i, b in enumerate(used)}
+    tables = np.full((len(pick), wl.block_tables.shape[1]), -1, np.int32)
+    for i, row in enumerate(rows):
+        tables[i, : len(row)] = [remap[int(b)] for b in row]
+    idx = torch.from_numpy(used.astype(np.int64)).to(cuda_device)
+    kc = W.bits(wl.k_cache.index_select(0, idx))
+    vc = W.bits(wl.v_cache.index_select(0, idx))
+    ctx = wl.context_lens[pick]
+    qs_all = wl.query_start
+    spans = [(int(qs_all[s]), int(qs_all[s + 1])) for s in pick]
+    qs = np.concatenate([[0], np.cumsum([b - a for a, b in spans])]).astype(np.int32)
+    sel = np.concatenate([np.arange(a, b) for a, b in spans])
+    slots = oracle.chunk_slot_mapping(tables, ctx, qs, B)
+    oracle.cache_append(W.bits(wl.k_new)[sel], W.bits(wl.v_new)[sel], slots, kc, vc, B, 0, 1.0)
+    ref = oracle.prefill(W.bits(wl.q)[sel], kc, vc, tables, ctx, qs, wl.shape.num_kv_heads, B,
+                         wl.softmax_scale)
+    _, out = _gpu_step(api, wl, cuda_device)
+    compare(out[torch.from_numpy(sel).to(cuda_device)], ref, what="prefill workload")
+    assert api.device_errors() == 0
