@@ -672,6 +672,15 @@ def run_prefill(args):
     assert api.device_errors() == 0
     step_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev])), world, device)
     kern_ms = float(np.mean([a.elapsed_time(b) for a, b in kev]))
+    # the warp-level MMA kernel on the same inputs, for comparison
+    mev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(min(K, 50))]
+    for a_, b_ in mev:
+        a_.record(stream)
+        api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, mq, wl.softmax_scale, out=out,
+                    kernel="mma")
+        b_.record(stream)
+    torch.cuda.synchronize()
+    mma_ms = float(np.mean([a_.elapsed_time(b_) for a_, b_ in mev]))
     flops = wl.attention_flops()
     peaks, kind = measured_peaks()
     peak = float(peaks.get("bf16_tflops", 1900.0))
@@ -689,9 +698,11 @@ def run_prefill(args):
                    "l2": f"KV pool {2 * wl.k_cache.numel() * 2 / 1e9:.2f} GB"},
         "tokens_per_s": round(world * T / (step_ms / 1e3), 1),
         "breakdown_ms": {"prefill_kernel": round(kern_ms, 5),
-                         "slots+append": round(step_ms - kern_ms, 5)},
+                         "slots+append": round(step_ms - kern_ms, 5),
+                         "prefill_kernel_warp_mma": round(mma_ms, 5)},
+        "warp_mma_kernel_tflops": round(flops / (mma_ms / 1e3) / 1e12, 1),
         "gpu_launches": 3 * K,
-        "roofline": {"bound": "tensor", "kernel": "prefill_kernel (mma.sync m16n8k16)",
+        "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel (tcgen05, TMEM accumulators)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
                      "peak_kind": f"{kind} cuBLAS bf16 burst (MEASURED_PEAKS.json bf16_tflops)",

@@ -298,10 +298,14 @@ pa_status pa_block_alloc(int32_t *block_tables, int max_blocks_per_seq, int32_t 
  *                         . V ),  K/V of KV head hq / group, t over the
  *   sequence's logical tokens 0..p_i through the block table (the chunk's
  *   own K/V must already be in the cache).
- *   q, out bf16 [query_start[num_seqs]][num_q_heads][head_dim].
+ *   q, out bf16 [num_tokens][num_q_heads][head_dim], num_tokens =
+ *   query_start[num_seqs] (the host's count of chunk rows).
  *   max_query_len >= every C_s (host-side bound used for the grid).
  *   Supported: bf16 cache, group 1, 2, 4, 8 or 16, head_dim 64/128, block 16/32.
- *   One kernel (tensor-core MMA, TMA page loads).  kv_scale is unused.
+ *   One kernel: for head_dim 128 on the tcgen05 tensor cores (accumulators
+ *   in tensor memory), otherwise with warp-level MMA.  kv_scale is unused.
+ * pa_prefill_mma: the same computation always with the warp-level MMA
+ *   kernel (kept as the comparison point for the tensor-memory kernel).
  */
 pa_status pa_chunk_slot_mapping(const int32_t *block_tables, int max_blocks_per_seq,
                                 const int32_t *context_lens, const int32_t *query_start,
@@ -310,9 +314,15 @@ pa_status pa_chunk_slot_mapping(const int32_t *block_tables, int max_blocks_per_
 pa_status pa_prefill(const void *q, const void *k_cache, const void *v_cache,
                      const int32_t *block_tables, int max_blocks_per_seq,
                      const int32_t *context_lens, const int32_t *query_start, int num_seqs,
-                     int max_query_len, int num_q_heads, int num_kv_heads, int head_dim,
-                     int num_blocks, int block_size, pa_kv_dtype kv_dtype, float kv_scale,
-                     float softmax_scale, void *out, cudaStream_t stream);
+                     int num_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
+                     int head_dim, int num_blocks, int block_size, pa_kv_dtype kv_dtype,
+                     float kv_scale, float softmax_scale, void *out, cudaStream_t stream);
+pa_status pa_prefill_mma(const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *context_lens, const int32_t *query_start, int num_seqs,
+                         int num_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
+                         int head_dim, int num_blocks, int block_size, pa_kv_dtype kv_dtype,
+                         float kv_scale, float softmax_scale, void *out, cudaStream_t stream);
 
 /*
  * pa_decode_static_workspace -- pa_decode with partition_size > 0, without

@@ -47,7 +47,10 @@ SIGNATURES = {
                                    _P, _F, _I, _P, _SZ, _P, _P, _P]),
     "pa_block_alloc": (_I, [_P, _I, _P, _I, _I, _I, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P]),
     "pa_chunk_slot_mapping": (_I, [_P, _I, _P, _P, _I, _I, _P, _P]),
-    "pa_prefill": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _F, _P, _P]),
+    "pa_prefill": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _F, _P,
+                        _P]),
+    "pa_prefill_mma": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _F,
+                            _P, _P]),
     "pa_decode_static_workspace": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                         _F, _I, _P, _P]),
     "pa_device_errors": (_I, [ctypes.POINTER(ctypes.c_uint), _I]),

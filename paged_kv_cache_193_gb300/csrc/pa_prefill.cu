@@ -335,6 +335,20 @@ static pa_status launch_prefill(const CUtensorMap &tk, const CUtensorMap &tv, co
     return cuda_check(cudaGetLastError(), "prefill launch");
 }
 
+pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, const int32_t *query_start, int num_seqs,
+                            int total_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
+                            int num_blocks, int block_size, float softmax_scale, void *out,
+                            unsigned int *err, cudaStream_t stream);
+static pa_status prefill_impl(const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, const int32_t *query_start,
+                              int num_seqs, int num_tokens, int max_query_len, int num_q_heads,
+                              int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                              pa_kv_dtype kv_dtype, float kv_scale, float softmax_scale,
+                              void *out, cudaStream_t stream, bool tensor_memory);
+
 }  // namespace pa
 
 using namespace pa;
@@ -363,13 +377,42 @@ pa_status pa_chunk_slot_mapping(const int32_t *block_tables, int max_blocks_per_
 pa_status pa_prefill(const void *q, const void *k_cache, const void *v_cache,
                      const int32_t *block_tables, int max_blocks_per_seq,
                      const int32_t *context_lens, const int32_t *query_start, int num_seqs,
-                     int max_query_len, int num_q_heads, int num_kv_heads, int head_dim,
-                     int num_blocks, int block_size, pa_kv_dtype kv_dtype, float kv_scale,
-                     float softmax_scale, void *out, cudaStream_t stream) {
+                     int num_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
+                     int head_dim, int num_blocks, int block_size, pa_kv_dtype kv_dtype,
+                     float kv_scale, float softmax_scale, void *out, cudaStream_t stream) {
+    return prefill_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                        query_start, num_seqs, num_tokens, max_query_len, num_q_heads,
+                        num_kv_heads, head_dim, num_blocks, block_size, kv_dtype, kv_scale,
+                        softmax_scale, out, stream, true);
+}
+
+pa_status pa_prefill_mma(const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *context_lens, const int32_t *query_start, int num_seqs,
+                         int num_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
+                         int head_dim, int num_blocks, int block_size, pa_kv_dtype kv_dtype,
+                         float kv_scale, float softmax_scale, void *out, cudaStream_t stream) {
+    return prefill_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                        query_start, num_seqs, num_tokens, max_query_len, num_q_heads,
+                        num_kv_heads, head_dim, num_blocks, block_size, kv_dtype, kv_scale,
+                        softmax_scale, out, stream, false);
+}
+
+}  // extern "C"
+
+namespace pa {
+
+static pa_status prefill_impl(const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, const int32_t *query_start,
+                              int num_seqs, int num_tokens, int max_query_len, int num_q_heads,
+                              int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                              pa_kv_dtype kv_dtype, float kv_scale, float softmax_scale,
+                              void *out, cudaStream_t stream, bool tensor_memory) {
     clear_error();
     (void)kv_scale;
-    if (num_seqs < 0 || max_query_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
-        num_blocks <= 0 || max_blocks_per_seq <= 0)
+    if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || num_q_heads <= 0 ||
+        num_kv_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
         return fail(PA_ERR_INVALID_ARG, "bad size");
     if (num_q_heads % num_kv_heads != 0)
         return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d",
@@ -387,11 +430,18 @@ pa_status pa_prefill(const void *q, const void *k_cache, const void *v_cache,
         return fail(PA_ERR_UNSUPPORTED, "pool exceeds 2^31 rows");
     if (num_seqs > 65535 || num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "grid too large");
     if (!isfinite(softmax_scale)) return fail(PA_ERR_INVALID_ARG, "softmax_scale is not finite");
-    if (num_seqs == 0 || max_query_len == 0) return PA_OK;
+    if (num_seqs == 0 || max_query_len == 0 || num_tokens == 0) return PA_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start || !out)
         return fail(PA_ERR_INVALID_ARG, "null pointer");
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return fail(PA_ERR_INVALID_ARG, "q, caches and out must be 16-byte aligned");
+    unsigned int *err0 = device_error_word();
+    if (!err0) return fail(PA_ERR_CUDA, "cannot resolve the device error word");
+    if (tensor_memory && head_dim == 128)
+        return launch_prefill_tc(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                 context_lens, query_start, num_seqs, num_tokens, max_query_len,
+                                 num_q_heads, num_kv_heads, num_blocks, block_size, softmax_scale,
+                                 out, err0, stream);
     const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
     CUtensorMap tk, tv;
     pa_status st = make_map(&tk, k_cache, false, head_dim, rows, block_size);
@@ -422,4 +472,4 @@ pa_status pa_prefill(const void *q, const void *k_cache, const void *v_cache,
                             : launch_prefill<64, 32>(tk, tv, a, grid, stream);
 }
 
-}  // extern "C"
+}  // namespace pa

@@ -1,0 +1,431 @@
+// Chunked prefill on the 5th-generation tensor cores (tcgen05, tensor memory).
+//
+// Same computation as pa_prefill.cu (causal attention of each chunk token over
+// its sequence's cached prefix and earlier chunk tokens, through the block
+// table), organised for sm_103a's asynchronous tensor cores:
+//  * One CTA per (query tile of 128 rows = (chunk token, query head of the KV
+//    head's group) pairs, KV head, sequence), one CTA per SM (192 KB of
+//    shared memory, 384 of the 512 TMEM columns).
+//  * Warp 4 (one lane) streams the tile's queries (one 3-D TMA box per
+//    64-dim slab) and, per block of 128 keys, the K and V pages of the KV
+//    head (2-D TMA boxes, hardware 128-byte swizzle) into two K and two V
+//    stages.
+//  * Warp 5 owns the tensor memory and one lane issues the MMAs:
+//    S = Q K^T (M 128 x N 128 x K 128, both operands K-major) into one of two
+//    S accumulators, and O += P V (P K-major from shared memory, V read
+//    MN-major straight from the page layout) into the O accumulator; each
+//    group is committed to an mbarrier.
+//  * Warps 0-3 (one query row per thread, TMEM lane = row) read S, apply the
+//    causal mask, keep the running max and sum of their row, rescale O in
+//    tensor memory when the max moved, and write P (bf16) to shared memory.
+//    While they work on block j the tensor cores compute S for block j + 1.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <atomic>
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+struct PrefillTcArgs {
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    const int32_t *query_start;
+    int max_blocks;
+    int num_blocks;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;
+    int tile_tokens;  // 128 / group
+    float score_scale;
+    __nv_bfloat16 *out;
+    unsigned int *err;
+};
+
+constexpr int kTcRows = 128;          // query rows per tile (TMEM lanes)
+constexpr int kTcKeys = 128;          // keys per block
+constexpr int kTcThreads = 192;       // warps 0-3 softmax, 4 loads, 5 MMA
+constexpr int kTcSlab = 16384;        // one 64-dim slab of 128 rows x 128 B
+constexpr int kTcTile = 2 * kTcSlab;  // 128 rows x 128 dims bf16
+constexpr int kTcQOff = 0;
+constexpr int kTcKOff = kTcTile;            // 2 stages
+constexpr int kTcVOff = kTcTile * 3;        // 2 stages
+constexpr int kTcPOff = kTcTile * 5;
+constexpr int kTcSmem = kTcTile * 6 + 1024;
+constexpr int kTcTmemCols = 512;            // S0 [0,128) S1 [128,256) O [256,384)
+constexpr uint64_t kTcWaitNs = 2000000000ull;
+
+template <int BS>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const PrefillTcArgs a) {
+    constexpr int NPG = kTcKeys / BS;  // pages per key block
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t q_full, o_done, p_full, drain;
+    __shared__ __align__(8) uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2];
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int failed_s;
+
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *base_ptr = smem_raw + (base - raw);
+
+    const int tile = gridDim.x - 1 - blockIdx.x;
+    const int h = blockIdx.y, s = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int q0 = a.query_start[s];
+    const int chunk = a.query_start[s + 1] - q0;
+    const int ctx = a.context_lens[s];
+    const int tok_begin = tile * a.tile_tokens;
+    if (tok_begin >= chunk) return;  // uniform: before any barrier or TMEM use
+    if (ctx > a.max_blocks * BS || ctx < chunk) {
+        if (tid == 0) set_device_error(a.err, PA_DEVERR_BAD_CONTEXT);
+        return;
+    }
+    const int tok_end = min(tok_begin + a.tile_tokens, chunk);
+    const int first_pos = ctx - chunk;
+    const int kend = first_pos + tok_end;               // keys [0, kend)
+    const int nkb = (kend + kTcKeys - 1) / kTcKeys;     // key blocks
+
+    if (tid == 0) {
+        mbar_init(smem_addr(&q_full), 1);
+        mbar_init(smem_addr(&o_done), 1);
+        mbar_init(smem_addr(&p_full), 4);
+        mbar_init(smem_addr(&drain), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_addr(&k_full[i]), 1);
+            mbar_init(smem_addr(&k_empty[i]), 1);
+            mbar_init(smem_addr(&v_full[i]), 1);
+            mbar_init(smem_addr(&v_empty[i]), 1);
+            mbar_init(smem_addr(&s_full[i]), 1);
+            mbar_init(smem_addr(&s_free[i]), 4);
+        }
+        failed_s = 0;
+        fence_barrier_init();
+        prefetch_tensormap(&tmQ);
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(&tmem_base_s)),
+                     "r"(kTcTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    auto fail = [&]() {
+        set_device_error(a.err, PA_DEVERR_TIMEOUT);
+        atomicExch(&failed_s, 1);
+    };
+
+    if (warp == 4) {
+        // ---------------- loads ----------------
+        const int32_t *bt = a.block_tables + static_cast<int64_t>(s) * a.max_blocks;
+        const int rows_total = a.num_blocks * a.num_kv_heads * BS;
+        const uint64_t policy = l2_evict_first_policy();
+        if (lane == 0) {
+            const uint32_t bar = smem_addr(&q_full);
+            mbar_arrive_expect_tx(bar, kTcTile);
+            for (int sl = 0; sl < 2; ++sl)
+                tma_load_3d(base + kTcQOff + sl * kTcSlab, &tmQ, sl * 64, h * a.group, q0 + tok_begin, bar);
+        }
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int st = kb & 1, use = kb >> 1;
+            // physical rows of this block's pages (pages past the keys: zero fill)
+            const int pg_idx = kb * NPG + lane;
+            int y = rows_total;
+            if (lane < NPG && pg_idx * BS < kend) {
+                const int blk = __ldg(bt + pg_idx);
+                if (blk >= 0 && blk < a.num_blocks)
+                    y = (blk * a.num_kv_heads + h) * BS;
+                else
+                    set_device_error(a.err, PA_DEVERR_BAD_BLOCK);
+            }
+            if (lane == 0) {
+                if (!mbar_wait_bounded(smem_addr(&k_empty[st]), (use & 1) ^ 1, kTcWaitNs)) fail();
+                mbar_arrive_expect_tx(smem_addr(&k_full[st]), kTcTile);
+            }
+            // lane pg holds page pg's row index
+#pragma unroll
+            for (int pg = 0; pg < NPG; ++pg) {
+                const int yy = __shfl_sync(0xffffffffu, y, pg);
+                if (lane == 0) {
+                    for (int sl = 0; sl < 2; ++sl)
+                        tma_load_2d(base + kTcKOff + st * kTcTile + sl * kTcSlab + pg * BS * 128, &tmK,
+                                    sl * 64, yy, smem_addr(&k_full[st]), policy);
+                }
+            }
+            if (lane == 0) {
+                if (!mbar_wait_bounded(smem_addr(&v_empty[st]), (use & 1) ^ 1, kTcWaitNs)) fail();
+                mbar_arrive_expect_tx(smem_addr(&v_full[st]), kTcTile);
+            }
+#pragma unroll
+            for (int pg = 0; pg < NPG; ++pg) {
+                const int yy = __shfl_sync(0xffffffffu, y, pg);
+                if (lane == 0) {
+                    for (int sl = 0; sl < 2; ++sl)
+                        tma_load_2d(base + kTcVOff + st * kTcTile + sl * kTcSlab + pg * BS * 128, &tmV,
+                                    sl * 64, yy, smem_addr(&v_full[st]), policy);
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------- MMA issue ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = tc_idesc_bf16(kTcRows, kTcKeys, 0, 0);
+            constexpr uint32_t idesc_pv = tc_idesc_bf16(kTcRows, 128, 0, 1);
+            const uint32_t tS[2] = {tmem, tmem + 128};
+            const uint32_t tO = tmem + 256;
+            bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, kTcWaitNs);
+            auto issue_pv = [&](int j) {
+                const int st = j & 1, use = j >> 1;
+                ok = ok && mbar_wait_bounded(smem_addr(&p_full), j & 1, kTcWaitNs);
+                ok = ok && mbar_wait_bounded(smem_addr(&v_full[st]), use & 1, kTcWaitNs);
+                tc_fence_after();
+                if (ok) {
+                    const uint32_t pbase = base + kTcPOff;
+                    const uint32_t vbase = base + kTcVOff + st * kTcTile;
+#pragma unroll
+                    for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                        const uint64_t ad = tc_smem_desc(pbase + (kk >> 2) * kTcSlab + (kk & 3) * 32, 16, 1024, 2);
+                        const uint64_t bd = tc_smem_desc(vbase + kk * 16 * 128, kTcSlab, 1024, 2);
+                        tc_mma_bf16(tO, ad, bd, idesc_pv, j > 0 || kk > 0);
+                    }
+                }
+                tc_commit(smem_addr(&o_done));
+                tc_commit(smem_addr(&v_empty[st]));
+            };
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int st = kb & 1, use = kb >> 1;
+                ok = ok && mbar_wait_bounded(smem_addr(&k_full[st]), use & 1, kTcWaitNs);
+                ok = ok && mbar_wait_bounded(smem_addr(&s_free[st]), (use & 1) ^ 1, kTcWaitNs);
+                tc_fence_after();
+                if (ok) {
+                    const uint32_t qbase = base + kTcQOff;
+                    const uint32_t kbase = base + kTcKOff + st * kTcTile;
+#pragma unroll
+                    for (int kk = 0; kk < 128 / 16; ++kk) {
+                        const uint64_t ad = tc_smem_desc(qbase + (kk >> 2) * kTcSlab + (kk & 3) * 32, 16, 1024, 2);
+                        const uint64_t bd = tc_smem_desc(kbase + (kk >> 2) * kTcSlab + (kk & 3) * 32, 16, 1024, 2);
+                        tc_mma_bf16(tS[st], ad, bd, idesc_qk, kk > 0);
+                    }
+                }
+                tc_commit(smem_addr(&s_full[st]));
+                tc_commit(smem_addr(&k_empty[st]));
+                if (kb >= 1) issue_pv(kb - 1);
+            }
+            issue_pv(nkb - 1);
+            if (!ok) fail();
+            // every MMA issued above is complete before the TMEM is released
+            tc_commit(smem_addr(&drain));
+            mbar_wait_bounded(smem_addr(&drain), 0, kTcWaitNs);
+        }
+    } else {
+        // ---------------- softmax: thread = query row ----------------
+        const int row = warp * 32 + lane;
+        const int t = row / a.group, g = row % a.group;
+        const bool live = tok_begin + t < tok_end;
+        const int pos = live ? first_pos + tok_begin + t : -1;
+        const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tO = tmem + lane_addr + 256;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int st = kb & 1, use = kb >> 1;
+            ok = ok && mbar_wait_bounded(smem_addr(&s_full[st]), use & 1, kTcWaitNs);
+            tc_fence_after();
+            float sv[kTcKeys];
+#pragma unroll
+            for (int c4 = 0; c4 < kTcKeys / 32; ++c4) {
+                float tmp[32];
+                tc_ld32(tmem + lane_addr + st * 128 + c4 * 32, tmp);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sv[c4 * 32 + i] = tmp[i];
+            }
+            tc_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&s_free[st]));
+            // mask + scale + running max / sum
+            const int key0 = kb * kTcKeys;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kTcKeys; ++i) {
+                float x = sv[i] * a.score_scale;
+                x = key0 + i <= pos ? x : -INFINITY;
+                sv[i] = x;
+                mx = fmaxf(mx, x);
+            }
+            const float m_new = fmaxf(m_run, mx);
+            const float m_use = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = fast_exp2(m_run - m_use);
+            m_run = m_new;
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < kTcKeys; ++i) {
+                sv[i] = fast_exp2(sv[i] - m_use);
+                sum += sv[i];
+            }
+            l_run = l_run * alpha + sum;
+            if (kb >= 1) {
+                // block kb-1's PV is done: O is final for it and P may be rewritten
+                ok = ok && mbar_wait_bounded(smem_addr(&o_done), (kb - 1) & 1, kTcWaitNs);
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        float ov[32];
+                        tc_ld32(tO + c4 * 32, ov);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+                        tc_st32(tO + c4 * 32, ov);
+                    }
+                    tc_wait_st();
+                }
+            }
+            // P row -> shared memory, K-major with the 128-byte swizzle
+            uint8_t *prow = base_ptr + kTcPOff + row * 128;
+#pragma unroll
+            for (int ch = 0; ch < kTcKeys / 8; ++ch) {
+                uint4 v;
+                v.x = pack2<false>(sv[ch * 8 + 0], sv[ch * 8 + 1]);
+                v.y = pack2<false>(sv[ch * 8 + 2], sv[ch * 8 + 3]);
+                v.z = pack2<false>(sv[ch * 8 + 4], sv[ch * 8 + 5]);
+                v.w = pack2<false>(sv[ch * 8 + 6], sv[ch * 8 + 7]);
+                const int slab = ch >> 3, c16 = ch & 7;
+                *reinterpret_cast<uint4 *>(prow + slab * kTcSlab + ((c16 ^ (row & 7)) << 4)) = v;
+            }
+            if (kend - key0 < kTcKeys) {
+                // keys past the context in the last block may hold anything:
+                // zero those V rows (0 x garbage could be NaN)
+                ok = ok && mbar_wait_bounded(smem_addr(&v_full[st]), use & 1, kTcWaitNs);
+                const int valid = kend - key0;
+                uint8_t *vbase = base_ptr + kTcVOff + st * kTcTile;
+                for (int r2 = valid + (tid & 127); r2 < kTcKeys; r2 += 128)
+                    for (int sl = 0; sl < 2; ++sl)
+                        for (int c16 = 0; c16 < 8; ++c16)
+                            *reinterpret_cast<uint4 *>(vbase + sl * kTcSlab + r2 * 128 + c16 * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                // every softmax warp zeroes before any arrives on p_full
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&p_full));
+        }
+        ok = ok && mbar_wait_bounded(smem_addr(&o_done), (nkb - 1) & 1, kTcWaitNs);
+        tc_fence_after();
+        if (!ok) fail();
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        __nv_bfloat16 *dst = a.out + ((static_cast<int64_t>(q0) + tok_begin + t) * a.num_q_heads +
+                                      h * a.group + g) * 128;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+            float ov[32];
+            tc_ld32(tO + c4 * 32, ov);
+            tc_wait_ld();
+            if (live && !failed_s) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                    uint4 v;
+                    v.x = pack2<false>(ov[i] * inv, ov[i + 1] * inv);
+                    v.y = pack2<false>(ov[i + 2] * inv, ov[i + 3] * inv);
+                    v.z = pack2<false>(ov[i + 4] * inv, ov[i + 5] * inv);
+                    v.w = pack2<false>(ov[i + 6] * inv, ov[i + 7] * inv);
+                    *reinterpret_cast<uint4 *>(dst + c4 * 32 + i) = v;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols)
+                     : "memory");
+    }
+}
+
+// Queries [Tq][Hq][D] as a 3-D tensor (D, Hq, Tq); one box is 64 dims x
+// `group` heads x `tile_tokens` tokens with the 128-byte swizzle.
+static pa_status make_q_map(CUtensorMap *map, const void *q, int total_tokens, int num_q_heads,
+                            int group, int tile_tokens) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) !=
+            cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess)
+        return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(num_q_heads), static_cast<cuuint64_t>(total_tokens)};
+    cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(num_q_heads) * 128 * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(tile_tokens)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box,
+                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (res != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "query tensor map failed (CUresult %d)", static_cast<int>(res));
+    return PA_OK;
+}
+
+template <int BS>
+static pa_status launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                           const PrefillTcArgs &a, dim3 grid, cudaStream_t stream) {
+    auto kern = prefill_tc_kernel<BS>;
+    static std::atomic<uint64_t> raised{0};
+    int dev = 0;
+    pa_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+    if (st != PA_OK) return st;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+    if (!bit || !(raised.load(std::memory_order_acquire) & bit)) {
+        st = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem),
+                        "cudaFuncSetAttribute(prefill tcgen05)");
+        if (st != PA_OK) return st;
+        raised.fetch_or(bit, std::memory_order_release);
+    }
+    kern<<<grid, kTcThreads, kTcSmem, stream>>>(tq, tk, tv, a);
+    return cuda_check(cudaGetLastError(), "prefill tcgen05 launch");
+}
+
+// Called by pa_prefill for head_dim 128 (arguments already checked).
+pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, const int32_t *query_start, int num_seqs,
+                            int total_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
+                            int num_blocks, int block_size, float softmax_scale, void *out,
+                            unsigned int *err, cudaStream_t stream) {
+    const int group = num_q_heads / num_kv_heads;
+    PrefillTcArgs a;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.query_start = query_start;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = group;
+    a.tile_tokens = kTcRows / group;
+    a.score_scale = softmax_scale * 1.4426950408889634f;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.err = err;
+    const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
+    CUtensorMap tq, tk, tv;
+    pa_status st = make_q_map(&tq, q, total_tokens, num_q_heads, group, a.tile_tokens);
+    if (st != PA_OK) return st;
+    st = make_map(&tk, k_cache, false, 128, rows, block_size);
+    if (st != PA_OK) return st;
+    st = make_map(&tv, v_cache, false, 128, rows, block_size);
+    if (st != PA_OK) return st;
+    dim3 grid((max_query_len + a.tile_tokens - 1) / a.tile_tokens, num_kv_heads, num_seqs);
+    return block_size == 16 ? launch_tc<16>(tq, tk, tv, a, grid, stream)
+                            : launch_tc<32>(tq, tk, tv, a, grid, stream);
+}
+
+}  // namespace pa

@@ -32,28 +32,31 @@ def _oracle_step(oracle, wl):
     return slots, kc, vc, out
 
 
-def _gpu_step(api, wl, device):
+def _gpu_step(api, wl, device, kernel="auto"):
     bt, cl, qs = _dev(wl, device)
     slots = api.chunk_slot_mapping(bt, cl, qs, wl.shape.block_size)
     api.cache_append(wl.k_new, wl.v_new, slots, wl.k_cache, wl.v_cache)
-    out = api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, wl.max_query_len, wl.softmax_scale)
+    out = api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, wl.max_query_len, wl.softmax_scale,
+                      kernel=kernel)
     torch.cuda.synchronize()
     return slots.cpu().numpy(), out
 
 
+@pytest.mark.parametrize("kernel", ["auto", "mma"])
 @pytest.mark.parametrize("D,B,G,Hkv", [(128, 16, 4, 2), (128, 32, 8, 1), (64, 16, 16, 1),
-                                       (64, 32, 1, 3), (128, 16, 2, 2)])
-def test_prefill_matches_oracle(api, oracle, cuda_device, D, B, G, Hkv):
-    wl = W.make_prefill(cuda_device, seed=D + B + G, num_seqs=5, chunk=[1, 7, 64, 100, 33],
+                                       (64, 32, 1, 3), (128, 16, 2, 2), (128, 16, 16, 1),
+                                       (128, 32, 1, 2)])
+def test_prefill_matches_oracle(api, oracle, cuda_device, D, B, G, Hkv, kernel):
+    wl = W.make_prefill(cuda_device, seed=D + B + G, num_seqs=5, chunk=[1, 7, 64, 300, 33],
                         prefixes=[0, 5, 33, 300, 16], num_q_heads=G * Hkv, num_kv_heads=Hkv,
                         head_dim=D, block_size=B)
     W.poison_prefill(wl)
     api.device_errors(clear=True)
     slots_ref, kc_ref, vc_ref, ref = _oracle_step(oracle, wl)
-    slots, out = _gpu_step(api, wl, cuda_device)
+    slots, out = _gpu_step(api, wl, cuda_device, kernel)
     assert np.array_equal(slots, slots_ref)
     assert np.array_equal(W.bits(wl.k_cache), kc_ref) and np.array_equal(W.bits(wl.v_cache), vc_ref)
-    compare(out, ref, what=f"prefill D{D} B{B} G{G}")
+    compare(out, ref, what=f"prefill {kernel} D{D} B{B} G{G}")
     assert api.device_errors() == 0
 
 
@@ -100,4 +103,8 @@ def test_prefill_workload_sampled(api, oracle, cuda_device):
                          wl.softmax_scale)
     _, out = _gpu_step(api, wl, cuda_device)
     compare(out[torch.from_numpy(sel).to(cuda_device)], ref, what="prefill workload")
+    bt, cl, qsd = _dev(wl, cuda_device)
+    out2 = api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qsd, wl.max_query_len,
+                       wl.softmax_scale, kernel="mma")
+    compare(out2[torch.from_numpy(sel).to(cuda_device)], ref, what="prefill workload (mma)")
     assert api.device_errors() == 0
