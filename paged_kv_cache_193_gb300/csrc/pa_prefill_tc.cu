@@ -4,21 +4,25 @@
 // its sequence's cached prefix and earlier chunk tokens, through the block
 // table), organised for sm_103a's asynchronous tensor cores:
 //  * One CTA per (query tile of 128 rows = (chunk token, query head of the KV
-//    head's group) pairs, KV head, sequence), one CTA per SM (192 KB of
+//    head's group) pairs, KV head, sequence), one CTA per SM (224 KB of
 //    shared memory, 384 of the 512 TMEM columns).
-//  * Warp 4 (one lane) streams the tile's queries (one 3-D TMA box per
+//  * Warp 8 (one lane) streams the tile's queries (one 3-D TMA box per
 //    64-dim slab) and, per block of 128 keys, the K and V pages of the KV
 //    head (2-D TMA boxes, hardware 128-byte swizzle) into two K and two V
 //    stages.
-//  * Warp 5 owns the tensor memory and one lane issues the MMAs:
+//  * Warp 9 owns the tensor memory and one lane issues the MMAs:
 //    S = Q K^T (M 128 x N 128 x K 128, both operands K-major) into one of two
 //    S accumulators, and O += P V (P K-major from shared memory, V read
 //    MN-major straight from the page layout) into the O accumulator; each
 //    group is committed to an mbarrier.
-//  * Warps 0-3 (one query row per thread, TMEM lane = row) read S, apply the
-//    causal mask, keep the running max and sum of their row, rescale O in
-//    tensor memory when the max moved, and write P (bf16) to shared memory.
-//    While they work on block j the tensor cores compute S for block j + 1.
+//  * Warps 0-7 do the softmax: a query row is TMEM lane (warp % 4) * 32 +
+//    lane, and warps w and w + 4 take its two 64-column halves (their
+//    partial maxima meet in shared memory once per block).  They read S,
+//    apply the causal mask, keep the row's sum against a reference max that
+//    only moves when the row max outgrows it by 2^8 (so O is rescaled in
+//    tensor memory rarely), and write P (bf16) to one of two P buffers.
+//    While they work on block j the tensor cores finish block j - 1's PV
+//    and compute S for block j + 1.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -45,14 +49,21 @@ struct PrefillTcArgs {
 
 constexpr int kTcRows = 128;          // query rows per tile (TMEM lanes)
 constexpr int kTcKeys = 128;          // keys per block
-constexpr int kTcThreads = 192;       // warps 0-3 softmax, 4 loads, 5 MMA
+constexpr int kTcThreads = 320;       // warps 0-7 softmax (2 per row), 8 loads, 9 MMA
+constexpr int kTcSoftmaxThreads = 256;
+constexpr int kTcLoadWarp = 8;
+constexpr int kTcMmaWarp = 9;
 constexpr int kTcSlab = 16384;        // one 64-dim slab of 128 rows x 128 B
 constexpr int kTcTile = 2 * kTcSlab;  // 128 rows x 128 dims bf16
 constexpr int kTcQOff = 0;
-constexpr int kTcKOff = kTcTile;            // 2 stages
-constexpr int kTcVOff = kTcTile * 3;        // 2 stages
-constexpr int kTcPOff = kTcTile * 5;
+constexpr int kTcKOff = kTcTile;            // 1 stage: QK retires long before the next K is due
+constexpr int kTcVOff = kTcTile * 2;        // 2 stages
+constexpr int kTcPOff = kTcTile * 4;        // 2 buffers
 constexpr int kTcSmem = kTcTile * 6 + 1024;
+// P is written against a reference max that only moves when the row max
+// grows past it by more than this (base-2 units): P <= 2^8, and O is
+// rescaled in tensor memory only then.
+constexpr float kTcRescaleThreshold = 8.f;
 constexpr int kTcTmemCols = 512;            // S0 [0,128) S1 [128,256) O [256,384)
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 
@@ -62,10 +73,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       const __grid_constant__ CUtensorMap tmV, const PrefillTcArgs a) {
     constexpr int NPG = kTcKeys / BS;  // pages per key block
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t q_full, o_done, p_full, drain;
-    __shared__ __align__(8) uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2];
+    __shared__ __align__(8) uint64_t q_full, o_done, drain;
+    __shared__ __align__(8) uint64_t k_full, k_empty, v_full[2], v_empty[2], s_full[2], s_free[2];
+    __shared__ __align__(8) uint64_t p_full[2], p_free[2];
     __shared__ uint32_t tmem_base_s;
     __shared__ int failed_s;
+    // per-row partial maxima of the two column halves, double-buffered by
+    // block parity so a fast half cannot overwrite a value its partner has
+    // not read yet
+    // (after the last block, the buffer it did not use carries the row sums)
+    __shared__ float half_max[2][2][kTcRows];
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -91,15 +108,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
         mbar_init(smem_addr(&q_full), 1);
         mbar_init(smem_addr(&o_done), 1);
-        mbar_init(smem_addr(&p_full), 4);
         mbar_init(smem_addr(&drain), 1);
+        mbar_init(smem_addr(&k_full), 1);
+        mbar_init(smem_addr(&k_empty), 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_addr(&k_full[i]), 1);
-            mbar_init(smem_addr(&k_empty[i]), 1);
+            mbar_init(smem_addr(&p_full[i]), 8);
+            mbar_init(smem_addr(&p_free[i]), 1);
             mbar_init(smem_addr(&v_full[i]), 1);
             mbar_init(smem_addr(&v_empty[i]), 1);
             mbar_init(smem_addr(&s_full[i]), 1);
-            mbar_init(smem_addr(&s_free[i]), 4);
+            mbar_init(smem_addr(&s_free[i]), 8);
         }
         failed_s = 0;
         fence_barrier_init();
@@ -107,7 +125,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
     }
-    if (warp == 5) {
+    if (warp == kTcMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(&tmem_base_s)),
                      "r"(kTcTmemCols)
@@ -123,7 +141,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         atomicExch(&failed_s, 1);
     };
 
-    if (warp == 4) {
+    if (warp == kTcLoadWarp) {
         // ---------------- loads ----------------
         const int32_t *bt = a.block_tables + static_cast<int64_t>(s) * a.max_blocks;
         const int rows_total = a.num_blocks * a.num_kv_heads * BS;
@@ -147,8 +165,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     set_device_error(a.err, PA_DEVERR_BAD_BLOCK);
             }
             if (lane == 0) {
-                if (!mbar_wait_bounded(smem_addr(&k_empty[st]), (use & 1) ^ 1, kTcWaitNs)) fail();
-                mbar_arrive_expect_tx(smem_addr(&k_full[st]), kTcTile);
+                if (!mbar_wait_bounded(smem_addr(&k_empty), (kb & 1) ^ 1, kTcWaitNs)) fail();
+                mbar_arrive_expect_tx(smem_addr(&k_full), kTcTile);
             }
             // lane pg holds page pg's row index
 #pragma unroll
@@ -156,8 +174,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int yy = __shfl_sync(0xffffffffu, y, pg);
                 if (lane == 0) {
                     for (int sl = 0; sl < 2; ++sl)
-                        tma_load_2d(base + kTcKOff + st * kTcTile + sl * kTcSlab + pg * BS * 128, &tmK,
-                                    sl * 64, yy, smem_addr(&k_full[st]), policy);
+                        tma_load_2d(base + kTcKOff + sl * kTcSlab + pg * BS * 128, &tmK,
+                                    sl * 64, yy, smem_addr(&k_full), policy);
                 }
             }
             if (lane == 0) {
@@ -174,7 +192,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kTcMmaWarp) {
         // ---------------- MMA issue ----------------
         if (lane == 0) {
             constexpr uint32_t idesc_qk = tc_idesc_bf16(kTcRows, kTcKeys, 0, 0);
@@ -184,11 +202,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, kTcWaitNs);
             auto issue_pv = [&](int j) {
                 const int st = j & 1, use = j >> 1;
-                ok = ok && mbar_wait_bounded(smem_addr(&p_full), j & 1, kTcWaitNs);
+                ok = ok && mbar_wait_bounded(smem_addr(&p_full[st]), use & 1, kTcWaitNs);
                 ok = ok && mbar_wait_bounded(smem_addr(&v_full[st]), use & 1, kTcWaitNs);
                 tc_fence_after();
                 if (ok) {
-                    const uint32_t pbase = base + kTcPOff;
+                    const uint32_t pbase = base + kTcPOff + st * kTcTile;
                     const uint32_t vbase = base + kTcVOff + st * kTcTile;
 #pragma unroll
                     for (int kk = 0; kk < kTcKeys / 16; ++kk) {
@@ -199,15 +217,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc_commit(smem_addr(&o_done));
                 tc_commit(smem_addr(&v_empty[st]));
+                tc_commit(smem_addr(&p_free[st]));
             };
             for (int kb = 0; kb < nkb; ++kb) {
                 const int st = kb & 1, use = kb >> 1;
-                ok = ok && mbar_wait_bounded(smem_addr(&k_full[st]), use & 1, kTcWaitNs);
+                ok = ok && mbar_wait_bounded(smem_addr(&k_full), kb & 1, kTcWaitNs);
                 ok = ok && mbar_wait_bounded(smem_addr(&s_free[st]), (use & 1) ^ 1, kTcWaitNs);
                 tc_fence_after();
                 if (ok) {
                     const uint32_t qbase = base + kTcQOff;
-                    const uint32_t kbase = base + kTcKOff + st * kTcTile;
+                    const uint32_t kbase = base + kTcKOff;
 #pragma unroll
                     for (int kk = 0; kk < 128 / 16; ++kk) {
                         const uint64_t ad = tc_smem_desc(qbase + (kk >> 2) * kTcSlab + (kk & 3) * 32, 16, 1024, 2);
@@ -216,7 +235,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
                 tc_commit(smem_addr(&s_full[st]));
-                tc_commit(smem_addr(&k_empty[st]));
+                tc_commit(smem_addr(&k_empty));
                 if (kb >= 1) issue_pv(kb - 1);
             }
             issue_pv(nkb - 1);
@@ -226,127 +245,154 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_wait_bounded(smem_addr(&drain), 0, kTcWaitNs);
         }
     } else {
-        // ---------------- softmax: thread = query row ----------------
-        const int row = warp * 32 + lane;
+        // -------- softmax: two threads per query row, 64 columns each --------
+        const int quarter = warp & 3, half = warp >> 2;
+        const int row = quarter * 32 + lane;
         const int t = row / a.group, g = row % a.group;
         const bool live = tok_begin + t < tok_end;
         const int pos = live ? first_pos + tok_begin + t : -1;
-        const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t tO = tmem + lane_addr + 256;
-        float m_run = -INFINITY, l_run = 0.f;
+        // blocks ending at or before every row's position need no mask
+        const int warp_min_pos = __reduce_min_sync(0xffffffffu, pos);
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t col0 = half * 64;  // this thread's columns of S, P and O
+        const uint32_t tO = tmem + lane_addr + 256 + col0;
+        const float scale = a.score_scale;
+        float m_ref = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
             const int st = kb & 1, use = kb >> 1;
+            const int key0 = kb * kTcKeys + col0;
+            const bool masked = kb * kTcKeys + kTcKeys - 1 > warp_min_pos;
             ok = ok && mbar_wait_bounded(smem_addr(&s_full[st]), use & 1, kTcWaitNs);
             tc_fence_after();
-            float sv[kTcKeys];
+            float v[64];
+            {
+                float lo[32], hi[32];
+                tc_ld32(tmem + lane_addr + st * 128 + col0, lo);
+                tc_ld32(tmem + lane_addr + st * 128 + col0 + 32, hi);
+                tc_wait_ld();
 #pragma unroll
-            for (int c4 = 0; c4 < kTcKeys / 32; ++c4) {
-                float tmp[32];
-                tc_ld32(tmem + lane_addr + st * 128 + c4 * 32, tmp);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) sv[c4 * 32 + i] = tmp[i];
-            }
-            tc_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&s_free[st]));
-            // mask + scale + running max / sum
-            const int key0 = kb * kTcKeys;
-            float mx = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < kTcKeys; ++i) {
-                float x = sv[i] * a.score_scale;
-                x = key0 + i <= pos ? x : -INFINITY;
-                sv[i] = x;
-                mx = fmaxf(mx, x);
-            }
-            const float m_new = fmaxf(m_run, mx);
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = fast_exp2(m_run - m_use);
-            m_run = m_new;
-            float sum = 0.f;
-#pragma unroll
-            for (int i = 0; i < kTcKeys; ++i) {
-                sv[i] = fast_exp2(sv[i] - m_use);
-                sum += sv[i];
-            }
-            l_run = l_run * alpha + sum;
-            if (kb >= 1) {
-                // block kb-1's PV is done: O is final for it and P may be rewritten
-                ok = ok && mbar_wait_bounded(smem_addr(&o_done), (kb - 1) & 1, kTcWaitNs);
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        float ov[32];
-                        tc_ld32(tO + c4 * 32, ov);
-                        tc_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-                        tc_st32(tO + c4 * 32, ov);
-                    }
-                    tc_wait_st();
+                for (int i = 0; i < 32; ++i) {
+                    v[i] = lo[i];
+                    v[32 + i] = hi[i];
                 }
             }
-            // P row -> shared memory, K-major with the 128-byte swizzle
-            uint8_t *prow = base_ptr + kTcPOff + row * 128;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&s_free[st]));  // S is in registers now
+            float mx = -INFINITY;
+            if (masked) {
 #pragma unroll
-            for (int ch = 0; ch < kTcKeys / 8; ++ch) {
-                uint4 v;
-                v.x = pack2<false>(sv[ch * 8 + 0], sv[ch * 8 + 1]);
-                v.y = pack2<false>(sv[ch * 8 + 2], sv[ch * 8 + 3]);
-                v.z = pack2<false>(sv[ch * 8 + 4], sv[ch * 8 + 5]);
-                v.w = pack2<false>(sv[ch * 8 + 6], sv[ch * 8 + 7]);
-                const int slab = ch >> 3, c16 = ch & 7;
-                *reinterpret_cast<uint4 *>(prow + slab * kTcSlab + ((c16 ^ (row & 7)) << 4)) = v;
+                for (int i = 0; i < 64; ++i) {
+                    v[i] = key0 + i <= pos ? v[i] : -INFINITY;
+                    mx = fmaxf(mx, v[i]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) mx = fmaxf(mx, v[i]);
             }
-            if (kend - key0 < kTcKeys) {
+            // combine the two halves of the row (scale > 0 keeps the order)
+            half_max[st][half][row] = mx;
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            mx = fmaxf(mx, half_max[st][half ^ 1][row]);
+            const float mxs = mx * scale;
+            // move the reference max only when the row max outgrew it
+            bool rescale = false;
+            float alpha = 1.f;
+            if (mxs > m_ref + kTcRescaleThreshold) {
+                alpha = fast_exp2(m_ref - mxs);  // 0 when m_ref = -inf
+                m_ref = mxs;
+                l_run *= alpha;
+                rescale = kb > 0;
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+                // O must hold block kb-1's PV before it is scaled
+                ok = ok && mbar_wait_bounded(smem_addr(&o_done), (kb - 1) & 1, kTcWaitNs);
+                tc_fence_after();
+                float o0[32], o1[32];
+                tc_ld32(tO, o0);
+                tc_ld32(tO + 32, o1);
+                tc_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    o0[i] *= alpha;
+                    o1[i] *= alpha;
+                }
+                tc_st32(tO, o0);
+                tc_st32(tO + 32, o1);
+                tc_wait_st();
+            }
+            // P = exp2(scale * s - m_ref) (bf16) into this block's P buffer
+            const float neg = m_ref == -INFINITY ? 0.f : -m_ref;
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                v[i] = fast_exp2(fmaf(v[i], scale, neg));  // masked: exp2(-inf) = 0
+                sum += v[i];
+            }
+            l_run += sum;
+            ok = ok && mbar_wait_bounded(smem_addr(&p_free[st]), (use & 1) ^ 1, kTcWaitNs);
+            uint8_t *prow = base_ptr + kTcPOff + st * kTcTile + half * kTcSlab + row * 128;
+#pragma unroll
+            for (int c16 = 0; c16 < 8; ++c16) {
+                uint4 w;
+                w.x = pack2<false>(v[c16 * 8 + 0], v[c16 * 8 + 1]);
+                w.y = pack2<false>(v[c16 * 8 + 2], v[c16 * 8 + 3]);
+                w.z = pack2<false>(v[c16 * 8 + 4], v[c16 * 8 + 5]);
+                w.w = pack2<false>(v[c16 * 8 + 6], v[c16 * 8 + 7]);
+                *reinterpret_cast<uint4 *>(prow + ((c16 ^ (row & 7)) << 4)) = w;
+            }
+            if (kend - kb * kTcKeys < kTcKeys) {
                 // keys past the context in the last block may hold anything:
                 // zero those V rows (0 x garbage could be NaN)
                 ok = ok && mbar_wait_bounded(smem_addr(&v_full[st]), use & 1, kTcWaitNs);
-                const int valid = kend - key0;
+                const int valid = kend - kb * kTcKeys;
                 uint8_t *vbase = base_ptr + kTcVOff + st * kTcTile;
-                for (int r2 = valid + (tid & 127); r2 < kTcKeys; r2 += 128)
+                for (int r2 = valid + tid; r2 < kTcKeys; r2 += kTcSoftmaxThreads)
                     for (int sl = 0; sl < 2; ++sl)
                         for (int c16 = 0; c16 < 8; ++c16)
                             *reinterpret_cast<uint4 *>(vbase + sl * kTcSlab + r2 * 128 + c16 * 16) =
                                 make_uint4(0u, 0u, 0u, 0u);
-                // every softmax warp zeroes before any arrives on p_full
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                asm volatile("bar.sync 1, 256;" ::: "memory");  // every softmax warp zeroed
             }
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&p_full));
+            if (lane == 0) mbar_arrive(smem_addr(&p_full[st]));
         }
         ok = ok && mbar_wait_bounded(smem_addr(&o_done), (nkb - 1) & 1, kTcWaitNs);
         tc_fence_after();
         if (!ok) fail();
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        half_max[nkb & 1][half][row] = l_run;
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        const float l = half_max[nkb & 1][0][row] + half_max[nkb & 1][1][row];
+        const float inv = l > 0.f ? 1.f / l : 0.f;
         __nv_bfloat16 *dst = a.out + ((static_cast<int64_t>(q0) + tok_begin + t) * a.num_q_heads +
-                                      h * a.group + g) * 128;
+                                      h * a.group + g) * 128 + col0;
+        float o0[32], o1[32];
+        tc_ld32(tO, o0);
+        tc_ld32(tO + 32, o1);
+        tc_wait_ld();
+        if (live && !failed_s) {
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-            float ov[32];
-            tc_ld32(tO + c4 * 32, ov);
-            tc_wait_ld();
-            if (live && !failed_s) {
-#pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                    uint4 v;
-                    v.x = pack2<false>(ov[i] * inv, ov[i + 1] * inv);
-                    v.y = pack2<false>(ov[i + 2] * inv, ov[i + 3] * inv);
-                    v.z = pack2<false>(ov[i + 4] * inv, ov[i + 5] * inv);
-                    v.w = pack2<false>(ov[i + 6] * inv, ov[i + 7] * inv);
-                    *reinterpret_cast<uint4 *>(dst + c4 * 32 + i) = v;
-                }
+            for (int i = 0; i < 32; i += 8) {
+                uint4 w0, w1;
+                w0.x = pack2<false>(o0[i] * inv, o0[i + 1] * inv);
+                w0.y = pack2<false>(o0[i + 2] * inv, o0[i + 3] * inv);
+                w0.z = pack2<false>(o0[i + 4] * inv, o0[i + 5] * inv);
+                w0.w = pack2<false>(o0[i + 6] * inv, o0[i + 7] * inv);
+                w1.x = pack2<false>(o1[i] * inv, o1[i + 1] * inv);
+                w1.y = pack2<false>(o1[i + 2] * inv, o1[i + 3] * inv);
+                w1.z = pack2<false>(o1[i + 4] * inv, o1[i + 5] * inv);
+                w1.w = pack2<false>(o1[i + 6] * inv, o1[i + 7] * inv);
+                *reinterpret_cast<uint4 *>(dst + i) = w0;
+                *reinterpret_cast<uint4 *>(dst + 32 + i) = w1;
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kTcMmaWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols)
                      : "memory");
