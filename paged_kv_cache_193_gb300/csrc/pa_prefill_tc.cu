@@ -49,23 +49,31 @@ struct PrefillTcArgs {
 
 constexpr int kTcRows = 128;          // query rows per tile (TMEM lanes)
 constexpr int kTcKeys = 128;          // keys per block
-constexpr int kTcThreads = 320;       // warps 0-7 softmax (2 per row), 8 loads, 9 MMA
+constexpr int kTcThreads = 352;       // warps 0-7 softmax (2 per row), 8 Q/K loads, 9 MMA, 10 V loads
 constexpr int kTcSoftmaxThreads = 256;
 constexpr int kTcLoadWarp = 8;
 constexpr int kTcMmaWarp = 9;
+constexpr int kTcVLoadWarp = 10;
 constexpr int kTcSlab = 16384;        // one 64-dim slab of 128 rows x 128 B
 constexpr int kTcTile = 2 * kTcSlab;  // 128 rows x 128 dims bf16
 constexpr int kTcQOff = 0;
-constexpr int kTcKOff = kTcTile;            // 1 stage: QK retires long before the next K is due
-constexpr int kTcVOff = kTcTile * 2;        // 2 stages
-constexpr int kTcPOff = kTcTile * 4;        // 2 buffers
-constexpr int kTcSmem = kTcTile * 6 + 1024;
+constexpr int kTcStages = 3;  // K and V rings: a page's TMA latency is about two blocks
+constexpr int kTcKOff = kTcTile;
+constexpr int kTcVOff = kTcTile * (1 + kTcStages);
+constexpr int kTcSmem = kTcTile * (1 + 2 * kTcStages) + 1024;
 // P is written against a reference max that only moves when the row max
 // grows past it by more than this (base-2 units): P <= 2^8, and O is
 // rescaled in tensor memory only then.
 constexpr float kTcRescaleThreshold = 8.f;
-constexpr int kTcTmemCols = 512;            // S0 [0,128) S1 [128,256) O [256,384)
+constexpr int kTcTmemCols = 512;  // S0 [0,128) S1 [128,256) O [256,384) P0 [384,448) P1 [448,512)
+constexpr int kTcOCol = 256;
+constexpr int kTcPCol = 384;      // P as bf16 pairs: 64 columns per 128 keys
 constexpr uint64_t kTcWaitNs = 2000000000ull;
+
+// Named barrier 1 over the softmax warps only.
+__device__ __forceinline__ void softmax_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kTcSoftmaxThreads) : "memory");
+}
 
 template <int BS>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -74,19 +82,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int NPG = kTcKeys / BS;  // pages per key block
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t q_full, o_done, drain;
-    __shared__ __align__(8) uint64_t k_full, k_empty, v_full[2], v_empty[2], s_full[2], s_free[2];
+    __shared__ __align__(8) uint64_t k_full[kTcStages], k_empty[kTcStages], v_full[kTcStages],
+        v_empty[kTcStages], s_full[2], s_free[2];
     __shared__ __align__(8) uint64_t p_full[2], p_free[2];
     __shared__ uint32_t tmem_base_s;
     __shared__ int failed_s;
-    // per-row partial maxima of the two column halves, double-buffered by
-    // block parity so a fast half cannot overwrite a value its partner has
-    // not read yet
-    // (after the last block, the buffer it did not use carries the row sums)
-    __shared__ float half_max[2][2][kTcRows];
+    // per-row partial maxima of the two column halves (after the last block:
+    // the partial row sums)
+    __shared__ float half_max[2][kTcRows];
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *base_ptr = smem_raw + (base - raw);
 
     const int tile = gridDim.x - 1 - blockIdx.x;
     const int h = blockIdx.y, s = blockIdx.z;
@@ -109,13 +115,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(smem_addr(&q_full), 1);
         mbar_init(smem_addr(&o_done), 1);
         mbar_init(smem_addr(&drain), 1);
-        mbar_init(smem_addr(&k_full), 1);
-        mbar_init(smem_addr(&k_empty), 1);
+        for (int i = 0; i < kTcStages; ++i) {
+            mbar_init(smem_addr(&k_full[i]), 1);
+            mbar_init(smem_addr(&k_empty[i]), 1);
+            mbar_init(smem_addr(&v_full[i]), 1);
+            mbar_init(smem_addr(&v_empty[i]), 1);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_addr(&p_full[i]), 8);
             mbar_init(smem_addr(&p_free[i]), 1);
-            mbar_init(smem_addr(&v_full[i]), 1);
-            mbar_init(smem_addr(&v_empty[i]), 1);
             mbar_init(smem_addr(&s_full[i]), 1);
             mbar_init(smem_addr(&s_free[i]), 8);
         }
@@ -141,10 +149,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         atomicExch(&failed_s, 1);
     };
 
+    // Loader lanes pg < NPG own page pg of a key block: its first row in the
+    // cache (pages past the keys: a row past the end, read as zeros).  The
+    // block table entry is fetched one block ahead.
+    const int32_t *bt = a.block_tables + static_cast<int64_t>(s) * a.max_blocks;
+    const int rows_total = a.num_blocks * a.num_kv_heads * BS;
+    auto page_row = [&](int kb) {
+        const int pg_idx = kb * NPG + lane;
+        int y = rows_total;
+        if (lane < NPG && pg_idx * BS < kend) {
+            const int blk = __ldg(bt + pg_idx);
+            if (blk >= 0 && blk < a.num_blocks)
+                y = (blk * a.num_kv_heads + h) * BS;
+            else
+                set_device_error(a.err, PA_DEVERR_BAD_BLOCK);
+        }
+        return y;
+    };
+
     if (warp == kTcLoadWarp) {
-        // ---------------- loads ----------------
-        const int32_t *bt = a.block_tables + static_cast<int64_t>(s) * a.max_blocks;
-        const int rows_total = a.num_blocks * a.num_kv_heads * BS;
+        // ---------------- Q and K loads ----------------
         const uint64_t policy = l2_evict_first_policy();
         if (lane == 0) {
             const uint32_t bar = smem_addr(&q_full);
@@ -152,44 +176,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int sl = 0; sl < 2; ++sl)
                 tma_load_3d(base + kTcQOff + sl * kTcSlab, &tmQ, sl * 64, h * a.group, q0 + tok_begin, bar);
         }
+        int y_next = page_row(0);
         for (int kb = 0; kb < nkb; ++kb) {
-            const int st = kb & 1, use = kb >> 1;
-            // physical rows of this block's pages (pages past the keys: zero fill)
-            const int pg_idx = kb * NPG + lane;
-            int y = rows_total;
-            if (lane < NPG && pg_idx * BS < kend) {
-                const int blk = __ldg(bt + pg_idx);
-                if (blk >= 0 && blk < a.num_blocks)
-                    y = (blk * a.num_kv_heads + h) * BS;
-                else
-                    set_device_error(a.err, PA_DEVERR_BAD_BLOCK);
-            }
+            const int st = kb % kTcStages, ph = (kb / kTcStages) & 1;
+            const int y = y_next;
+            if (kb + 1 < nkb) y_next = page_row(kb + 1);
             if (lane == 0) {
-                if (!mbar_wait_bounded(smem_addr(&k_empty), (kb & 1) ^ 1, kTcWaitNs)) fail();
-                mbar_arrive_expect_tx(smem_addr(&k_full), kTcTile);
+                if (!mbar_wait_bounded(smem_addr(&k_empty[st]), ph ^ 1, kTcWaitNs)) fail();
+                mbar_arrive_expect_tx(smem_addr(&k_full[st]), kTcTile);
             }
-            // lane pg holds page pg's row index
-#pragma unroll
-            for (int pg = 0; pg < NPG; ++pg) {
-                const int yy = __shfl_sync(0xffffffffu, y, pg);
-                if (lane == 0) {
-                    for (int sl = 0; sl < 2; ++sl)
-                        tma_load_2d(base + kTcKOff + sl * kTcSlab + pg * BS * 128, &tmK,
-                                    sl * 64, yy, smem_addr(&k_full), policy);
-                }
+            __syncwarp();
+            if (lane < NPG) {
+                for (int sl = 0; sl < 2; ++sl)
+                    tma_load_2d(base + kTcKOff + st * kTcTile + sl * kTcSlab + lane * BS * 128, &tmK,
+                                sl * 64, y, smem_addr(&k_full[st]), policy);
             }
+        }
+    } else if (warp == kTcVLoadWarp) {
+        // ---------------- V loads: the same pages, from a second warp ----------------
+        const uint64_t policy = l2_evict_first_policy();
+        int y_next = page_row(0);
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int st = kb % kTcStages, ph = (kb / kTcStages) & 1;
+            const int y = y_next;
+            if (kb + 1 < nkb) y_next = page_row(kb + 1);
             if (lane == 0) {
-                if (!mbar_wait_bounded(smem_addr(&v_empty[st]), (use & 1) ^ 1, kTcWaitNs)) fail();
+                if (!mbar_wait_bounded(smem_addr(&v_empty[st]), ph ^ 1, kTcWaitNs)) fail();
                 mbar_arrive_expect_tx(smem_addr(&v_full[st]), kTcTile);
             }
-#pragma unroll
-            for (int pg = 0; pg < NPG; ++pg) {
-                const int yy = __shfl_sync(0xffffffffu, y, pg);
-                if (lane == 0) {
-                    for (int sl = 0; sl < 2; ++sl)
-                        tma_load_2d(base + kTcVOff + st * kTcTile + sl * kTcSlab + pg * BS * 128, &tmV,
-                                    sl * 64, yy, smem_addr(&v_full[st]), policy);
-                }
+            __syncwarp();
+            if (lane < NPG) {
+                for (int sl = 0; sl < 2; ++sl)
+                    tma_load_2d(base + kTcVOff + st * kTcTile + sl * kTcSlab + lane * BS * 128, &tmV,
+                                sl * 64, y, smem_addr(&v_full[st]), policy);
             }
         }
     } else if (warp == kTcMmaWarp) {
@@ -198,35 +217,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             constexpr uint32_t idesc_qk = tc_idesc_bf16(kTcRows, kTcKeys, 0, 0);
             constexpr uint32_t idesc_pv = tc_idesc_bf16(kTcRows, 128, 0, 1);
             const uint32_t tS[2] = {tmem, tmem + 128};
-            const uint32_t tO = tmem + 256;
+            const uint32_t tO = tmem + kTcOCol;
             bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, kTcWaitNs);
             auto issue_pv = [&](int j) {
-                const int st = j & 1, use = j >> 1;
-                ok = ok && mbar_wait_bounded(smem_addr(&p_full[st]), use & 1, kTcWaitNs);
-                ok = ok && mbar_wait_bounded(smem_addr(&v_full[st]), use & 1, kTcWaitNs);
+                const int pb = j & 1, vs = j % kTcStages;
+                ok = ok && mbar_wait_bounded(smem_addr(&p_full[pb]), (j >> 1) & 1, kTcWaitNs);
+                ok = ok && mbar_wait_bounded(smem_addr(&v_full[vs]), (j / kTcStages) & 1, kTcWaitNs);
                 tc_fence_after();
                 if (ok) {
-                    const uint32_t pbase = base + kTcPOff + st * kTcTile;
-                    const uint32_t vbase = base + kTcVOff + st * kTcTile;
+                    const uint32_t tP = tmem + kTcPCol + pb * 64;
+                    const uint32_t vbase = base + kTcVOff + vs * kTcTile;
 #pragma unroll
                     for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-                        const uint64_t ad = tc_smem_desc(pbase + (kk >> 2) * kTcSlab + (kk & 3) * 32, 16, 1024, 2);
                         const uint64_t bd = tc_smem_desc(vbase + kk * 16 * 128, kTcSlab, 1024, 2);
-                        tc_mma_bf16(tO, ad, bd, idesc_pv, j > 0 || kk > 0);
+                        tc_mma_bf16_ts(tO, tP + kk * 8, bd, idesc_pv, j > 0 || kk > 0);
                     }
                 }
                 tc_commit(smem_addr(&o_done));
-                tc_commit(smem_addr(&v_empty[st]));
-                tc_commit(smem_addr(&p_free[st]));
+                tc_commit(smem_addr(&v_empty[vs]));
+                tc_commit(smem_addr(&p_free[pb]));
             };
             for (int kb = 0; kb < nkb; ++kb) {
-                const int st = kb & 1, use = kb >> 1;
-                ok = ok && mbar_wait_bounded(smem_addr(&k_full), kb & 1, kTcWaitNs);
-                ok = ok && mbar_wait_bounded(smem_addr(&s_free[st]), (use & 1) ^ 1, kTcWaitNs);
+                const int st = kb & 1, ks = kb % kTcStages;
+                ok = ok && mbar_wait_bounded(smem_addr(&k_full[ks]), (kb / kTcStages) & 1, kTcWaitNs);
+                ok = ok && mbar_wait_bounded(smem_addr(&s_free[st]), ((kb >> 1) & 1) ^ 1, kTcWaitNs);
                 tc_fence_after();
                 if (ok) {
                     const uint32_t qbase = base + kTcQOff;
-                    const uint32_t kbase = base + kTcKOff;
+                    const uint32_t kbase = base + kTcKOff + ks * kTcTile;
 #pragma unroll
                     for (int kk = 0; kk < 128 / 16; ++kk) {
                         const uint64_t ad = tc_smem_desc(qbase + (kk >> 2) * kTcSlab + (kk & 3) * 32, 16, 1024, 2);
@@ -235,7 +253,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
                 tc_commit(smem_addr(&s_full[st]));
-                tc_commit(smem_addr(&k_empty));
+                tc_commit(smem_addr(&k_empty[ks]));
                 if (kb >= 1) issue_pv(kb - 1);
             }
             issue_pv(nkb - 1);
@@ -255,7 +273,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int warp_min_pos = __reduce_min_sync(0xffffffffu, pos);
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t col0 = half * 64;  // this thread's columns of S, P and O
-        const uint32_t tO = tmem + lane_addr + 256 + col0;
+        const uint32_t tO = tmem + lane_addr + kTcOCol + col0;
         const float scale = a.score_scale;
         float m_ref = -INFINITY, l_run = 0.f;
         bool ok = true;
@@ -292,9 +310,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int i = 0; i < 64; ++i) mx = fmaxf(mx, v[i]);
             }
             // combine the two halves of the row (scale > 0 keeps the order)
-            half_max[st][half][row] = mx;
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            mx = fmaxf(mx, half_max[st][half ^ 1][row]);
+            half_max[half][row] = mx;
+            softmax_bar();
+            mx = fmaxf(mx, half_max[half ^ 1][row]);
             const float mxs = mx * scale;
             // move the reference max only when the row max outgrew it
             bool rescale = false;
@@ -331,41 +349,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 sum += v[i];
             }
             l_run += sum;
-            ok = ok && mbar_wait_bounded(smem_addr(&p_free[st]), (use & 1) ^ 1, kTcWaitNs);
-            uint8_t *prow = base_ptr + kTcPOff + st * kTcTile + half * kTcSlab + row * 128;
+            // both halves have read their partner's maximum: its slot is free
+            softmax_bar();
+            // P (bf16 pairs) into this block's P columns once PV(kb - 2) has read them
+            uint32_t pk[32];
 #pragma unroll
-            for (int c16 = 0; c16 < 8; ++c16) {
-                uint4 w;
-                w.x = pack2<false>(v[c16 * 8 + 0], v[c16 * 8 + 1]);
-                w.y = pack2<false>(v[c16 * 8 + 2], v[c16 * 8 + 3]);
-                w.z = pack2<false>(v[c16 * 8 + 4], v[c16 * 8 + 5]);
-                w.w = pack2<false>(v[c16 * 8 + 6], v[c16 * 8 + 7]);
-                *reinterpret_cast<uint4 *>(prow + ((c16 ^ (row & 7)) << 4)) = w;
-            }
+            for (int i = 0; i < 32; ++i) pk[i] = pack2<false>(v[2 * i], v[2 * i + 1]);
+            ok = ok && mbar_wait_bounded(smem_addr(&p_free[st]), (use & 1) ^ 1, kTcWaitNs);
+            tc_fence_after();
+            tc_st32(tmem + lane_addr + kTcPCol + st * 64 + half * 32, pk);
+            tc_wait_st();
             if (kend - kb * kTcKeys < kTcKeys) {
                 // keys past the context in the last block may hold anything:
-                // zero those V rows (0 x garbage could be NaN)
-                ok = ok && mbar_wait_bounded(smem_addr(&v_full[st]), use & 1, kTcWaitNs);
+                // zero those V rows (P is 0 there, but 0 x garbage could be NaN)
+                const int vs = kb % kTcStages;
+                ok = ok && mbar_wait_bounded(smem_addr(&v_full[vs]), (kb / kTcStages) & 1, kTcWaitNs);
                 const int valid = kend - kb * kTcKeys;
-                uint8_t *vbase = base_ptr + kTcVOff + st * kTcTile;
+                const uint32_t vbase = base + kTcVOff + vs * kTcTile;
                 for (int r2 = valid + tid; r2 < kTcKeys; r2 += kTcSoftmaxThreads)
                     for (int sl = 0; sl < 2; ++sl)
                         for (int c16 = 0; c16 < 8; ++c16)
-                            *reinterpret_cast<uint4 *>(vbase + sl * kTcSlab + r2 * 128 + c16 * 16) =
-                                make_uint4(0u, 0u, 0u, 0u);
-                asm volatile("bar.sync 1, 256;" ::: "memory");  // every softmax warp zeroed
+                            st_shared_zero16(vbase + sl * kTcSlab + r2 * 128 + c16 * 16);
+                fence_proxy_async_smem();
+                softmax_bar();  // every softmax warp zeroed its rows
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&p_full[st]));
         }
-        ok = ok && mbar_wait_bounded(smem_addr(&o_done), (nkb - 1) & 1, kTcWaitNs);
+        // every PV is done once the MMA warp's final commit lands (o_done can
+        // be two phases behind here, too far for a parity wait)
+        ok = ok && mbar_wait_bounded(smem_addr(&drain), 0, kTcWaitNs);
         tc_fence_after();
         if (!ok) fail();
-        half_max[nkb & 1][half][row] = l_run;
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        const float l = half_max[nkb & 1][0][row] + half_max[nkb & 1][1][row];
+        half_max[half][row] = l_run;
+        softmax_bar();
+        const float l = half_max[0][row] + half_max[1][row];
         const float inv = l > 0.f ? 1.f / l : 0.f;
         __nv_bfloat16 *dst = a.out + ((static_cast<int64_t>(q0) + tok_begin + t) * a.num_q_heads +
                                       h * a.group + g) * 128 + col0;
