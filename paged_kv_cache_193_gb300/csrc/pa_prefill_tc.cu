@@ -24,6 +24,7 @@
 //    While they work on block j the tensor cores finish block j - 1's PV
 //    and compute S for block j + 1.
 #include <cudaTypedefs.h>
+#include <limits.h>
 #include <math.h>
 
 #include <atomic>
@@ -149,22 +150,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         atomicExch(&failed_s, 1);
     };
 
-    // Loader lanes pg < NPG own page pg of a key block: its first row in the
-    // cache (pages past the keys: a row past the end, read as zeros).  The
-    // block table entry is fetched one block ahead.
+    // Loader lanes pg < NPG own page pg of a key block.  The block table
+    // entry is fetched one block ahead and only checked when it is used, so
+    // the fetch overlaps the current block's copies.
     const int32_t *bt = a.block_tables + static_cast<int64_t>(s) * a.max_blocks;
     const int rows_total = a.num_blocks * a.num_kv_heads * BS;
-    auto page_row = [&](int kb) {
+    constexpr int kPastKeys = INT_MIN;
+    auto page_entry = [&](int kb) {
         const int pg_idx = kb * NPG + lane;
-        int y = rows_total;
-        if (lane < NPG && pg_idx * BS < kend) {
-            const int blk = __ldg(bt + pg_idx);
-            if (blk >= 0 && blk < a.num_blocks)
-                y = (blk * a.num_kv_heads + h) * BS;
-            else
-                set_device_error(a.err, PA_DEVERR_BAD_BLOCK);
+        return (lane < NPG && pg_idx * BS < kend) ? __ldg(bt + pg_idx) : kPastKeys;
+    };
+    // the page's first row in the cache; pages past the keys (and bad
+    // entries, which are reported) read a row past the end: zeros
+    auto page_row = [&](int blk) {
+        if (blk == kPastKeys) return rows_total;
+        if (blk < 0 || blk >= a.num_blocks) {
+            set_device_error(a.err, PA_DEVERR_BAD_BLOCK);
+            return rows_total;
         }
-        return y;
+        return (blk * a.num_kv_heads + h) * BS;
     };
 
     if (warp == kTcLoadWarp) {
@@ -176,11 +180,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int sl = 0; sl < 2; ++sl)
                 tma_load_3d(base + kTcQOff + sl * kTcSlab, &tmQ, sl * 64, h * a.group, q0 + tok_begin, bar);
         }
-        int y_next = page_row(0);
+        int e_next = page_entry(0);
         for (int kb = 0; kb < nkb; ++kb) {
             const int st = kb % kTcStages, ph = (kb / kTcStages) & 1;
-            const int y = y_next;
-            if (kb + 1 < nkb) y_next = page_row(kb + 1);
+            const int y = page_row(e_next);
+            if (kb + 1 < nkb) e_next = page_entry(kb + 1);
             if (lane == 0) {
                 if (!mbar_wait_bounded(smem_addr(&k_empty[st]), ph ^ 1, kTcWaitNs)) fail();
                 mbar_arrive_expect_tx(smem_addr(&k_full[st]), kTcTile);
@@ -195,11 +199,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp == kTcVLoadWarp) {
         // ---------------- V loads: the same pages, from a second warp ----------------
         const uint64_t policy = l2_evict_first_policy();
-        int y_next = page_row(0);
+        int e_next = page_entry(0);
         for (int kb = 0; kb < nkb; ++kb) {
             const int st = kb % kTcStages, ph = (kb / kTcStages) & 1;
-            const int y = y_next;
-            if (kb + 1 < nkb) y_next = page_row(kb + 1);
+            const int y = page_row(e_next);
+            if (kb + 1 < nkb) e_next = page_entry(kb + 1);
             if (lane == 0) {
                 if (!mbar_wait_bounded(smem_addr(&v_empty[st]), ph ^ 1, kTcWaitNs)) fail();
                 mbar_arrive_expect_tx(smem_addr(&v_full[st]), kTcTile);
