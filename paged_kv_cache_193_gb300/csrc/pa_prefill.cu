@@ -21,7 +21,7 @@
 
 #include <atomic>
 
-#include "pa_device.cuh"
+#include "pa_prefill.cuh"
 
 namespace pa {
 

@@ -4,32 +4,33 @@
 // its sequence's cached prefix and earlier chunk tokens, through the block
 // table), organised for sm_103a's asynchronous tensor cores:
 //  * One CTA per (query tile of 128 rows = (chunk token, query head of the KV
-//    head's group) pairs, KV head, sequence), one CTA per SM (224 KB of
-//    shared memory, 384 of the 512 TMEM columns).
-//  * Warp 8 (one lane) streams the tile's queries (one 3-D TMA box per
-//    64-dim slab) and, per block of 128 keys, the K and V pages of the KV
-//    head (2-D TMA boxes, hardware 128-byte swizzle) into two K and two V
-//    stages.
+//    head's group) pairs, KV head, sequence), one CTA per SM (225 KB of
+//    shared memory: the query tile and three K and three V stages; all 512
+//    TMEM columns: two S accumulators, O, and two P buffers).
+//  * Warp 8 streams the tile's queries (one 3-D TMA box per 64-dim slab) and
+//    the K pages of each block of 128 keys; warp 10 streams the V pages.
+//    Lane p issues page p's boxes (2-D TMA, hardware 128-byte swizzle), with
+//    the block table read one block ahead.
 //  * Warp 9 owns the tensor memory and one lane issues the MMAs:
-//    S = Q K^T (M 128 x N 128 x K 128, both operands K-major) into one of two
-//    S accumulators, and O += P V (P K-major from shared memory, V read
-//    MN-major straight from the page layout) into the O accumulator; each
-//    group is committed to an mbarrier.
+//    S = Q K^T (M 128 x N 128 x K 128, both operands K-major in shared
+//    memory) into one of two S accumulators, and O += P V (P read from
+//    tensor memory, V read MN-major straight from the page layout) into the
+//    O accumulator; each group is committed to an mbarrier.
 //  * Warps 0-7 do the softmax: a query row is TMEM lane (warp % 4) * 32 +
 //    lane, and warps w and w + 4 take its two 64-column halves (their
 //    partial maxima meet in shared memory once per block).  They read S,
 //    apply the causal mask, keep the row's sum against a reference max that
 //    only moves when the row max outgrows it by 2^8 (so O is rescaled in
-//    tensor memory rarely), and write P (bf16) to one of two P buffers.
-//    While they work on block j the tensor cores finish block j - 1's PV
-//    and compute S for block j + 1.
+//    tensor memory rarely), and store P as bf16 pairs into one of two P
+//    buffers in tensor memory.  While they work on block j the tensor cores
+//    finish block j - 1's PV and compute S for block j + 1.
 #include <cudaTypedefs.h>
 #include <limits.h>
 #include <math.h>
 
 #include <atomic>
 
-#include "pa_device.cuh"
+#include "pa_prefill.cuh"
 
 namespace pa {
 
