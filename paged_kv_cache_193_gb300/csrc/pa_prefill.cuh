@@ -148,4 +148,34 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Two fp32 fused multiply-adds (each rounded once, as fmaf) in one instruction.
+__device__ __forceinline__ void ffma2(float &x0, float &x1, float b, float c) {
+    asm("{\n\t.reg .b64 x, y, z;\n\t"
+        "mov.b64 x, {%0, %1};\n\t"
+        "mov.b64 y, {%2, %2};\n\t"
+        "mov.b64 z, {%3, %3};\n\t"
+        "fma.rn.f32x2 x, x, y, z;\n\t"
+        "mov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(x0), "+f"(x1)
+        : "f"(b), "f"(c));
+}
+
+// (s0, s1) += (a0, a1) in one instruction.
+__device__ __forceinline__ void fadd2(float &s0, float &s1, float a0, float a1) {
+    asm("{\n\t.reg .b64 x, y;\n\t"
+        "mov.b64 x, {%0, %1};\n\t"
+        "mov.b64 y, {%2, %3};\n\t"
+        "add.rn.f32x2 x, x, y;\n\t"
+        "mov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "f"(a0), "f"(a1));
+}
+
 }  // namespace pa

@@ -51,25 +51,33 @@ struct PrefillTcArgs {
 
 constexpr int kTcRows = 128;          // query rows per tile (TMEM lanes)
 constexpr int kTcKeys = 128;          // keys per block
-constexpr int kTcThreads = 352;       // warps 0-7 softmax (2 per row), 8 Q/K loads, 9 MMA, 10 V loads
+constexpr int kTcTiles = 2;           // query tiles per CTA; both read every K/V stage
+// warps 0-7 softmax (2 per row), 8 Q/K loads, 9 and 11 the MMAs of tiles 0
+// and 1 (two issuing threads, on sub-partitions apart from each other and
+// from the loaders, so neither tile's chain waits behind the other's), 10 V loads
+constexpr int kTcThreads = 384;
 constexpr int kTcSoftmaxThreads = 256;
 constexpr int kTcLoadWarp = 8;
 constexpr int kTcMmaWarp = 9;
 constexpr int kTcVLoadWarp = 10;
+constexpr int kTcMmaWarpB = 11;
 constexpr int kTcSlab = 16384;        // one 64-dim slab of 128 rows x 128 B
 constexpr int kTcTile = 2 * kTcSlab;  // 128 rows x 128 dims bf16
-constexpr int kTcQOff = 0;
-constexpr int kTcStages = 3;  // K and V rings: a page's TMA latency is about two blocks
-constexpr int kTcKOff = kTcTile;
-constexpr int kTcVOff = kTcTile * (1 + kTcStages);
-constexpr int kTcSmem = kTcTile * (1 + 2 * kTcStages) + 1024;
+constexpr int kTcKStages = 3;
+constexpr int kTcVStages = 2;
+constexpr int kTcQOff = 0;                                   // one query tile after the other
+constexpr int kTcKOff = kTcTiles * kTcTile;
+constexpr int kTcVOff = kTcKOff + kTcKStages * kTcTile;
+constexpr int kTcSmem = kTcVOff + kTcVStages * kTcTile + 1024;
 // P is written against a reference max that only moves when the row max
 // grows past it by more than this (base-2 units): P <= 2^8, and O is
 // rescaled in tensor memory only then.
 constexpr float kTcRescaleThreshold = 8.f;
-constexpr int kTcTmemCols = 512;  // S0 [0,128) S1 [128,256) O [256,384) P0 [384,448) P1 [448,512)
+// Tensor memory: S of tile T at columns [128 T, 128 T + 128), O of tile T at
+// [256 + 128 T, ...); P of tile T (bf16 pairs, 64 columns) over the first
+// half of its S once the softmax has read S.
+constexpr int kTcTmemCols = 512;
 constexpr int kTcOCol = 256;
-constexpr int kTcPCol = 384;      // P as bf16 pairs: 64 columns per 128 keys
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 
 // Named barrier 1 over the softmax warps only.
@@ -83,51 +91,62 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       const __grid_constant__ CUtensorMap tmV, const PrefillTcArgs a) {
     constexpr int NPG = kTcKeys / BS;  // pages per key block
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t q_full, o_done, drain;
-    __shared__ __align__(8) uint64_t k_full[kTcStages], k_empty[kTcStages], v_full[kTcStages],
-        v_empty[kTcStages], s_full[2], s_free[2];
-    __shared__ __align__(8) uint64_t p_full[2], p_free[2];
+    __shared__ __align__(8) uint64_t q_full, drain[kTcTiles];
+    __shared__ __align__(8) uint64_t k_full[kTcKStages], k_empty[kTcKStages], v_full[kTcVStages],
+        v_empty[kTcVStages];
+    __shared__ __align__(8) uint64_t s_full[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles];
     __shared__ uint32_t tmem_base_s;
     __shared__ int failed_s;
-    // per-row partial maxima of the two column halves (after the last block:
-    // the partial row sums)
+    // per-row partial maxima of the two column halves (at the end: the
+    // partial row sums)
     __shared__ float half_max[2][kTcRows];
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
 
-    const int tile = gridDim.x - 1 - blockIdx.x;
+    const int pair = gridDim.x - 1 - blockIdx.x;  // tiles 2 pair and 2 pair + 1
     const int h = blockIdx.y, s = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int q0 = a.query_start[s];
     const int chunk = a.query_start[s + 1] - q0;
     const int ctx = a.context_lens[s];
-    const int tok_begin = tile * a.tile_tokens;
-    if (tok_begin >= chunk) return;  // uniform: before any barrier or TMEM use
+    int tok_begin[kTcTiles], kend[kTcTiles], nkb[kTcTiles];
+#pragma unroll
+    for (int T = 0; T < kTcTiles; ++T) tok_begin[T] = (kTcTiles * pair + T) * a.tile_tokens;
+    // uniform exits, before any barrier or TMEM use
     if (ctx > a.max_blocks * BS || ctx < chunk) {
-        if (tid == 0) set_device_error(a.err, PA_DEVERR_BAD_CONTEXT);
+        if (tid == 0 && tok_begin[0] < chunk) set_device_error(a.err, PA_DEVERR_BAD_CONTEXT);
         return;
     }
-    const int tok_end = min(tok_begin + a.tile_tokens, chunk);
+    if (tok_begin[0] >= chunk) return;
+    const int ntiles = tok_begin[1] < chunk ? 2 : 1;
     const int first_pos = ctx - chunk;
-    const int kend = first_pos + tok_end;               // keys [0, kend)
-    const int nkb = (kend + kTcKeys - 1) / kTcKeys;     // key blocks
+#pragma unroll
+    for (int T = 0; T < kTcTiles; ++T) {
+        kend[T] = first_pos + min(tok_begin[T] + a.tile_tokens, chunk);  // keys [0, kend)
+        nkb[T] = (kend[T] + kTcKeys - 1) / kTcKeys;
+    }
+    // the later tile needs the most keys; the loads cover its blocks and both
+    // tiles visit all of them (the earlier tile's extra block, at most one,
+    // is fully masked), so every stage is released by every tile
+    const int kend_c = kend[ntiles - 1];
+    const int nkb_c = nkb[ntiles - 1];
 
     if (tid == 0) {
         mbar_init(smem_addr(&q_full), 1);
-        mbar_init(smem_addr(&o_done), 1);
-        mbar_init(smem_addr(&drain), 1);
-        for (int i = 0; i < kTcStages; ++i) {
+        for (int i = 0; i < kTcKStages; ++i) {
             mbar_init(smem_addr(&k_full[i]), 1);
-            mbar_init(smem_addr(&k_empty[i]), 1);
-            mbar_init(smem_addr(&v_full[i]), 1);
-            mbar_init(smem_addr(&v_empty[i]), 1);
+            mbar_init(smem_addr(&k_empty[i]), ntiles);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_addr(&p_full[i]), 8);
-            mbar_init(smem_addr(&p_free[i]), 1);
+        for (int i = 0; i < kTcVStages; ++i) {
+            mbar_init(smem_addr(&v_full[i]), 1);
+            mbar_init(smem_addr(&v_empty[i]), ntiles);
+        }
+        for (int i = 0; i < kTcTiles; ++i) {
+            mbar_init(smem_addr(&drain[i]), 1);
             mbar_init(smem_addr(&s_full[i]), 1);
-            mbar_init(smem_addr(&s_free[i]), 8);
+            mbar_init(smem_addr(&p_full[i]), kTcSoftmaxThreads / 32);
+            mbar_init(smem_addr(&pv_done[i]), 1);
         }
         failed_s = 0;
         fence_barrier_init();
@@ -159,7 +178,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int kPastKeys = INT_MIN;
     auto page_entry = [&](int kb) {
         const int pg_idx = kb * NPG + lane;
-        return (lane < NPG && pg_idx * BS < kend) ? __ldg(bt + pg_idx) : kPastKeys;
+        return (lane < NPG && pg_idx * BS < kend_c) ? __ldg(bt + pg_idx) : kPastKeys;
     };
     // the page's first row in the cache; pages past the keys (and bad
     // entries, which are reported) read a row past the end: zeros
@@ -177,15 +196,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint64_t policy = l2_evict_first_policy();
         if (lane == 0) {
             const uint32_t bar = smem_addr(&q_full);
-            mbar_arrive_expect_tx(bar, kTcTile);
-            for (int sl = 0; sl < 2; ++sl)
-                tma_load_3d(base + kTcQOff + sl * kTcSlab, &tmQ, sl * 64, h * a.group, q0 + tok_begin, bar);
+            mbar_arrive_expect_tx(bar, ntiles * kTcTile);
+            for (int T = 0; T < ntiles; ++T)
+                for (int sl = 0; sl < 2; ++sl)
+                    tma_load_3d(base + kTcQOff + T * kTcTile + sl * kTcSlab, &tmQ, sl * 64, h * a.group,
+                                q0 + tok_begin[T], bar);
         }
         int e_next = page_entry(0);
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int st = kb % kTcStages, ph = (kb / kTcStages) & 1;
+        for (int kb = 0; kb < nkb_c; ++kb) {
+            const int st = kb % kTcKStages, ph = (kb / kTcKStages) & 1;
             const int y = page_row(e_next);
-            if (kb + 1 < nkb) e_next = page_entry(kb + 1);
+            if (kb + 1 < nkb_c) e_next = page_entry(kb + 1);
             if (lane == 0) {
                 if (!mbar_wait_bounded(smem_addr(&k_empty[st]), ph ^ 1, kTcWaitNs)) fail();
                 mbar_arrive_expect_tx(smem_addr(&k_full[st]), kTcTile);
@@ -201,10 +222,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ---------------- V loads: the same pages, from a second warp ----------------
         const uint64_t policy = l2_evict_first_policy();
         int e_next = page_entry(0);
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int st = kb % kTcStages, ph = (kb / kTcStages) & 1;
+        for (int kb = 0; kb < nkb_c; ++kb) {
+            const int st = kb % kTcVStages, ph = (kb / kTcVStages) & 1;
             const int y = page_row(e_next);
-            if (kb + 1 < nkb) e_next = page_entry(kb + 1);
+            if (kb + 1 < nkb_c) e_next = page_entry(kb + 1);
             if (lane == 0) {
                 if (!mbar_wait_bounded(smem_addr(&v_empty[st]), ph ^ 1, kTcWaitNs)) fail();
                 mbar_arrive_expect_tx(smem_addr(&v_full[st]), kTcTile);
@@ -216,201 +237,233 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 sl * 64, y, smem_addr(&v_full[st]), policy);
             }
         }
-    } else if (warp == kTcMmaWarp) {
-        // ---------------- MMA issue ----------------
-        if (lane == 0) {
+    } else if (warp == kTcMmaWarp || warp == kTcMmaWarpB) {
+        // ---------------- MMA issue, one thread per tile ----------------
+        // Per tile the chain is S(j) -> softmax -> PV(j) -> S(j + 1): P lives
+        // in S's columns, so S(j + 1) waits until PV(j) has read it.  The
+        // softmax warps alternate between the tiles, so each tile's PV and
+        // next S run on the tensor cores while they work on the other tile.
+        const int T = warp == kTcMmaWarp ? 0 : 1;
+        if (lane == 0 && T < ntiles) {
             constexpr uint32_t idesc_qk = tc_idesc_bf16(kTcRows, kTcKeys, 0, 0);
             constexpr uint32_t idesc_pv = tc_idesc_bf16(kTcRows, 128, 0, 1);
-            const uint32_t tS[2] = {tmem, tmem + 128};
-            const uint32_t tO = tmem + kTcOCol;
+            // A descriptor's start address is its low field (16-byte units,
+            // no carry out within shared memory): every operand descriptor is
+            // a base descriptor plus an offset, so issuing an MMA costs one add
+            const uint64_t q_desc = tc_smem_desc(base + kTcQOff, 16, 1024, 2);
+            const uint64_t k_desc = tc_smem_desc(base + kTcKOff, 16, 1024, 2);
+            const uint64_t v_desc = tc_smem_desc(base + kTcVOff, kTcSlab, 1024, 2);
             bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, kTcWaitNs);
-            auto issue_pv = [&](int j) {
-                const int pb = j & 1, vs = j % kTcStages;
-                ok = ok && mbar_wait_bounded(smem_addr(&p_full[pb]), (j >> 1) & 1, kTcWaitNs);
-                ok = ok && mbar_wait_bounded(smem_addr(&v_full[vs]), (j / kTcStages) & 1, kTcWaitNs);
+            auto qk = [&](int T, int kb) {  // S_T = Q_T K(kb)^T
+                const int ks = kb % kTcKStages;
+                ok = ok && mbar_wait_bounded(smem_addr(&k_full[ks]), (kb / kTcKStages) & 1, kTcWaitNs);
+                if (kb > 0) ok = ok && mbar_wait_bounded(smem_addr(&pv_done[T]), (kb - 1) & 1, kTcWaitNs);
                 tc_fence_after();
                 if (ok) {
-                    const uint32_t tP = tmem + kTcPCol + pb * 64;
-                    const uint32_t vbase = base + kTcVOff + vs * kTcTile;
-#pragma unroll
-                    for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-                        const uint64_t bd = tc_smem_desc(vbase + kk * 16 * 128, kTcSlab, 1024, 2);
-                        tc_mma_bf16_ts(tO, tP + kk * 8, bd, idesc_pv, j > 0 || kk > 0);
-                    }
-                }
-                tc_commit(smem_addr(&o_done));
-                tc_commit(smem_addr(&v_empty[vs]));
-                tc_commit(smem_addr(&p_free[pb]));
-            };
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int st = kb & 1, ks = kb % kTcStages;
-                ok = ok && mbar_wait_bounded(smem_addr(&k_full[ks]), (kb / kTcStages) & 1, kTcWaitNs);
-                ok = ok && mbar_wait_bounded(smem_addr(&s_free[st]), ((kb >> 1) & 1) ^ 1, kTcWaitNs);
-                tc_fence_after();
-                if (ok) {
-                    const uint32_t qbase = base + kTcQOff;
-                    const uint32_t kbase = base + kTcKOff + ks * kTcTile;
+                    const uint64_t a0 = q_desc + ((T * kTcTile) >> 4);
+                    const uint64_t b0 = k_desc + ((ks * kTcTile) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 128 / 16; ++kk) {
-                        const uint64_t ad = tc_smem_desc(qbase + (kk >> 2) * kTcSlab + (kk & 3) * 32, 16, 1024, 2);
-                        const uint64_t bd = tc_smem_desc(kbase + (kk >> 2) * kTcSlab + (kk & 3) * 32, 16, 1024, 2);
-                        tc_mma_bf16(tS[st], ad, bd, idesc_qk, kk > 0);
+                        const uint32_t off = ((kk >> 2) * kTcSlab + (kk & 3) * 32) >> 4;
+                        tc_mma_bf16(tmem + T * 128, a0 + off, b0 + off, idesc_qk, kk > 0);
                     }
                 }
-                tc_commit(smem_addr(&s_full[st]));
-                tc_commit(smem_addr(&k_empty[ks]));
-                if (kb >= 1) issue_pv(kb - 1);
+                tc_commit(smem_addr(&s_full[T]));
+            };
+            auto pv = [&](int T, int kb) {  // O_T += P_T V(kb)
+                const int vs = kb % kTcVStages;
+                ok = ok && mbar_wait_bounded(smem_addr(&p_full[T]), kb & 1, kTcWaitNs);
+                ok = ok && mbar_wait_bounded(smem_addr(&v_full[vs]), (kb / kTcVStages) & 1, kTcWaitNs);
+                tc_fence_after();
+                if (ok) {
+                    const uint64_t b0 = v_desc + ((vs * kTcTile) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < kTcKeys / 16; ++kk)
+                        tc_mma_bf16_ts(tmem + kTcOCol + T * 128, tmem + T * 128 + kk * 8, b0 + ((kk * 16 * 128) >> 4),
+                                       idesc_pv, kb > 0 || kk > 0);
+                }
+                tc_commit(smem_addr(&pv_done[T]));
+            };
+            qk(T, 0);
+            tc_commit(smem_addr(&k_empty[0]));
+            for (int kb = 0; kb < nkb_c; ++kb) {
+                pv(T, kb);
+                tc_commit(smem_addr(&v_empty[kb % kTcVStages]));
+                if (kb + 1 < nkb_c) {
+                    qk(T, kb + 1);
+                    tc_commit(smem_addr(&k_empty[(kb + 1) % kTcKStages]));
+                }
             }
-            issue_pv(nkb - 1);
             if (!ok) fail();
             // every MMA issued above is complete before the TMEM is released
-            tc_commit(smem_addr(&drain));
-            mbar_wait_bounded(smem_addr(&drain), 0, kTcWaitNs);
+            tc_commit(smem_addr(&drain[T]));
+            mbar_wait_bounded(smem_addr(&drain[T]), 0, kTcWaitNs);
         }
     } else {
-        // -------- softmax: two threads per query row, 64 columns each --------
+        // -------- softmax: two threads per query row, 64 columns each, --------
+        // -------- the two tiles in turn                                 --------
         const int quarter = warp & 3, half = warp >> 2;
         const int row = quarter * 32 + lane;
         const int t = row / a.group, g = row % a.group;
-        const bool live = tok_begin + t < tok_end;
-        const int pos = live ? first_pos + tok_begin + t : -1;
-        // blocks ending at or before every row's position need no mask
-        const int warp_min_pos = __reduce_min_sync(0xffffffffu, pos);
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t col0 = half * 64;  // this thread's columns of S, P and O
-        const uint32_t tO = tmem + lane_addr + kTcOCol + col0;
+        const uint32_t col0 = half * 64;  // this thread's columns of S and O
         const float scale = a.score_scale;
-        float m_ref = -INFINITY, l_run = 0.f;
-        bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int st = kb & 1, use = kb >> 1;
-            const int key0 = kb * kTcKeys + col0;
-            const bool masked = kb * kTcKeys + kTcKeys - 1 > warp_min_pos;
-            ok = ok && mbar_wait_bounded(smem_addr(&s_full[st]), use & 1, kTcWaitNs);
-            tc_fence_after();
-            float v[64];
-            {
-                float lo[32], hi[32];
-                tc_ld32(tmem + lane_addr + st * 128 + col0, lo);
-                tc_ld32(tmem + lane_addr + st * 128 + col0 + 32, hi);
-                tc_wait_ld();
+        int pos[kTcTiles], warp_min_pos[kTcTiles];
+        float m_ref[kTcTiles], l_run[kTcTiles];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    v[i] = lo[i];
-                    v[32 + i] = hi[i];
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&s_free[st]));  // S is in registers now
-            float mx = -INFINITY;
-            if (masked) {
-#pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    v[i] = key0 + i <= pos ? v[i] : -INFINITY;
-                    mx = fmaxf(mx, v[i]);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 64; ++i) mx = fmaxf(mx, v[i]);
-            }
-            // combine the two halves of the row (scale > 0 keeps the order)
-            half_max[half][row] = mx;
-            softmax_bar();
-            mx = fmaxf(mx, half_max[half ^ 1][row]);
-            const float mxs = mx * scale;
-            // move the reference max only when the row max outgrew it
-            bool rescale = false;
-            float alpha = 1.f;
-            if (mxs > m_ref + kTcRescaleThreshold) {
-                alpha = fast_exp2(m_ref - mxs);  // 0 when m_ref = -inf
-                m_ref = mxs;
-                l_run *= alpha;
-                rescale = kb > 0;
-            }
-            if (__any_sync(0xffffffffu, rescale)) {
-                // O must hold block kb-1's PV before it is scaled
-                ok = ok && mbar_wait_bounded(smem_addr(&o_done), (kb - 1) & 1, kTcWaitNs);
-                tc_fence_after();
-                float o0[32], o1[32];
-                tc_ld32(tO, o0);
-                tc_ld32(tO + 32, o1);
-                tc_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    o0[i] *= alpha;
-                    o1[i] *= alpha;
-                }
-                tc_st32(tO, o0);
-                tc_st32(tO + 32, o1);
-                tc_wait_st();
-            }
-            // P = exp2(scale * s - m_ref) (bf16) into this block's P buffer
-            const float neg = m_ref == -INFINITY ? 0.f : -m_ref;
-            float sum = 0.f;
-#pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                v[i] = fast_exp2(fmaf(v[i], scale, neg));  // masked: exp2(-inf) = 0
-                sum += v[i];
-            }
-            l_run += sum;
-            // both halves have read their partner's maximum: its slot is free
-            softmax_bar();
-            // P (bf16 pairs) into this block's P columns once PV(kb - 2) has read them
-            uint32_t pk[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) pk[i] = pack2<false>(v[2 * i], v[2 * i + 1]);
-            ok = ok && mbar_wait_bounded(smem_addr(&p_free[st]), (use & 1) ^ 1, kTcWaitNs);
-            tc_fence_after();
-            tc_st32(tmem + lane_addr + kTcPCol + st * 64 + half * 32, pk);
-            tc_wait_st();
-            if (kend - kb * kTcKeys < kTcKeys) {
-                // keys past the context in the last block may hold anything:
-                // zero those V rows (P is 0 there, but 0 x garbage could be NaN)
-                const int vs = kb % kTcStages;
-                ok = ok && mbar_wait_bounded(smem_addr(&v_full[vs]), (kb / kTcStages) & 1, kTcWaitNs);
-                const int valid = kend - kb * kTcKeys;
-                const uint32_t vbase = base + kTcVOff + vs * kTcTile;
-                for (int r2 = valid + tid; r2 < kTcKeys; r2 += kTcSoftmaxThreads)
-                    for (int sl = 0; sl < 2; ++sl)
-                        for (int c16 = 0; c16 < 8; ++c16)
-                            st_shared_zero16(vbase + sl * kTcSlab + r2 * 128 + c16 * 16);
-                fence_proxy_async_smem();
-                softmax_bar();  // every softmax warp zeroed its rows
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&p_full[st]));
+        for (int T = 0; T < kTcTiles; ++T) {
+            const bool live = T < ntiles && tok_begin[T] + t < chunk;
+            pos[T] = live ? first_pos + tok_begin[T] + t : -1;
+            // blocks ending at or before every row's position need no mask
+            warp_min_pos[T] = __reduce_min_sync(0xffffffffu, pos[T]);
+            m_ref[T] = -INFINITY;
+            l_run[T] = 0.f;
         }
-        // every PV is done once the MMA warp's final commit lands (o_done can
-        // be two phases behind here, too far for a parity wait)
-        ok = ok && mbar_wait_bounded(smem_addr(&drain), 0, kTcWaitNs);
+        bool ok = true;
+        for (int kb = 0; kb < nkb_c; ++kb) {
+#pragma unroll
+            for (int T = 0; T < kTcTiles; ++T) {
+                if (T >= ntiles) continue;  // uniform over the softmax warps
+                const uint32_t tS = tmem + lane_addr + T * 128;
+                const uint32_t tO = tmem + lane_addr + kTcOCol + T * 128 + col0;
+                const int key0 = kb * kTcKeys + col0;
+                const bool masked = kb * kTcKeys + kTcKeys - 1 > warp_min_pos[T];
+                ok = ok && mbar_wait_bounded(smem_addr(&s_full[T]), kb & 1, kTcWaitNs);
+                tc_fence_after();
+                float v[64];
+                {
+                    float lo[32], hi[32];
+                    tc_ld32(tS + col0, lo);
+                    tc_ld32(tS + col0 + 32, hi);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        v[i] = lo[i];
+                        v[32 + i] = hi[i];
+                    }
+                }
+                if (masked) {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) v[i] = key0 + i <= pos[T] ? v[i] : -INFINITY;
+                }
+                // row max of this half: four independent chains of 3-input maxima
+                float mq[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    mq[q] = fmax3(v[16 * q], v[16 * q + 1], v[16 * q + 2]);
+#pragma unroll
+                    for (int i = 3; i < 15; i += 2) mq[q] = fmax3(mq[q], v[16 * q + i], v[16 * q + i + 1]);
+                    mq[q] = fmaxf(mq[q], v[16 * q + 15]);
+                }
+                float mx = fmaxf(fmax3(mq[0], mq[1], mq[2]), mq[3]);
+                // combine the two halves of the row (scale > 0 keeps the
+                // order); past this barrier both halves have S in registers,
+                // so P may overwrite it
+                half_max[half][row] = mx;
+                tc_fence_before();
+                softmax_bar();
+                tc_fence_after();
+                mx = fmaxf(mx, half_max[half ^ 1][row]);
+                const float mxs = mx * scale;
+                // move the reference max only when the row max outgrew it;
+                // O holds PV(kb - 1) here: S(kb) was computed after it
+                bool rescale = false;
+                float alpha = 1.f;
+                if (mxs > m_ref[T] + kTcRescaleThreshold) {
+                    alpha = fast_exp2(m_ref[T] - mxs);  // 0 when m_ref = -inf
+                    m_ref[T] = mxs;
+                    l_run[T] *= alpha;
+                    rescale = kb > 0;
+                }
+                if (__any_sync(0xffffffffu, rescale)) {
+                    float o0[32], o1[32];
+                    tc_ld32(tO, o0);
+                    tc_ld32(tO + 32, o1);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        o0[i] *= alpha;
+                        o1[i] *= alpha;
+                    }
+                    tc_st32(tO, o0);
+                    tc_st32(tO + 32, o1);
+                    tc_wait_st();
+                }
+                // P = exp2(scale * s - m_ref) (bf16)
+                const float neg = m_ref[T] == -INFINITY ? 0.f : -m_ref[T];
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < 64; i += 2) {
+                    ffma2(v[i], v[i + 1], scale, neg);
+                    v[i] = fast_exp2(v[i]);  // masked: exp2(-inf) = 0
+                    v[i + 1] = fast_exp2(v[i + 1]);
+                    fadd2(sa[(i >> 1) & 3], sb[(i >> 1) & 3], v[i], v[i + 1]);
+                }
+                fadd2(sa[0], sb[0], sa[1], sb[1]);
+                fadd2(sa[2], sb[2], sa[3], sb[3]);
+                fadd2(sa[0], sb[0], sa[2], sb[2]);
+                l_run[T] += sa[0] + sb[0];
+                // both halves have read their partner's maximum: its slot is free
+                softmax_bar();
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) pk[i] = pack2<false>(v[2 * i], v[2 * i + 1]);
+                tc_st32(tS + half * 32, pk);
+                tc_wait_st();
+                if (kb == nkb_c - 1 && T == 0 && kend_c - kb * kTcKeys < kTcKeys) {
+                    // keys past the context in the last block may hold
+                    // anything: zero those V rows before the first PV reads
+                    // them (P is 0 there, but 0 x garbage could be NaN)
+                    const int vs = kb % kTcVStages;
+                    ok = ok && mbar_wait_bounded(smem_addr(&v_full[vs]), (kb / kTcVStages) & 1, kTcWaitNs);
+                    const int valid = kend_c - kb * kTcKeys;
+                    const uint32_t vbase = base + kTcVOff + vs * kTcTile;
+                    for (int r2 = valid + tid; r2 < kTcKeys; r2 += kTcSoftmaxThreads)
+                        for (int sl = 0; sl < 2; ++sl)
+                            for (int c16 = 0; c16 < 8; ++c16)
+                                st_shared_zero16(vbase + sl * kTcSlab + r2 * 128 + c16 * 16);
+                    fence_proxy_async_smem();
+                    softmax_bar();  // every softmax warp zeroed its rows
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&p_full[T]));
+            }
+        }
+        // every PV is done once the MMA threads' final commits land
+        for (int T = 0; T < ntiles; ++T) ok = ok && mbar_wait_bounded(smem_addr(&drain[T]), 0, kTcWaitNs);
         tc_fence_after();
         if (!ok) fail();
-        half_max[half][row] = l_run;
-        softmax_bar();
-        const float l = half_max[0][row] + half_max[1][row];
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16 *dst = a.out + ((static_cast<int64_t>(q0) + tok_begin + t) * a.num_q_heads +
-                                      h * a.group + g) * 128 + col0;
-        float o0[32], o1[32];
-        tc_ld32(tO, o0);
-        tc_ld32(tO + 32, o1);
-        tc_wait_ld();
-        if (live && !failed_s) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-                uint4 w0, w1;
-                w0.x = pack2<false>(o0[i] * inv, o0[i + 1] * inv);
-                w0.y = pack2<false>(o0[i + 2] * inv, o0[i + 3] * inv);
-                w0.z = pack2<false>(o0[i + 4] * inv, o0[i + 5] * inv);
-                w0.w = pack2<false>(o0[i + 6] * inv, o0[i + 7] * inv);
-                w1.x = pack2<false>(o1[i] * inv, o1[i + 1] * inv);
-                w1.y = pack2<false>(o1[i + 2] * inv, o1[i + 3] * inv);
-                w1.z = pack2<false>(o1[i + 4] * inv, o1[i + 5] * inv);
-                w1.w = pack2<false>(o1[i + 6] * inv, o1[i + 7] * inv);
-                *reinterpret_cast<uint4 *>(dst + i) = w0;
-                *reinterpret_cast<uint4 *>(dst + 32 + i) = w1;
+        for (int T = 0; T < kTcTiles; ++T) {
+            if (T >= ntiles) continue;
+            half_max[half][row] = l_run[T];
+            softmax_bar();
+            const float l = half_max[0][row] + half_max[1][row];
+            softmax_bar();  // both read before the next tile's sums overwrite them
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const uint32_t tO = tmem + lane_addr + kTcOCol + T * 128 + col0;
+            float o0[32], o1[32];
+            tc_ld32(tO, o0);
+            tc_ld32(tO + 32, o1);
+            tc_wait_ld();
+            if (pos[T] >= 0 && !failed_s) {
+                __nv_bfloat16 *dst = a.out + ((static_cast<int64_t>(q0) + tok_begin[T] + t) * a.num_q_heads +
+                                              h * a.group + g) * 128 + col0;
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                    uint4 w0, w1;
+                    w0.x = pack2<false>(o0[i] * inv, o0[i + 1] * inv);
+                    w0.y = pack2<false>(o0[i + 2] * inv, o0[i + 3] * inv);
+                    w0.z = pack2<false>(o0[i + 4] * inv, o0[i + 5] * inv);
+                    w0.w = pack2<false>(o0[i + 6] * inv, o0[i + 7] * inv);
+                    w1.x = pack2<false>(o1[i] * inv, o1[i + 1] * inv);
+                    w1.y = pack2<false>(o1[i + 2] * inv, o1[i + 3] * inv);
+                    w1.z = pack2<false>(o1[i + 4] * inv, o1[i + 5] * inv);
+                    w1.w = pack2<false>(o1[i + 6] * inv, o1[i + 7] * inv);
+                    *reinterpret_cast<uint4 *>(dst + i) = w0;
+                    *reinterpret_cast<uint4 *>(dst + 32 + i) = w1;
+                }
             }
         }
     }
@@ -493,7 +546,8 @@ pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_ca
     if (st != PA_OK) return st;
     st = make_map(&tv, v_cache, false, 128, rows, block_size);
     if (st != PA_OK) return st;
-    dim3 grid((max_query_len + a.tile_tokens - 1) / a.tile_tokens, num_kv_heads, num_seqs);
+    const int tiles = (max_query_len + a.tile_tokens - 1) / a.tile_tokens;
+    dim3 grid((tiles + kTcTiles - 1) / kTcTiles, num_kv_heads, num_seqs);
     return block_size == 16 ? launch_tc<16>(tq, tk, tv, a, grid, stream)
                             : launch_tc<32>(tq, tk, tv, a, grid, stream);
 }
