@@ -3,27 +3,27 @@
 // Same computation as pa_prefill.cu (causal attention of each chunk token over
 // its sequence's cached prefix and earlier chunk tokens, through the block
 // table), organised for sm_103a's asynchronous tensor cores:
-//  * One CTA per (query tile of 128 rows = (chunk token, query head of the KV
-//    head's group) pairs, KV head, sequence), one CTA per SM (225 KB of
-//    shared memory: the query tile and three K and three V stages; all 512
-//    TMEM columns: two S accumulators, O, and two P buffers).
-//  * Warp 8 streams the tile's queries (one 3-D TMA box per 64-dim slab) and
-//    the K pages of each block of 128 keys; warp 10 streams the V pages.
-//    Lane p issues page p's boxes (2-D TMA, hardware 128-byte swizzle), with
-//    the block table read one block ahead.
-//  * Warp 9 owns the tensor memory and one lane issues the MMAs:
-//    S = Q K^T (M 128 x N 128 x K 128, both operands K-major in shared
-//    memory) into one of two S accumulators, and O += P V (P read from
-//    tensor memory, V read MN-major straight from the page layout) into the
-//    O accumulator; each group is committed to an mbarrier.
-//  * Warps 0-7 do the softmax: a query row is TMEM lane (warp % 4) * 32 +
-//    lane, and warps w and w + 4 take its two 64-column halves (their
-//    partial maxima meet in shared memory once per block).  They read S,
-//    apply the causal mask, keep the row's sum against a reference max that
-//    only moves when the row max outgrows it by 2^8 (so O is rescaled in
-//    tensor memory rarely), and store P as bf16 pairs into one of two P
-//    buffers in tensor memory.  While they work on block j the tensor cores
-//    finish block j - 1's PV and compute S for block j + 1.
+//  * One CTA per (two neighbouring query tiles, KV head, sequence).  A tile is
+//    128 rows = (chunk token, query head of the KV head's group) pairs; both
+//    tiles read every K/V stage, so each SM moves half the page bytes per
+//    FLOP that one tile per CTA would.  One CTA per SM: 225 KB of shared
+//    memory (both query tiles, five K and five V stages of 64 keys) and all
+//    512 TMEM columns (per tile: two S buffers of 64 columns and O).
+//  * Warp 8 streams the queries (3-D TMA) and the K pages of each block of
+//    64 keys, warp 10 the V pages; lane p issues page p's 2-D TMA boxes
+//    (hardware 128-byte swizzle), with the block table read one block ahead.
+//    Warp 10 also zeroes the V rows past the context in the last block.
+//  * Warp 9 + 2 T issues tile T's MMAs (tcgen05.mma.cta_group::1.kind::f16,
+//    one thread): S = Q K^T (M 128 x N 64 x K 128, both operands K-major
+//    in shared memory) into one of two S buffers, and O += P V (P read from
+//    tensor memory, V read MN-major straight from the page layout).  Each
+//    group is committed to an mbarrier.  S(j + 1) is computed while the
+//    softmax works on S(j).
+//  * Warps 4 T .. 4 T + 3 do tile T's softmax, one query row (TMEM lane) per
+//    thread: read S, apply the causal mask, keep the row's sum against a
+//    reference max that only moves when the row max outgrows it by 2^8 (so
+//    O is rescaled in tensor memory rarely), and store P as bf16 pairs over
+//    the first half of S(j), which PV(j) reads.
 #include <cudaTypedefs.h>
 #include <limits.h>
 #include <math.h>
@@ -50,40 +50,34 @@ struct PrefillTcArgs {
 };
 
 constexpr int kTcRows = 128;          // query rows per tile (TMEM lanes)
-constexpr int kTcKeys = 128;          // keys per block
+constexpr int kTcKeys = 64;           // keys per block
 constexpr int kTcTiles = 2;           // query tiles per CTA; both read every K/V stage
-// warps 0-7 softmax (2 per row), 8 Q/K loads, 9 and 11 the MMAs of tiles 0
-// and 1 (two issuing threads, on sub-partitions apart from each other and
-// from the loaders, so neither tile's chain waits behind the other's), 10 V loads
+// warps 0-3 softmax of tile 0 and 4-7 of tile 1 (one query row per thread),
+// 8 Q/K loads, 9 and 11 the MMAs of tiles 0 and 1, 10 V loads
 constexpr int kTcThreads = 384;
-constexpr int kTcSoftmaxThreads = 256;
 constexpr int kTcLoadWarp = 8;
 constexpr int kTcMmaWarp = 9;
 constexpr int kTcVLoadWarp = 10;
 constexpr int kTcMmaWarpB = 11;
-constexpr int kTcSlab = 16384;        // one 64-dim slab of 128 rows x 128 B
-constexpr int kTcTile = 2 * kTcSlab;  // 128 rows x 128 dims bf16
-constexpr int kTcKStages = 3;
-constexpr int kTcVStages = 2;
-constexpr int kTcQOff = 0;                                   // one query tile after the other
-constexpr int kTcKOff = kTcTiles * kTcTile;
-constexpr int kTcVOff = kTcKOff + kTcKStages * kTcTile;
-constexpr int kTcSmem = kTcVOff + kTcVStages * kTcTile + 1024;
+constexpr int kTcQSlab = 16384;       // 64 dims of a 128-row query tile
+constexpr int kTcQTile = 2 * kTcQSlab;
+constexpr int kTcKVSlab = kTcKeys * 128;  // 64 dims of a 64-key block
+constexpr int kTcKVStage = 2 * kTcKVSlab;
+constexpr int kTcStages = 5;          // K and V rings
+constexpr int kTcQOff = 0;                            // one query tile after the other
+constexpr int kTcKOff = kTcTiles * kTcQTile;
+constexpr int kTcVOff = kTcKOff + kTcStages * kTcKVStage;
+constexpr int kTcSmem = kTcVOff + kTcStages * kTcKVStage + 1024;
 // P is written against a reference max that only moves when the row max
 // grows past it by more than this (base-2 units): P <= 2^8, and O is
 // rescaled in tensor memory only then.
 constexpr float kTcRescaleThreshold = 8.f;
-// Tensor memory: S of tile T at columns [128 T, 128 T + 128), O of tile T at
-// [256 + 128 T, ...); P of tile T (bf16 pairs, 64 columns) over the first
-// half of its S once the softmax has read S.
+// Tensor memory, tile T at columns [256 T, 256 T + 256): S of even blocks
+// [0, 64), S of odd blocks [64, 128), O [128, 256).  P of a block (bf16
+// pairs, 32 columns) is written over the first half of that block's S.
 constexpr int kTcTmemCols = 512;
-constexpr int kTcOCol = 256;
+constexpr int kTcOCol = 128;
 constexpr uint64_t kTcWaitNs = 2000000000ull;
-
-// Named barrier 1 over the softmax warps only.
-__device__ __forceinline__ void softmax_bar() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kTcSoftmaxThreads) : "memory");
-}
 
 template <int BS>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -91,15 +85,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       const __grid_constant__ CUtensorMap tmV, const PrefillTcArgs a) {
     constexpr int NPG = kTcKeys / BS;  // pages per key block
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t q_full, drain[kTcTiles];
-    __shared__ __align__(8) uint64_t k_full[kTcKStages], k_empty[kTcKStages], v_full[kTcVStages],
-        v_empty[kTcVStages];
-    __shared__ __align__(8) uint64_t s_full[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles];
+    __shared__ __align__(8) uint64_t q_full, v_zeroed;
+    __shared__ __align__(8) uint64_t k_full[kTcStages], k_empty[kTcStages], v_full[kTcStages], v_empty[kTcStages];
+    __shared__ __align__(8) uint64_t s_full[kTcTiles][2], p_full[kTcTiles][2], pv_done[kTcTiles], drain[kTcTiles];
     __shared__ uint32_t tmem_base_s;
     __shared__ int failed_s;
-    // per-row partial maxima of the two column halves (at the end: the
-    // partial row sums)
-    __shared__ float half_max[2][kTcRows];
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -110,43 +100,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q0 = a.query_start[s];
     const int chunk = a.query_start[s + 1] - q0;
     const int ctx = a.context_lens[s];
-    int tok_begin[kTcTiles], kend[kTcTiles], nkb[kTcTiles];
-#pragma unroll
-    for (int T = 0; T < kTcTiles; ++T) tok_begin[T] = (kTcTiles * pair + T) * a.tile_tokens;
+    const int tok_begin0 = kTcTiles * pair * a.tile_tokens;
     // uniform exits, before any barrier or TMEM use
     if (ctx > a.max_blocks * BS || ctx < chunk) {
-        if (tid == 0 && tok_begin[0] < chunk) set_device_error(a.err, PA_DEVERR_BAD_CONTEXT);
+        if (tid == 0 && tok_begin0 < chunk) set_device_error(a.err, PA_DEVERR_BAD_CONTEXT);
         return;
     }
-    if (tok_begin[0] >= chunk) return;
-    const int ntiles = tok_begin[1] < chunk ? 2 : 1;
+    if (tok_begin0 >= chunk) return;
+    const int ntiles = tok_begin0 + a.tile_tokens < chunk ? 2 : 1;
     const int first_pos = ctx - chunk;
-#pragma unroll
-    for (int T = 0; T < kTcTiles; ++T) {
-        kend[T] = first_pos + min(tok_begin[T] + a.tile_tokens, chunk);  // keys [0, kend)
-        nkb[T] = (kend[T] + kTcKeys - 1) / kTcKeys;
-    }
-    // the later tile needs the most keys; the loads cover its blocks and both
-    // tiles visit all of them (the earlier tile's extra block, at most one,
-    // is fully masked), so every stage is released by every tile
-    const int kend_c = kend[ntiles - 1];
-    const int nkb_c = nkb[ntiles - 1];
+    // keys [0, kend) cover the later tile's last row; both tiles visit every
+    // block (rows past their own position are masked), so each stage is
+    // released once per tile
+    const int kend = first_pos + min(tok_begin0 + ntiles * a.tile_tokens, chunk);
+    const int nkb = (kend + kTcKeys - 1) / kTcKeys;
+    const bool partial = kend % kTcKeys != 0;  // the last block holds keys past the context
 
     if (tid == 0) {
         mbar_init(smem_addr(&q_full), 1);
-        for (int i = 0; i < kTcKStages; ++i) {
+        mbar_init(smem_addr(&v_zeroed), 1);
+        for (int i = 0; i < kTcStages; ++i) {
             mbar_init(smem_addr(&k_full[i]), 1);
             mbar_init(smem_addr(&k_empty[i]), ntiles);
-        }
-        for (int i = 0; i < kTcVStages; ++i) {
             mbar_init(smem_addr(&v_full[i]), 1);
             mbar_init(smem_addr(&v_empty[i]), ntiles);
         }
-        for (int i = 0; i < kTcTiles; ++i) {
-            mbar_init(smem_addr(&drain[i]), 1);
-            mbar_init(smem_addr(&s_full[i]), 1);
-            mbar_init(smem_addr(&p_full[i]), kTcSoftmaxThreads / 32);
-            mbar_init(smem_addr(&pv_done[i]), 1);
+        for (int t = 0; t < kTcTiles; ++t) {
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(smem_addr(&s_full[t][b]), 1);
+                mbar_init(smem_addr(&p_full[t][b]), 4);
+            }
+            mbar_init(smem_addr(&pv_done[t]), 1);
+            mbar_init(smem_addr(&drain[t]), 1);
         }
         failed_s = 0;
         fence_barrier_init();
@@ -178,7 +163,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int kPastKeys = INT_MIN;
     auto page_entry = [&](int kb) {
         const int pg_idx = kb * NPG + lane;
-        return (lane < NPG && pg_idx * BS < kend_c) ? __ldg(bt + pg_idx) : kPastKeys;
+        return (lane < NPG && pg_idx * BS < kend) ? __ldg(bt + pg_idx) : kPastKeys;
     };
     // the page's first row in the cache; pages past the keys (and bad
     // entries, which are reported) read a row past the end: zeros
@@ -191,108 +176,106 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return (blk * a.num_kv_heads + h) * BS;
     };
 
-    if (warp == kTcLoadWarp) {
-        // ---------------- Q and K loads ----------------
+    if (warp == kTcLoadWarp || warp == kTcVLoadWarp) {
+        // ------------- loads: warp 8 the queries and K, warp 10 V -------------
+        const bool is_k = warp == kTcLoadWarp;
+        const CUtensorMap *map = is_k ? &tmK : &tmV;
+        uint64_t *full = is_k ? k_full : v_full;
+        uint64_t *empty = is_k ? k_empty : v_empty;
+        const uint32_t ring = base + (is_k ? kTcKOff : kTcVOff);
         const uint64_t policy = l2_evict_first_policy();
-        if (lane == 0) {
+        if (is_k && lane == 0) {
             const uint32_t bar = smem_addr(&q_full);
-            mbar_arrive_expect_tx(bar, ntiles * kTcTile);
+            mbar_arrive_expect_tx(bar, ntiles * kTcQTile);
             for (int T = 0; T < ntiles; ++T)
                 for (int sl = 0; sl < 2; ++sl)
-                    tma_load_3d(base + kTcQOff + T * kTcTile + sl * kTcSlab, &tmQ, sl * 64, h * a.group,
-                                q0 + tok_begin[T], bar);
+                    tma_load_3d(base + kTcQOff + T * kTcQTile + sl * kTcQSlab, &tmQ, sl * 64, h * a.group,
+                                q0 + tok_begin0 + T * a.tile_tokens, bar);
         }
         int e_next = page_entry(0);
-        for (int kb = 0; kb < nkb_c; ++kb) {
-            const int st = kb % kTcKStages, ph = (kb / kTcKStages) & 1;
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int st = kb % kTcStages, ph = (kb / kTcStages) & 1;
             const int y = page_row(e_next);
-            if (kb + 1 < nkb_c) e_next = page_entry(kb + 1);
+            if (kb + 1 < nkb) e_next = page_entry(kb + 1);
             if (lane == 0) {
-                if (!mbar_wait_bounded(smem_addr(&k_empty[st]), ph ^ 1, kTcWaitNs)) fail();
-                mbar_arrive_expect_tx(smem_addr(&k_full[st]), kTcTile);
+                if (!mbar_wait_bounded(smem_addr(&empty[st]), ph ^ 1, kTcWaitNs)) fail();
+                mbar_arrive_expect_tx(smem_addr(&full[st]), kTcKVStage);
             }
             __syncwarp();
             if (lane < NPG) {
                 for (int sl = 0; sl < 2; ++sl)
-                    tma_load_2d(base + kTcKOff + st * kTcTile + sl * kTcSlab + lane * BS * 128, &tmK,
-                                sl * 64, y, smem_addr(&k_full[st]), policy);
+                    tma_load_2d(ring + st * kTcKVStage + sl * kTcKVSlab + lane * BS * 128, map, sl * 64, y,
+                                smem_addr(&full[st]), policy);
             }
         }
-    } else if (warp == kTcVLoadWarp) {
-        // ---------------- V loads: the same pages, from a second warp ----------------
-        const uint64_t policy = l2_evict_first_policy();
-        int e_next = page_entry(0);
-        for (int kb = 0; kb < nkb_c; ++kb) {
-            const int st = kb % kTcVStages, ph = (kb / kTcVStages) & 1;
-            const int y = page_row(e_next);
-            if (kb + 1 < nkb_c) e_next = page_entry(kb + 1);
-            if (lane == 0) {
-                if (!mbar_wait_bounded(smem_addr(&v_empty[st]), ph ^ 1, kTcWaitNs)) fail();
-                mbar_arrive_expect_tx(smem_addr(&v_full[st]), kTcTile);
-            }
+        if (!is_k && partial) {
+            // keys past the context in the last block may hold anything:
+            // zero those V rows before a PV reads them (P is 0 there, but
+            // 0 x garbage could be NaN)
+            const int kb = nkb - 1, st = kb % kTcStages;
+            if (lane == 0 && !mbar_wait_bounded(smem_addr(&v_full[st]), (kb / kTcStages) & 1, kTcWaitNs)) fail();
             __syncwarp();
-            if (lane < NPG) {
+            const uint32_t vbase = base + kTcVOff + st * kTcKVStage;
+            for (int r2 = kend - kb * kTcKeys + lane; r2 < kTcKeys; r2 += 32)
                 for (int sl = 0; sl < 2; ++sl)
-                    tma_load_2d(base + kTcVOff + st * kTcTile + sl * kTcSlab + lane * BS * 128, &tmV,
-                                sl * 64, y, smem_addr(&v_full[st]), policy);
-            }
+                    for (int c16 = 0; c16 < 8; ++c16)
+                        st_shared_zero16(vbase + sl * kTcKVSlab + r2 * 128 + c16 * 16);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&v_zeroed));
         }
     } else if (warp == kTcMmaWarp || warp == kTcMmaWarpB) {
         // ---------------- MMA issue, one thread per tile ----------------
-        // Per tile the chain is S(j) -> softmax -> PV(j) -> S(j + 1): P lives
-        // in S's columns, so S(j + 1) waits until PV(j) has read it.  The
-        // softmax warps alternate between the tiles, so each tile's PV and
-        // next S run on the tensor cores while they work on the other tile.
+        // S(j + 1) is computed while the softmax works on S(j); P(j) lives in
+        // S(j)'s columns, so S(j + 2) waits until PV(j) has read it.
         const int T = warp == kTcMmaWarp ? 0 : 1;
         if (lane == 0 && T < ntiles) {
             constexpr uint32_t idesc_qk = tc_idesc_bf16(kTcRows, kTcKeys, 0, 0);
             constexpr uint32_t idesc_pv = tc_idesc_bf16(kTcRows, 128, 0, 1);
-            // A descriptor's start address is its low field (16-byte units,
+            // a descriptor's start address is its low field (16-byte units,
             // no carry out within shared memory): every operand descriptor is
             // a base descriptor plus an offset, so issuing an MMA costs one add
-            const uint64_t q_desc = tc_smem_desc(base + kTcQOff, 16, 1024, 2);
+            const uint64_t q_desc = tc_smem_desc(base + kTcQOff + T * kTcQTile, 16, 1024, 2);
             const uint64_t k_desc = tc_smem_desc(base + kTcKOff, 16, 1024, 2);
-            const uint64_t v_desc = tc_smem_desc(base + kTcVOff, kTcSlab, 1024, 2);
+            const uint64_t v_desc = tc_smem_desc(base + kTcVOff, kTcKVSlab, 1024, 2);
+            const uint32_t tS = tmem + T * 256, tO = tS + kTcOCol;
             bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, kTcWaitNs);
-            auto qk = [&](int T, int kb) {  // S_T = Q_T K(kb)^T
-                const int ks = kb % kTcKStages;
-                ok = ok && mbar_wait_bounded(smem_addr(&k_full[ks]), (kb / kTcKStages) & 1, kTcWaitNs);
-                if (kb > 0) ok = ok && mbar_wait_bounded(smem_addr(&pv_done[T]), (kb - 1) & 1, kTcWaitNs);
+            auto qk = [&](int kb) {  // S(kb) = Q K(kb)^T
+                const int ks = kb % kTcStages, b = kb & 1;
+                ok = ok && mbar_wait_bounded(smem_addr(&k_full[ks]), (kb / kTcStages) & 1, kTcWaitNs);
+                // S(kb)'s columns held P(kb - 2): PV(kb - 2) must have read them
+                if (kb >= 2) ok = ok && mbar_wait_bounded(smem_addr(&pv_done[T]), kb & 1, kTcWaitNs);
                 tc_fence_after();
                 if (ok) {
-                    const uint64_t a0 = q_desc + ((T * kTcTile) >> 4);
-                    const uint64_t b0 = k_desc + ((ks * kTcTile) >> 4);
+                    const uint64_t b0 = k_desc + ((ks * kTcKVStage) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 128 / 16; ++kk) {
-                        const uint32_t off = ((kk >> 2) * kTcSlab + (kk & 3) * 32) >> 4;
-                        tc_mma_bf16(tmem + T * 128, a0 + off, b0 + off, idesc_qk, kk > 0);
+                        const uint32_t qoff = ((kk >> 2) * kTcQSlab + (kk & 3) * 32) >> 4;
+                        const uint32_t koff = ((kk >> 2) * kTcKVSlab + (kk & 3) * 32) >> 4;
+                        tc_mma_bf16(tS + b * 64, q_desc + qoff, b0 + koff, idesc_qk, kk > 0);
                     }
                 }
-                tc_commit(smem_addr(&s_full[T]));
+                tc_commit(smem_addr(&s_full[T][b]));
+                tc_commit(smem_addr(&k_empty[ks]));
             };
-            auto pv = [&](int T, int kb) {  // O_T += P_T V(kb)
-                const int vs = kb % kTcVStages;
-                ok = ok && mbar_wait_bounded(smem_addr(&p_full[T]), kb & 1, kTcWaitNs);
-                ok = ok && mbar_wait_bounded(smem_addr(&v_full[vs]), (kb / kTcVStages) & 1, kTcWaitNs);
+            qk(0);
+            if (nkb > 1) qk(1);
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int vs = kb % kTcStages, b = kb & 1;
+                ok = ok && mbar_wait_bounded(smem_addr(&p_full[T][b]), (kb >> 1) & 1, kTcWaitNs);
+                ok = ok && mbar_wait_bounded(smem_addr(&v_full[vs]), (kb / kTcStages) & 1, kTcWaitNs);
+                if (kb == nkb - 1 && partial) ok = ok && mbar_wait_bounded(smem_addr(&v_zeroed), 0, kTcWaitNs);
                 tc_fence_after();
-                if (ok) {
-                    const uint64_t b0 = v_desc + ((vs * kTcTile) >> 4);
+                if (ok) {  // O += P(kb) V(kb)
+                    const uint64_t b0 = v_desc + ((vs * kTcKVStage) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kTcKeys / 16; ++kk)
-                        tc_mma_bf16_ts(tmem + kTcOCol + T * 128, tmem + T * 128 + kk * 8, b0 + ((kk * 16 * 128) >> 4),
-                                       idesc_pv, kb > 0 || kk > 0);
+                        tc_mma_bf16_ts(tO, tS + b * 64 + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_pv,
+                                       kb > 0 || kk > 0);
                 }
                 tc_commit(smem_addr(&pv_done[T]));
-            };
-            qk(T, 0);
-            tc_commit(smem_addr(&k_empty[0]));
-            for (int kb = 0; kb < nkb_c; ++kb) {
-                pv(T, kb);
-                tc_commit(smem_addr(&v_empty[kb % kTcVStages]));
-                if (kb + 1 < nkb_c) {
-                    qk(T, kb + 1);
-                    tc_commit(smem_addr(&k_empty[(kb + 1) % kTcKStages]));
-                }
+                tc_commit(smem_addr(&v_empty[vs]));
+                if (kb + 2 < nkb) qk(kb + 2);
             }
             if (!ok) fail();
             // every MMA issued above is complete before the TMEM is released
@@ -300,41 +283,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_wait_bounded(smem_addr(&drain[T]), 0, kTcWaitNs);
         }
     } else {
-        // -------- softmax: two threads per query row, 64 columns each, --------
-        // -------- the two tiles in turn                                 --------
-        const int quarter = warp & 3, half = warp >> 2;
-        const int row = quarter * 32 + lane;
-        const int t = row / a.group, g = row % a.group;
-        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t col0 = half * 64;  // this thread's columns of S and O
-        const float scale = a.score_scale;
-        int pos[kTcTiles], warp_min_pos[kTcTiles];
-        float m_ref[kTcTiles], l_run[kTcTiles];
-#pragma unroll
-        for (int T = 0; T < kTcTiles; ++T) {
-            const bool live = T < ntiles && tok_begin[T] + t < chunk;
-            pos[T] = live ? first_pos + tok_begin[T] + t : -1;
+        // ------------- softmax: one query row per thread, 64 keys a block -------------
+        const int T = warp >> 2;
+        if (T < ntiles) {
+            const int row = (warp & 3) * 32 + lane;
+            const int t = row / a.group, g = row % a.group;
+            const int tok_begin = tok_begin0 + T * a.tile_tokens;
+            const bool live = tok_begin + t < chunk;
+            const int pos = live ? first_pos + tok_begin + t : -1;
             // blocks ending at or before every row's position need no mask
-            warp_min_pos[T] = __reduce_min_sync(0xffffffffu, pos[T]);
-            m_ref[T] = -INFINITY;
-            l_run[T] = 0.f;
-        }
-        bool ok = true;
-        for (int kb = 0; kb < nkb_c; ++kb) {
-#pragma unroll
-            for (int T = 0; T < kTcTiles; ++T) {
-                if (T >= ntiles) continue;  // uniform over the softmax warps
-                const uint32_t tS = tmem + lane_addr + T * 128;
-                const uint32_t tO = tmem + lane_addr + kTcOCol + T * 128 + col0;
-                const int key0 = kb * kTcKeys + col0;
-                const bool masked = kb * kTcKeys + kTcKeys - 1 > warp_min_pos[T];
-                ok = ok && mbar_wait_bounded(smem_addr(&s_full[T]), kb & 1, kTcWaitNs);
+            const int warp_min_pos = __reduce_min_sync(0xffffffffu, pos);
+            const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+            const uint32_t tS = tmem + lane_addr + T * 256, tO = tS + kTcOCol;
+            const float scale = a.score_scale;
+            float m_ref = -INFINITY, l_run = 0.f;
+            bool ok = true;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int b = kb & 1;
+                const int key0 = kb * kTcKeys;
+                const bool masked = key0 + kTcKeys - 1 > warp_min_pos;
+                ok = ok && mbar_wait_bounded(smem_addr(&s_full[T][b]), (kb >> 1) & 1, kTcWaitNs);
                 tc_fence_after();
                 float v[64];
                 {
                     float lo[32], hi[32];
-                    tc_ld32(tS + col0, lo);
-                    tc_ld32(tS + col0 + 32, hi);
+                    tc_ld32(tS + b * 64, lo);
+                    tc_ld32(tS + b * 64 + 32, hi);
                     tc_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -344,9 +318,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 if (masked) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) v[i] = key0 + i <= pos[T] ? v[i] : -INFINITY;
+                    for (int i = 0; i < 64; ++i) v[i] = key0 + i <= pos ? v[i] : -INFINITY;
                 }
-                // row max of this half: four independent chains of 3-input maxima
+                // row max of the block: four independent chains of 3-input maxima
                 float mq[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -355,42 +329,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int i = 3; i < 15; i += 2) mq[q] = fmax3(mq[q], v[16 * q + i], v[16 * q + i + 1]);
                     mq[q] = fmaxf(mq[q], v[16 * q + 15]);
                 }
-                float mx = fmaxf(fmax3(mq[0], mq[1], mq[2]), mq[3]);
-                // combine the two halves of the row (scale > 0 keeps the
-                // order); past this barrier both halves have S in registers,
-                // so P may overwrite it
-                half_max[half][row] = mx;
-                tc_fence_before();
-                softmax_bar();
-                tc_fence_after();
-                mx = fmaxf(mx, half_max[half ^ 1][row]);
-                const float mxs = mx * scale;
-                // move the reference max only when the row max outgrew it;
-                // O holds PV(kb - 1) here: S(kb) was computed after it
+                const float mxs = fmaxf(fmax3(mq[0], mq[1], mq[2]), mq[3]) * scale;  // scale > 0 keeps the order
+                // move the reference max only when the row max outgrew it
                 bool rescale = false;
                 float alpha = 1.f;
-                if (mxs > m_ref[T] + kTcRescaleThreshold) {
-                    alpha = fast_exp2(m_ref[T] - mxs);  // 0 when m_ref = -inf
-                    m_ref[T] = mxs;
-                    l_run[T] *= alpha;
+                if (mxs > m_ref + kTcRescaleThreshold) {
+                    alpha = fast_exp2(m_ref - mxs);  // 0 when m_ref = -inf
+                    m_ref = mxs;
+                    l_run *= alpha;
                     rescale = kb > 0;
                 }
                 if (__any_sync(0xffffffffu, rescale)) {
-                    float o0[32], o1[32];
-                    tc_ld32(tO, o0);
-                    tc_ld32(tO + 32, o1);
-                    tc_wait_ld();
+                    // O must hold PV(kb - 1) before it is scaled (PV(kb - 2)
+                    // finished before S(kb) was computed)
+                    ok = ok && mbar_wait_bounded(smem_addr(&pv_done[T]), (kb - 1) & 1, kTcWaitNs);
+                    tc_fence_after();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        o0[i] *= alpha;
-                        o1[i] *= alpha;
+                    for (int c = 0; c < 128; c += 32) {
+                        float o[32];
+                        tc_ld32(tO + c, o);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tc_st32(tO + c, o);
                     }
-                    tc_st32(tO, o0);
-                    tc_st32(tO + 32, o1);
                     tc_wait_st();
                 }
-                // P = exp2(scale * s - m_ref) (bf16)
-                const float neg = m_ref[T] == -INFINITY ? 0.f : -m_ref[T];
+                // P = exp2(scale * s - m_ref) (bf16), over the first half of S(kb)
+                const float neg = m_ref == -INFINITY ? 0.f : -m_ref;
                 float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int i = 0; i < 64; i += 2) {
@@ -402,67 +368,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 fadd2(sa[0], sb[0], sa[1], sb[1]);
                 fadd2(sa[2], sb[2], sa[3], sb[3]);
                 fadd2(sa[0], sb[0], sa[2], sb[2]);
-                l_run[T] += sa[0] + sb[0];
-                // both halves have read their partner's maximum: its slot is free
-                softmax_bar();
+                l_run += sa[0] + sb[0];
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) pk[i] = pack2<false>(v[2 * i], v[2 * i + 1]);
-                tc_st32(tS + half * 32, pk);
+                tc_st32(tS + b * 64, pk);
                 tc_wait_st();
-                if (kb == nkb_c - 1 && T == 0 && kend_c - kb * kTcKeys < kTcKeys) {
-                    // keys past the context in the last block may hold
-                    // anything: zero those V rows before the first PV reads
-                    // them (P is 0 there, but 0 x garbage could be NaN)
-                    const int vs = kb % kTcVStages;
-                    ok = ok && mbar_wait_bounded(smem_addr(&v_full[vs]), (kb / kTcVStages) & 1, kTcWaitNs);
-                    const int valid = kend_c - kb * kTcKeys;
-                    const uint32_t vbase = base + kTcVOff + vs * kTcTile;
-                    for (int r2 = valid + tid; r2 < kTcKeys; r2 += kTcSoftmaxThreads)
-                        for (int sl = 0; sl < 2; ++sl)
-                            for (int c16 = 0; c16 < 8; ++c16)
-                                st_shared_zero16(vbase + sl * kTcSlab + r2 * 128 + c16 * 16);
-                    fence_proxy_async_smem();
-                    softmax_bar();  // every softmax warp zeroed its rows
-                }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&p_full[T]));
+                if (lane == 0) mbar_arrive(smem_addr(&p_full[T][b]));
             }
-        }
-        // every PV is done once the MMA threads' final commits land
-        for (int T = 0; T < ntiles; ++T) ok = ok && mbar_wait_bounded(smem_addr(&drain[T]), 0, kTcWaitNs);
-        tc_fence_after();
-        if (!ok) fail();
+            // every PV is done once the tile's MMA thread's final commit lands
+            ok = ok && mbar_wait_bounded(smem_addr(&drain[T]), 0, kTcWaitNs);
+            tc_fence_after();
+            if (!ok) fail();
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            __nv_bfloat16 *dst = a.out + ((static_cast<int64_t>(q0) + tok_begin + t) * a.num_q_heads +
+                                          h * a.group + g) * 128;
 #pragma unroll
-        for (int T = 0; T < kTcTiles; ++T) {
-            if (T >= ntiles) continue;
-            half_max[half][row] = l_run[T];
-            softmax_bar();
-            const float l = half_max[0][row] + half_max[1][row];
-            softmax_bar();  // both read before the next tile's sums overwrite them
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const uint32_t tO = tmem + lane_addr + kTcOCol + T * 128 + col0;
-            float o0[32], o1[32];
-            tc_ld32(tO, o0);
-            tc_ld32(tO + 32, o1);
-            tc_wait_ld();
-            if (pos[T] >= 0 && !failed_s) {
-                __nv_bfloat16 *dst = a.out + ((static_cast<int64_t>(q0) + tok_begin[T] + t) * a.num_q_heads +
-                                              h * a.group + g) * 128 + col0;
+            for (int c = 0; c < 128; c += 32) {
+                float o[32];
+                tc_ld32(tO + c, o);
+                tc_wait_ld();
+                if (live && !failed_s) {
 #pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                    uint4 w0, w1;
-                    w0.x = pack2<false>(o0[i] * inv, o0[i + 1] * inv);
-                    w0.y = pack2<false>(o0[i + 2] * inv, o0[i + 3] * inv);
-                    w0.z = pack2<false>(o0[i + 4] * inv, o0[i + 5] * inv);
-                    w0.w = pack2<false>(o0[i + 6] * inv, o0[i + 7] * inv);
-                    w1.x = pack2<false>(o1[i] * inv, o1[i + 1] * inv);
-                    w1.y = pack2<false>(o1[i + 2] * inv, o1[i + 3] * inv);
-                    w1.z = pack2<false>(o1[i + 4] * inv, o1[i + 5] * inv);
-                    w1.w = pack2<false>(o1[i + 6] * inv, o1[i + 7] * inv);
-                    *reinterpret_cast<uint4 *>(dst + i) = w0;
-                    *reinterpret_cast<uint4 *>(dst + 32 + i) = w1;
+                    for (int i = 0; i < 32; i += 8) {
+                        uint4 w;
+                        w.x = pack2<false>(o[i] * inv, o[i + 1] * inv);
+                        w.y = pack2<false>(o[i + 2] * inv, o[i + 3] * inv);
+                        w.z = pack2<false>(o[i + 4] * inv, o[i + 5] * inv);
+                        w.w = pack2<false>(o[i + 6] * inv, o[i + 7] * inv);
+                        *reinterpret_cast<uint4 *>(dst + c + i) = w;
+                    }
                 }
             }
         }
