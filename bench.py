@@ -362,9 +362,12 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(wl, ps):
+def recorded_traffic(wl, ps, args):
     """DRAM bytes per decode launch from a committed ncu capture, if it was
-    taken on the current decode kernel source for this workload."""
+    taken on the current decode kernel source for this workload, page size,
+    partition size and KV type (bf16 records carry no type suffix)."""
+    if args.device_alloc:  # contexts grow during the run: no single figure applies
+        return None
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
     try:
         with open(path) as f:
@@ -372,6 +375,8 @@ def recorded_traffic(wl, ps):
     except (OSError, ValueError):
         return None
     key = f"{wl.name}/B{wl.shape.block_size}/P{ps}"
+    if wl.shape.kv_dtype != W.KV_BF16:
+        key += "/e4m3"
     entry = rec.get(key)
     if not entry or entry.get("source_digest") != source_digest():
         return None
@@ -531,7 +536,7 @@ def run_ours(args):
     if args.device_alloc:  # the kernel-only launches ran at the final contexts
         kv_launch = kv0 + per_token * sh.num_seqs * calls[0]
     achieved = kv_launch / (dec_ms / 1e3) / 1e9
-    traffic = recorded_traffic(wl, ps)
+    traffic = recorded_traffic(wl, ps, args)
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
