@@ -77,6 +77,9 @@ def parse():
                     help="attention layers per step, each with its own KV cache")
     ap.add_argument("--per-head-scales", action="store_true",
                     help="E4M3 cache with its own K and V scale per KV head")
+    ap.add_argument("--fp8-qk", action="store_true",
+                    help="E4M3 cache and E4M3 x E4M3 scores: the query is rounded to E4M3 with "
+                         "q_scale = amax |q| / 448 (pa_decode_step_fp8_qk)")
     ap.add_argument("--device-alloc", action="store_true",
                     help="each step first advances every context by one token and allocates "
                          "blocks on the device (pa_block_alloc), then runs the step")
@@ -244,6 +247,8 @@ def config_of(wl, ps, args):
         "kv_dtype": "bf16" if sh.kv_dtype == W.KV_BF16 else
                     ("fp8_e4m3, K and V scale per KV head" if args.per_head_scales else
                      "fp8_e4m3, one scale"),
+        "scores": "E4M3 x E4M3 (query rounded to E4M3, q_scale = amax|q|/448)" if args.fp8_qk else
+                  "query at full precision",
         "mean_context": float(np.mean(wl.context_lens)), "num_blocks": wl.num_blocks,
         "kv_bytes_per_step": wl.kv_bytes(), "unique_kv_bytes_per_step": wl.unique_kv_bytes(),
         "seed": wl.seed, "parallelism": "replicas", "layers": args.layers,
@@ -418,9 +423,14 @@ def run_ours(args):
             quantize_fp8_pool(api, lw)
         lbt = torch.from_numpy(lw.block_tables).to(device)
         lcl = torch.from_numpy(lw.context_lens).to(device)
+        qs = None
+        if args.fp8_qk:
+            if lw.shape.kv_dtype != W.KV_FP8_E4M3:
+                raise SystemExit("--fp8-qk needs an E4M3 cache (--fp8 or prefix_fp8)")
+            qs = float(lw.q.float().abs().max().item()) / 448.0
         steps.append(api.DecodeStep(lw.k_cache, lw.v_cache, lbt, lcl, lw.shape.num_q_heads,
                                     lw.softmax_scale, lw.kv_scale, ps, fused=not args.separate,
-                                    k_scales=ks, v_scales=vs))
+                                    k_scales=ks, v_scales=vs, q_scale=qs))
         inputs.append((lw.q, lw.k_new, lw.v_new))
     sh = wl.shape
     step = steps[0]
@@ -542,7 +552,8 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if
-        sh.kv_dtype == W.KV_BF16 else "fp8_e4m3 KV, bf16 q/out, fp32 accumulate",
+        sh.kv_dtype == W.KV_BF16 else ("fp8_e4m3 KV and E4M3 x E4M3 scores, bf16 q/out, fp32 accumulate"
+                                       if args.fp8_qk else "fp8_e4m3 KV, bf16 q/out, fp32 accumulate"),
         "data": "synthetic (seeded N(0,1) bf16, shuffled block tables)",
         "config": config_of(wl, ps, args),
         "tokens_per_s": round(world * sh.num_seqs * K / (total_ms / 1e3), 1),

@@ -282,6 +282,27 @@ pa_status pa_block_alloc(int32_t *block_tables, int max_blocks_per_seq, int32_t 
                          int32_t *cow_src, cudaStream_t stream);
 
 /*
+ * pa_decode_step_fp8_qk -- pa_decode_step_scaled with the scores taken as an
+ * E4M3 x E4M3 tensor-core product (the first ranked variant of the FP8 KV
+ * cache; the tuning guide's Step 3 quantises only the cache, so this is an
+ * opt-in change to what is computed).  Every query element is first rounded
+ * exactly as the cache's values are: q8 = e4m3_rn_satfinite((float)q / q_scale),
+ * and the scores are softmax_scale * q_scale * k_scales[h] * sum_d
+ * e4m3(q8[d]) * e4m3(k[t][d]); the softmax, PV and output are as in
+ * pa_decode_step_scaled.  q_scale: a HOST float, positive and finite
+ * (PA_ERR_INVALID_ARG otherwise); queries with |q| / q_scale above 448
+ * saturate.  Other arguments and layouts as pa_decode_step_scaled.
+ */
+pa_status pa_decode_step_fp8_qk(const void *q, const void *k_new, const void *v_new,
+                                void *k_cache, void *v_cache, const int32_t *block_tables,
+                                int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+                                int block_size, const float *k_scales, const float *v_scales,
+                                float q_scale, float softmax_scale, int partition_size,
+                                void *workspace, size_t workspace_bytes, int32_t *slot_mapping,
+                                void *out, cudaStream_t stream);
+
+/*
  * pa_chunk_slot_mapping / pa_prefill -- chunked prefill over the paged cache.
  * Chunked prefill is named in the first page's "Production Checklist" and in
  * Step 2 of the tuning guide; the attention walks the block table as the

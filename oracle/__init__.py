@@ -61,6 +61,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.pa_oracle_cache_append_scaled.argtypes = [P, P, P, I, P, P, I, I, I, P, P]
     lib.pa_oracle_decode_scaled.restype = None
     lib.pa_oracle_decode_scaled.argtypes = [P, P, P, P, I, P, I, I, I, I, I, D, P, P, P, I, P]
+    lib.pa_oracle_decode_fp8_qk.restype = None
+    lib.pa_oracle_decode_fp8_qk.argtypes = [P, P, P, P, I, P, I, I, I, I, I, D, ctypes.c_float, P, P, P,
+                                            I, P]
     lib.pa_oracle_block_alloc.restype = I
     lib.pa_oracle_block_alloc.argtypes = [P, I, P, I, I, P, P, P, I, P, P, I, I, I, P]
     lib.pa_oracle_chunk_slot_mapping.restype = None
@@ -232,6 +235,32 @@ class Oracle:
         self.lib.pa_oracle_decode_scaled(_p(q), _p(kc), _p(vc), _p(bt), bt.shape[1], _p(cl), S, Hq,
                                          num_kv_heads, D, block_size, float(softmax_scale), _p(ks),
                                          _p(vs), _p(pr), pr.shape[0], _p(out))
+        return out
+
+    def decode_fp8_qk(self, q_bits, k_cache, v_cache, block_tables, context_lens, num_kv_heads,
+                      block_size, softmax_scale, q_scale, k_scales, v_scales, pairs=None) -> np.ndarray:
+        """As decode_scaled, with every query element first rounded to E4M3
+        (e4m3(float(q) / q_scale), read back times q_scale)."""
+        q = _c(q_bits, np.uint16)
+        bt = _c(block_tables, np.int32)
+        cl = _c(context_lens, np.int32)
+        kc = np.ascontiguousarray(k_cache, dtype=np.uint8)
+        vc = np.ascontiguousarray(v_cache, dtype=np.uint8)
+        ks = _c(k_scales, np.float32)
+        vs = _c(v_scales, np.float32)
+        S, Hq, D = q.shape
+        if pairs is None:
+            pr, n = None, S * Hq
+            out = np.zeros((S, Hq, D), np.float64)
+        else:
+            pr = _c(pairs, np.int32).reshape(-1, 2)
+            n = pr.shape[0]
+            out = np.zeros((n, D), np.float64)
+        self.lib.pa_oracle_decode_fp8_qk(_p(q), _p(kc), _p(vc), _p(bt), bt.shape[1], _p(cl), S, Hq,
+                                         num_kv_heads, D, block_size, float(softmax_scale),
+                                         float(q_scale), _p(ks), _p(vs),
+                                         _p(pr) if pr is not None else None, n if pr is not None else 0,
+                                         _p(out))
         return out
 
     # -- chunked prefill ------------------------------------------------------

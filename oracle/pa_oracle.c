@@ -449,6 +449,49 @@ void pa_oracle_decode_scaled(const uint16_t *q, const uint8_t *k_cache, const ui
     }
 }
 
+/* Decode attention whose scores take the query rounded to E4M3 the way the
+ * cache's values are (the first ranked variant of the FP8 KV cache, beyond
+ * the tuning guide's Step 3, which quantises only the cache): every query
+ * element becomes e4m3(float(q) / q_scale) and is read back as
+ * e4m3(code) * q_scale.  An E4M3 value is exact in bf16, so the rounded row
+ * is passed on as bf16 bits of e4m3(code) with q_scale folded into the
+ * softmax scale.  Cache scales per KV head as pa_oracle_decode_scaled. */
+void pa_oracle_decode_fp8_qk(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                             const int32_t *block_tables, int max_blocks_per_seq,
+                             const int32_t *context_lens, int num_seqs, int num_q_heads,
+                             int num_kv_heads, int head_dim, int block_size,
+                             double softmax_scale, float q_scale, const float *k_scales,
+                             const float *v_scales, const int32_t *pairs, int n_pairs,
+                             double *out)
+{
+    int group = num_q_heads / num_kv_heads;
+    int n = pairs ? n_pairs : num_seqs * num_q_heads;
+#pragma omp parallel for schedule(dynamic)
+    for (int i = 0; i < n; ++i) {
+        int s = pairs ? pairs[2 * i] : i / num_q_heads;
+        int hq = pairs ? pairs[2 * i + 1] : i % num_q_heads;
+        int kvh = hq / group;
+        int len = context_lens[s];
+        const uint16_t *q_row = q + ((int64_t)s * num_q_heads + hq) * head_dim;
+        uint16_t *q8 = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)head_dim);
+        for (int d = 0; d < head_dim; ++d) {
+            float x = (float)pa_oracle_bf16_to_double(q_row[d]);
+            float r = (float)pa_oracle_e4m3_to_double(pa_oracle_e4m3_from_float(x / q_scale));
+            uint32_t bits;
+            memcpy(&bits, &r, sizeof bits);
+            q8[d] = (uint16_t)(bits >> 16); /* exact: an E4M3 value has 3 fraction bits */
+        }
+        double *x = (double *)malloc(sizeof(double) * (size_t)(len > 0 ? len : 1));
+        double m, l;
+        attend_range(q8, k_cache, v_cache, block_tables, max_blocks_per_seq, s, kvh, 0, len,
+                     num_kv_heads, head_dim, block_size, softmax_scale * (double)q_scale, 1,
+                     (double)k_scales[kvh], (double)v_scales[kvh], x, out + (int64_t)i * head_dim,
+                     &m, &l);
+        free(x);
+        free(q8);
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* chunked prefill: many new tokens per sequence                             */
 /* ------------------------------------------------------------------------ */

@@ -211,9 +211,11 @@ def cache_append_scaled(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Te
 
 def decode_step_scaled(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, k_scales,
                        v_scales, softmax_scale=None, partition_size=0, workspace=None,
-                       slot_mapping=None, out=None, stream=None) -> torch.Tensor:
+                       slot_mapping=None, out=None, stream=None, q_scale=None) -> torch.Tensor:
     """Fused decode step over an E4M3 cache with per-KV-head K and V scales.
-    ``k_new``/``v_new`` may both be None: attention without an append."""
+    ``k_new``/``v_new`` may both be None: attention without an append.
+    ``q_scale`` (a positive float) rounds the query to E4M3 with that scale
+    and takes the scores as an E4M3 x E4M3 product (pa_decode_step_fp8_qk)."""
     kv_dtype, S, Hq, D, NB, Hkv, B = _decode_common(q, k_cache, v_cache, block_tables, context_lens)
     if kv_dtype != PA_KV_FP8_E4M3:
         raise TypeError("per-head scales need an E4M3 cache")
@@ -230,13 +232,17 @@ def decode_step_scaled(q, k_new, v_new, k_cache, v_cache, block_tables, context_
         workspace = alloc_workspace(q, block_tables, B, partition_size)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(_lib_handle().pa_decode_step_scaled(
-        q.data_ptr(), k_new.data_ptr() if k_new is not None else None,
-        v_new.data_ptr() if v_new is not None else None, k_cache.data_ptr(), v_cache.data_ptr(),
-        block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), S, Hq, Hkv, D, NB,
-        B, k_scales.data_ptr(), v_scales.data_ptr(), float(softmax_scale), int(partition_size),
-        ws_ptr, ws_bytes, slot_mapping.data_ptr() if slot_mapping is not None else None,
-        out.data_ptr(), _stream(stream)))
+    lead = (q.data_ptr(), k_new.data_ptr() if k_new is not None else None,
+            v_new.data_ptr() if v_new is not None else None, k_cache.data_ptr(), v_cache.data_ptr(),
+            block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), S, Hq, Hkv, D,
+            NB, B, k_scales.data_ptr(), v_scales.data_ptr())
+    tail = (float(softmax_scale), int(partition_size), ws_ptr, ws_bytes,
+            slot_mapping.data_ptr() if slot_mapping is not None else None, out.data_ptr(),
+            _stream(stream))
+    if q_scale is None:
+        _check(_lib_handle().pa_decode_step_scaled(*lead, *tail))
+    else:
+        _check(_lib_handle().pa_decode_step_fp8_qk(*lead, float(q_scale), *tail))
     return out
 
 
@@ -369,8 +375,15 @@ class DecodeStep:
 
     def __init__(self, k_cache, v_cache, block_tables, context_lens, num_q_heads,
                  softmax_scale=None, kv_scale=1.0, partition_size=0, fused=True,
-                 k_scales=None, v_scales=None):
+                 k_scales=None, v_scales=None, q_scale=None):
         self.fused = fused
+        # q_scale: E4M3 query and E4M3 x E4M3 scores (pa_decode_step_fp8_qk);
+        # with one cache scale, every head gets it
+        self.q_scale = q_scale
+        if q_scale is not None and k_scales is None:
+            k_scales = torch.full((k_cache.shape[1],), float(kv_scale), dtype=torch.float32,
+                                  device=k_cache.device)
+            v_scales = k_scales
         # per-KV-head E4M3 scales (device float32 [Hkv]); fused path only
         self.k_scales, self.v_scales = k_scales, v_scales
         if k_scales is not None and not fused:
@@ -415,7 +428,8 @@ class DecodeStep:
             return decode_step_scaled(q, k_new, v_new, self.k_cache, self.v_cache,
                                       self.block_tables, self.context_lens, self.k_scales,
                                       self.v_scales, self.softmax_scale, self.partition_size,
-                                      self.workspace, self.slots, self.out, stream)
+                                      self.workspace, self.slots, self.out, stream,
+                                      q_scale=self.q_scale)
         if self.fused:
             return decode_step(q, k_new, v_new, self.k_cache, self.v_cache, self.block_tables,
                                self.context_lens, self.softmax_scale, self.kv_scale,

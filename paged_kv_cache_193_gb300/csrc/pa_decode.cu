@@ -69,6 +69,7 @@ struct DecodeArgs {
     const float *k_scales;
     const float *v_scales;
     float softmax_log2;  // softmax_scale * log2(e)
+    float q_scale;       // E4M3 query scale of the E4M3 x E4M3 score product
 };
 
 // Give up on a page copy after this long (normal waits are microseconds).
@@ -110,10 +111,14 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int t, int b) {
     return base + slab * (BS * C::SLAB) + t * C::SLAB + (phys << 4) + (within & 15);
 }
 
-template <int D, int BS, bool FP8, int NT, int NW, int SPW>
+// FQ (E4M3 cache only): the query is rounded to E4M3 (x / q_scale) and the
+// scores are an E4M3 x E4M3 tensor-core product over the cache bytes as
+// they lie in shared memory.
+template <int D, int BS, bool FP8, int NT, int NW, int SPW, bool FQ = false>
 __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeArgs a) {
+    static_assert(!FQ || FP8, "the E4M3 score product needs the E4M3 cache");
     using C = Cfg<D, BS, FP8, NT, NW, SPW>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[C::NSTAGE];
@@ -135,6 +140,7 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
         score_scale = a.softmax_log2 * append_k_scale;
         v_scale = append_v_scale;
     }
+    if constexpr (FQ) score_scale *= a.q_scale;
 
     // let a dependent merge kernel launch now; it waits for our results
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -163,7 +169,7 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
                     // logical k = 2c, 2c+1 and 2c+8, 2c+9 of this 16-dim step
                     qf[kk][nt][0] = live ? __ldg(reinterpret_cast<const uint32_t *>(qg + kk * 16 + 2 * c)) : 0u;
                     qf[kk][nt][1] = live ? __ldg(reinterpret_cast<const uint32_t *>(qg + kk * 16 + 8 + 2 * c)) : 0u;
-                } else {
+                } else if constexpr (!FQ) {
                     // permuted order: this thread's dims are c*16*CPT + 4*kk + {0,1,2,3}
                     uint2 w = live ? __ldg(reinterpret_cast<const uint2 *>(qg + c * 16 * C::CPT + 4 * kk))
                                    : make_uint2(0u, 0u);
@@ -171,6 +177,15 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
                     float2 f1 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w.y));
                     qf[kk][nt][0] = pack2<true>(f0.x, f0.y);
                     qf[kk][nt][1] = pack2<true>(f1.x, f1.y);
+                } else if (kk < C::KSTEPS / 2) {
+                    // E4M3 codes; permuted order: 32-dim step kk takes this
+                    // thread's dims c*16*CPT + 8*kk + {0..3} (logical k = 4c + i)
+                    // and + {4..7} (logical k = 16 + 4c + i), as the K bytes below
+                    const uint4 w = live ? __ldg(reinterpret_cast<const uint4 *>(qg + c * 16 * C::CPT + 8 * kk))
+                                         : make_uint4(0u, 0u, 0u, 0u);
+                    const uint2 q8 = quantize8_e4m3(w, a.q_scale);
+                    qf[kk][nt][0] = q8.x;
+                    qf[kk][nt][1] = q8.y;
                 }
             }
         }
@@ -334,6 +349,29 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
                         mma16816<false>(sc[mt][nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
+                }
+            }
+        } else if constexpr (FQ) {
+            // E4M3 x E4M3: this thread's 8 bytes of a row per 32-dim step are
+            // A fragment words as they lie in shared memory
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                const int t0 = mt * 16 + r, t1 = t0 + 8;
+                uint4 ra[C::CPT], rb[C::CPT];
+#pragma unroll
+                for (int j = 0; j < C::CPT; ++j) {
+                    ra[j] = lds128(swz<C, BS>(kbase, t0, (c * C::CPT + j) * 16));
+                    rb[j] = lds128(swz<C, BS>(kbase, t1, (c * C::CPT + j) * 16));
+                }
+                auto word = [](const uint4 &u, int i) { return i == 0 ? u.x : i == 1 ? u.y : i == 2 ? u.z : u.w; };
+#pragma unroll
+                for (int kk = 0; kk < C::KSTEPS / 2; ++kk) {
+                    const int w = 2 * kk;
+                    const uint32_t a0 = word(ra[w / 4], w % 4), a2 = word(ra[w / 4], w % 4 + 1);
+                    const uint32_t a1 = word(rb[w / 4], w % 4), a3 = word(rb[w / 4], w % 4 + 1);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma16832_e4m3(sc[mt][nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
                 }
             }
         } else {
@@ -619,12 +657,12 @@ constexpr int stages_per_warp() {
     return spw < 1 ? 1 : spw;
 }
 
-template <int D, int BS, bool FP8, int NT>
+template <int D, int BS, bool FP8, int NT, bool FQ>
 static pa_status launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
                                dim3 grid, cudaStream_t stream) {
     constexpr int SPW = stages_per_warp<D, BS, FP8>();
     using C = Cfg<D, BS, FP8, NT, kWarps, SPW>;
-    auto kern = decode_kernel<D, BS, FP8, NT, kWarps, SPW>;
+    auto kern = decode_kernel<D, BS, FP8, NT, kWarps, SPW, FQ>;
     // Raise the kernel's shared-memory limit once per device (the first call
     // on a device should precede any stream capture).
     static std::atomic<uint64_t> raised{0};
@@ -642,18 +680,19 @@ static pa_status launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, con
     return cuda_check(cudaGetLastError(), "decode launch");
 }
 
-template <int D, int BS, bool FP8>
+template <int D, int BS, bool FP8, bool FQ>
 static pa_status launch_nt(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
                            dim3 grid, cudaStream_t stream) {
-    if (a.group <= 8) return launch_decode<D, BS, FP8, 1>(tk, tv, a, grid, stream);
-    return launch_decode<D, BS, FP8, 2>(tk, tv, a, grid, stream);
+    if (a.group <= 8) return launch_decode<D, BS, FP8, 1, FQ>(tk, tv, a, grid, stream);
+    return launch_decode<D, BS, FP8, 2, FQ>(tk, tv, a, grid, stream);
 }
 
 template <int D, int BS>
 static pa_status launch_dtype(bool fp8, const CUtensorMap &tk, const CUtensorMap &tv,
                               const DecodeArgs &a, dim3 grid, cudaStream_t stream) {
-    if (fp8) return launch_nt<D, BS, true>(tk, tv, a, grid, stream);
-    return launch_nt<D, BS, false>(tk, tv, a, grid, stream);
+    if (fp8 && a.q_scale > 0.f) return launch_nt<D, BS, true, true>(tk, tv, a, grid, stream);
+    if (fp8) return launch_nt<D, BS, true, false>(tk, tv, a, grid, stream);
+    return launch_nt<D, BS, false, false>(tk, tv, a, grid, stream);
 }
 
 struct DecodeShape {
@@ -715,6 +754,7 @@ struct StepAppend {
     int32_t *slot_out;
     const float *k_scales;  // optional per-KV-head E4M3 scales
     const float *v_scales;
+    float q_scale;          // > 0: E4M3 query and E4M3 x E4M3 scores
 };
 
 // Launch the per-partition (split) or whole-context (unsplit) kernel.
@@ -765,6 +805,7 @@ static pa_status run_decode(const void *q, const void *k_cache, const void *v_ca
     a.k_scales = app ? app->k_scales : nullptr;
     a.v_scales = app ? app->v_scales : nullptr;
     a.softmax_log2 = softmax_scale * 1.4426950408889634f;
+    a.q_scale = app ? app->q_scale : 0.f;
 
     if (parts > 0x7fffffffLL) return fail(PA_ERR_UNSUPPORTED, "too many partitions");
     dim3 grid(static_cast<unsigned>(split ? parts : 1), sh.num_kv_heads, sh.num_seqs);
@@ -924,15 +965,17 @@ pa_status pa_decode_step(const void *q, const void *k_new, const void *v_new, vo
                          static_cast<int>(parts), out, stream);
 }
 
-pa_status pa_decode_step_scaled(const void *q, const void *k_new, const void *v_new,
-                                void *k_cache, void *v_cache, const int32_t *block_tables,
-                                int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
-                                int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
-                                int block_size, const float *k_scales, const float *v_scales,
-                                float softmax_scale, int partition_size, void *workspace,
-                                size_t workspace_bytes, int32_t *slot_mapping, void *out,
-                                cudaStream_t stream) {
-    clear_error();
+}  // extern "C"
+
+// The per-head-scaled E4M3 step; q_scale > 0 selects the E4M3 x E4M3 scores.
+static pa_status step_scaled(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                             void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                             const int32_t *context_lens, int num_seqs, int num_q_heads,
+                             int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                             const float *k_scales, const float *v_scales, float q_scale,
+                             float softmax_scale, int partition_size, void *workspace,
+                             size_t workspace_bytes, int32_t *slot_mapping, void *out,
+                             cudaStream_t stream) {
     DecodeShape sh{num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
                    max_blocks_per_seq, partition_size, PA_KV_FP8_E4M3};
     pa_status st = check_shape(sh, 1.f, softmax_scale);
@@ -946,7 +989,7 @@ pa_status pa_decode_step_scaled(const void *q, const void *k_new, const void *v_
     if (k_new && (!aligned16(k_new) || !aligned16(v_new)))
         return fail(PA_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
     if (!out || !aligned16(out)) return fail(PA_ERR_INVALID_ARG, "out must be non-null and 16-byte aligned");
-    StepAppend app{k_new, v_new, slot_mapping, k_scales, v_scales};
+    StepAppend app{k_new, v_new, slot_mapping, k_scales, v_scales, q_scale};
     if (partition_size == 0)
         return run_decode(q, k_cache, v_cache, block_tables, context_lens, sh, 1.f, softmax_scale,
                           nullptr, out, stream, &app);
@@ -960,6 +1003,40 @@ pa_status pa_decode_step_scaled(const void *q, const void *k_new, const void *v_
     if (st != PA_OK) return st;
     return launch_reduce(workspace, context_lens, num_seqs, num_q_heads, head_dim, partition_size,
                          static_cast<int>(parts), out, stream);
+}
+
+extern "C" {
+
+pa_status pa_decode_step_scaled(const void *q, const void *k_new, const void *v_new,
+                                void *k_cache, void *v_cache, const int32_t *block_tables,
+                                int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+                                int block_size, const float *k_scales, const float *v_scales,
+                                float softmax_scale, int partition_size, void *workspace,
+                                size_t workspace_bytes, int32_t *slot_mapping, void *out,
+                                cudaStream_t stream) {
+    clear_error();
+    return step_scaled(q, k_new, v_new, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                       block_size, k_scales, v_scales, 0.f, softmax_scale, partition_size, workspace,
+                       workspace_bytes, slot_mapping, out, stream);
+}
+
+pa_status pa_decode_step_fp8_qk(const void *q, const void *k_new, const void *v_new,
+                                void *k_cache, void *v_cache, const int32_t *block_tables,
+                                int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+                                int block_size, const float *k_scales, const float *v_scales,
+                                float q_scale, float softmax_scale, int partition_size,
+                                void *workspace, size_t workspace_bytes, int32_t *slot_mapping,
+                                void *out, cudaStream_t stream) {
+    clear_error();
+    if (!(q_scale > 0.f) || !isfinite(q_scale))
+        return fail(PA_ERR_INVALID_ARG, "q_scale %g must be positive and finite", static_cast<double>(q_scale));
+    return step_scaled(q, k_new, v_new, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                       block_size, k_scales, v_scales, q_scale, softmax_scale, partition_size,
+                       workspace, workspace_bytes, slot_mapping, out, stream);
 }
 
 }  // extern "C"

@@ -192,6 +192,16 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
     }
 }
 
+// D += A * B, m16n8k32, both operands E4M3 (four per register, lowest k in
+// the lowest byte), fp32 accumulate.
+__device__ __forceinline__ void mma16832_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Four E4M3 bytes b0..b3 of a word (b0 lowest) -> two fp16x2 registers:
 // lo = {b0, b1}, hi = {b2, b3}, low half first.  Exact (every E4M3 value is
 // an fp16 value).  The conversion reads the two 16-bit halves of the word

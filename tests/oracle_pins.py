@@ -429,7 +429,66 @@ def pin_prefill(o):
         assert np.array_equal(slots[last], o.slot_mapping(tables, np.array(ctx), B))
 
 
+def pin_fp8_qk(o):
+    """E4M3 x E4M3 scores: the oracle equals torch SDPA over a query rounded
+    by torch's float8_e4m3fn (x / q_scale, read back times q_scale) and an
+    E4M3 cache decoded with each head's scales; a query already on the E4M3
+    grid with q_scale 1 gives the per-head-scaled decode unchanged; a query
+    element past the E4M3 range counts as +-448 q_scale."""
+    rng = np.random.default_rng(16)
+    c = _case(Hq=12, Hkv=3, seed=43)
+    B = 16
+    tables, _, _ = c.paged(B, 30, rng)
+    ks = np.array([0.012, 0.021, 0.009], np.float32)
+    vs = np.array([0.017, 0.006, 0.029], np.float32)
+    kc = np.full((30, c.Hkv, B, c.D), 0x7F, np.uint8)
+    vc = np.full_like(kc, 0x7F)
+    for s_, n in enumerate(c.ctx):
+        slots = np.array([tables[s_, t // B] * B + t % B for t in range(n)], np.int32)
+        o.cache_append_scaled(c.k[s_].transpose(1, 0, 2), c.v[s_].transpose(1, 0, 2), slots,
+                              kc, vc, B, ks, vs)
+    ctx = np.array(c.ctx)
+    qs = 0.0173  # N(0,1) queries stay far inside +-448 qs
+    out = o.decode_fp8_qk(c.q, kc, vc, tables, ctx, c.Hkv, B, 0.21, qs, ks, vs)
+    codes_k, codes_v = [], []
+    for s_, n in enumerate(c.ctx):
+        ck = np.zeros((c.Hkv, n, c.D), np.uint8)
+        cv = np.zeros_like(ck)
+        for t in range(n):
+            ck[:, t] = kc[tables[s_, t // B], :, t % B]
+            cv[:, t] = vc[tables[s_, t // B], :, t % B]
+        codes_k.append(ck)
+        codes_v.append(cv)
+    plain = o.decode_scaled(c.q, kc, vc, tables, ctx, c.Hkv, B, 0.21, ks, vs)
+
+    def round_q(bits):
+        x = torch.from_numpy(bits_to_f64(bits).astype(np.float32) / np.float32(qs))
+        return x.to(torch.float8_e4m3fn).to(torch.float64).numpy() * np.float64(np.float32(qs))
+
+    logical = LogicalCase(c.ctx, c.Hq, c.Hkv, c.D, 43)
+    logical.k, logical.v = codes_k, codes_v
+    ref = logical.sdpa(0.21, deq_q=round_q,
+                       deq_k=lambda a: _e4m3_torch(a) * ks[:, None, None].astype(np.float64),
+                       deq_v=lambda a: _e4m3_torch(a) * vs[:, None, None].astype(np.float64))
+    assert np.abs(out - ref).max() < 1e-12, np.abs(out - ref).max()
+    assert np.abs(out - plain).max() > 1e-6  # the rounding of the query is visible
+    # a query already on the E4M3 grid, q_scale 1: nothing changes
+    grid = _e4m3_torch(rng.integers(0, 0x7F, size=c.q.shape).astype(np.uint8))
+    grid *= np.where(rng.random(c.q.shape) < 0.5, -1.0, 1.0)
+    qg = (torch.from_numpy(grid).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    a1 = o.decode_fp8_qk(qg, kc, vc, tables, ctx, c.Hkv, B, 0.21, 1.0, ks, vs)
+    a2 = o.decode_scaled(qg, kc, vc, tables, ctx, c.Hkv, B, 0.21, ks, vs)
+    assert np.array_equal(a1, a2)
+    # saturation: 1000 becomes 448 (q_scale 1)
+    big, sat = qg.copy(), qg.copy()
+    big[:, :, 3] = 0x447A  # bf16 1000.0
+    sat[:, :, 3] = 0x43E0  # bf16 448.0
+    b1 = o.decode_fp8_qk(big, kc, vc, tables, ctx, c.Hkv, B, 0.21, 1.0, ks, vs)
+    b2 = o.decode_scaled(sat, kc, vc, tables, ctx, c.Hkv, B, 0.21, ks, vs)
+    assert np.array_equal(b1, b2)
+
+
 ALL = [pin_kv_formula, pin_e4m3_decode, pin_e4m3_encode, pin_e4m3_roundtrip, pin_attention_sdpa,
        pin_attention_fp8, pin_extreme_scores, pin_permutation, pin_prefix_sharing, pin_context_one,
        pin_identical_keys, pin_empty_context, pin_slot_mapping, pin_append_readback,
-       pin_partition_merge, pin_fp8_per_head_scales, pin_block_alloc, pin_prefill]
+       pin_partition_merge, pin_fp8_per_head_scales, pin_block_alloc, pin_prefill, pin_fp8_qk]

@@ -59,7 +59,7 @@ class LogicalCase:
                 vc[b, :, t % B, :] = self.v[s][:, t, :]
         return tables, kc, vc
 
-    def sdpa(self, softmax_scale, deq_k=None, deq_v=None) -> np.ndarray:
+    def sdpa(self, softmax_scale, deq_k=None, deq_v=None, deq_q=None) -> np.ndarray:
         """torch scaled_dot_product_attention in float64 over the logical K/V,
         each KV head repeated for its G query heads (grouped-query attention)."""
         G = self.Hq // self.Hkv
@@ -67,7 +67,7 @@ class LogicalCase:
         for s, c in enumerate(self.ctx):
             if c == 0:
                 continue
-            q = torch.from_numpy(bits_to_f64(self.q[s]))[None, :, None, :]
+            q = torch.from_numpy(deq_q(self.q[s]) if deq_q else bits_to_f64(self.q[s]))[None, :, None, :]
             k = torch.from_numpy(deq_k(self.k[s]) if deq_k else bits_to_f64(self.k[s]))
             v = torch.from_numpy(deq_v(self.v[s]) if deq_v else bits_to_f64(self.v[s]))
             k = k.repeat_interleave(G, dim=0)[None]

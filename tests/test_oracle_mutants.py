@@ -31,6 +31,9 @@ MUTANTS = {
                           "(double)v_scales[kvh], (double)k_scales[kvh]"),
     "scaled_head_ignored": ("k_cache[dst] = pa_oracle_e4m3_from_float(kf / k_scales[h]);",
                             "k_cache[dst] = pa_oracle_e4m3_from_float(kf / k_scales[0]);"),
+    "fp8qk_scale_dropped": ("softmax_scale * (double)q_scale, 1,", "softmax_scale, 1,"),
+    "fp8qk_query_not_rounded": ("float r = (float)pa_oracle_e4m3_to_double(pa_oracle_e4m3_from_float(x / q_scale));",
+                                "float r = x / q_scale;"),
     "alloc_copies_sole_owner": ("if (refcounts[cur] > 1)\n                action[s] = 2;",
                                 "if (refcounts[cur] > 0)\n                action[s] = 2;"),
     "alloc_copy_short": ("int rows = pos % block_size;", "int rows = pos % block_size - (pos % block_size > 0);"),
