@@ -86,7 +86,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int NPG = kTcKeys / BS;  // pages per key block
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t q_full, v_zeroed;
-    __shared__ __align__(8) uint64_t k_full[kTcStages], k_empty[kTcStages], v_full[kTcStages], v_empty[kTcStages];
+    // kv_full[st]: both the K and the V pages of the stage's block have landed
+    __shared__ __align__(8) uint64_t kv_full[kTcStages], k_empty[kTcStages], v_empty[kTcStages];
     __shared__ __align__(8) uint64_t s_full[kTcTiles][2], p_full[kTcTiles][2], pv_done[kTcTiles], drain[kTcTiles];
     __shared__ uint32_t tmem_base_s;
     __shared__ int failed_s;
@@ -120,9 +121,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(smem_addr(&q_full), 1);
         mbar_init(smem_addr(&v_zeroed), 1);
         for (int i = 0; i < kTcStages; ++i) {
-            mbar_init(smem_addr(&k_full[i]), 1);
+            mbar_init(smem_addr(&kv_full[i]), 2);  // the K loader and the V loader
             mbar_init(smem_addr(&k_empty[i]), ntiles);
-            mbar_init(smem_addr(&v_full[i]), 1);
             mbar_init(smem_addr(&v_empty[i]), ntiles);
         }
         for (int t = 0; t < kTcTiles; ++t) {
@@ -180,7 +180,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------- loads: warp 8 the queries and K, warp 10 V -------------
         const bool is_k = warp == kTcLoadWarp;
         const CUtensorMap *map = is_k ? &tmK : &tmV;
-        uint64_t *full = is_k ? k_full : v_full;
         uint64_t *empty = is_k ? k_empty : v_empty;
         const uint32_t ring = base + (is_k ? kTcKOff : kTcVOff);
         const uint64_t policy = l2_evict_first_policy();
@@ -199,13 +198,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (kb + 1 < nkb) e_next = page_entry(kb + 1);
             if (lane == 0) {
                 if (!mbar_wait_bounded(smem_addr(&empty[st]), ph ^ 1, kTcWaitNs)) fail();
-                mbar_arrive_expect_tx(smem_addr(&full[st]), kTcKVStage);
+                mbar_arrive_expect_tx(smem_addr(&kv_full[st]), kTcKVStage);
             }
             __syncwarp();
             if (lane < NPG) {
                 for (int sl = 0; sl < 2; ++sl)
                     tma_load_2d(ring + st * kTcKVStage + sl * kTcKVSlab + lane * BS * 128, map, sl * 64, y,
-                                smem_addr(&full[st]), policy);
+                                smem_addr(&kv_full[st]), policy);
             }
         }
         if (!is_k && partial) {
@@ -213,7 +212,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // zero those V rows before a PV reads them (P is 0 there, but
             // 0 x garbage could be NaN)
             const int kb = nkb - 1, st = kb % kTcStages;
-            if (lane == 0 && !mbar_wait_bounded(smem_addr(&v_full[st]), (kb / kTcStages) & 1, kTcWaitNs)) fail();
+            if (lane == 0 && !mbar_wait_bounded(smem_addr(&kv_full[st]), (kb / kTcStages) & 1, kTcWaitNs)) fail();
             __syncwarp();
             const uint32_t vbase = base + kTcVOff + st * kTcKVStage;
             for (int r2 = kend - kb * kTcKeys + lane; r2 < kTcKeys; r2 += 32)
@@ -242,7 +241,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, kTcWaitNs);
             auto qk = [&](int kb) {  // S(kb) = Q K(kb)^T
                 const int ks = kb % kTcStages, b = kb & 1;
-                ok = ok && mbar_wait_bounded(smem_addr(&k_full[ks]), (kb / kTcStages) & 1, kTcWaitNs);
+                // K and V of the block: V(kb) is in place for PV(kb) too
+                ok = ok && mbar_wait_bounded(smem_addr(&kv_full[ks]), (kb / kTcStages) & 1, kTcWaitNs);
                 // S(kb)'s columns held P(kb - 2): PV(kb - 2) must have read them
                 if (kb >= 2) ok = ok && mbar_wait_bounded(smem_addr(&pv_done[T]), kb & 1, kTcWaitNs);
                 tc_fence_after();
@@ -263,7 +263,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int kb = 0; kb < nkb; ++kb) {
                 const int vs = kb % kTcStages, b = kb & 1;
                 ok = ok && mbar_wait_bounded(smem_addr(&p_full[T][b]), (kb >> 1) & 1, kTcWaitNs);
-                ok = ok && mbar_wait_bounded(smem_addr(&v_full[vs]), (kb / kTcStages) & 1, kTcWaitNs);
                 if (kb == nkb - 1 && partial) ok = ok && mbar_wait_bounded(smem_addr(&v_zeroed), 0, kTcWaitNs);
                 tc_fence_after();
                 if (ok) {  // O += P(kb) V(kb)
