@@ -82,12 +82,14 @@ constexpr uint64_t kTcWaitNs = 2000000000ull;
 template <int BS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const PrefillTcArgs a) {
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                      const PrefillTcArgs a) {
     constexpr int NPG = kTcKeys / BS;  // pages per key block
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t q_full, v_zeroed;
-    // kv_full[st]: both the K and the V pages of the stage's block have landed
-    __shared__ __align__(8) uint64_t kv_full[kTcStages], k_empty[kTcStages], v_empty[kTcStages];
+    // kv_full[st]: both the K and the V pages of the stage's block have landed;
+    // kv_empty[st]: every tile's PV of that block is done (its QK came before)
+    __shared__ __align__(8) uint64_t kv_full[kTcStages], kv_empty[kTcStages];
     __shared__ __align__(8) uint64_t s_full[kTcTiles][2], p_full[kTcTiles][2], pv_done[kTcTiles], drain[kTcTiles];
     __shared__ uint32_t tmem_base_s;
     __shared__ int failed_s;
@@ -122,8 +124,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(smem_addr(&v_zeroed), 1);
         for (int i = 0; i < kTcStages; ++i) {
             mbar_init(smem_addr(&kv_full[i]), 2);  // the K loader and the V loader
-            mbar_init(smem_addr(&k_empty[i]), ntiles);
-            mbar_init(smem_addr(&v_empty[i]), ntiles);
+            mbar_init(smem_addr(&kv_empty[i]), ntiles);
         }
         for (int t = 0; t < kTcTiles; ++t) {
             for (int b = 0; b < 2; ++b) {
@@ -138,6 +139,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prefetch_tensormap(&tmQ);
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
+        prefetch_tensormap(&tmO);
     }
     if (warp == kTcMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -180,7 +182,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------- loads: warp 8 the queries and K, warp 10 V -------------
         const bool is_k = warp == kTcLoadWarp;
         const CUtensorMap *map = is_k ? &tmK : &tmV;
-        uint64_t *empty = is_k ? k_empty : v_empty;
         const uint32_t ring = base + (is_k ? kTcKOff : kTcVOff);
         const uint64_t policy = l2_evict_first_policy();
         if (is_k && lane == 0) {
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int y = page_row(e_next);
             if (kb + 1 < nkb) e_next = page_entry(kb + 1);
             if (lane == 0) {
-                if (!mbar_wait_bounded(smem_addr(&empty[st]), ph ^ 1, kTcWaitNs)) fail();
+                if (!mbar_wait_bounded(smem_addr(&kv_empty[st]), ph ^ 1, kTcWaitNs)) fail();
                 mbar_arrive_expect_tx(smem_addr(&kv_full[st]), kTcKVStage);
             }
             __syncwarp();
@@ -256,7 +257,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
                 tc_commit(smem_addr(&s_full[T][b]));
-                tc_commit(smem_addr(&k_empty[ks]));
             };
             qk(0);
             if (nkb > 1) qk(1);
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                        kb > 0 || kk > 0);
                 }
                 tc_commit(smem_addr(&pv_done[T]));
-                tc_commit(smem_addr(&v_empty[vs]));
+                tc_commit(smem_addr(&kv_empty[vs]));
                 if (kb + 2 < nkb) qk(kb + 2);
             }
             if (!ok) fail();
@@ -382,6 +382,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_after();
             if (!ok) fail();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            // A tile wholly inside its chunk leaves through shared memory (its
+            // query tile's space, in the same swizzled layout) and two TMA
+            // stores; a tile at the chunk's end is written row by row, so no
+            // box reaches into the next sequence's rows.
+            const bool full_tile = tok_begin + a.tile_tokens <= chunk;
+            const uint32_t stage = base + kTcQOff + T * kTcQTile;
             __nv_bfloat16 *dst = a.out + ((static_cast<int64_t>(q0) + tok_begin + t) * a.num_q_heads +
                                           h * a.group + g) * 128;
 #pragma unroll
@@ -389,16 +395,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 float o[32];
                 tc_ld32(tO + c, o);
                 tc_wait_ld();
-                if (live && !failed_s) {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 8) {
-                        uint4 w;
-                        w.x = pack2<false>(o[i] * inv, o[i + 1] * inv);
-                        w.y = pack2<false>(o[i + 2] * inv, o[i + 3] * inv);
-                        w.z = pack2<false>(o[i + 4] * inv, o[i + 5] * inv);
-                        w.w = pack2<false>(o[i + 6] * inv, o[i + 7] * inv);
-                        *reinterpret_cast<uint4 *>(dst + c + i) = w;
-                    }
+                for (int i = 0; i < 32; i += 8) {
+                    uint4 w;
+                    w.x = pack2<false>(o[i] * inv, o[i + 1] * inv);
+                    w.y = pack2<false>(o[i + 2] * inv, o[i + 3] * inv);
+                    w.z = pack2<false>(o[i + 4] * inv, o[i + 5] * inv);
+                    w.w = pack2<false>(o[i + 6] * inv, o[i + 7] * inv);
+                    const int d0 = c + i;  // dims d0 .. d0 + 7
+                    if (full_tile)
+                        st_shared16(stage + (d0 >> 6) * kTcQSlab + row * 128 + ((((d0 & 63) >> 3) ^ (row & 7)) << 4), w);
+                    else if (live && !failed_s)
+                        *reinterpret_cast<uint4 *>(dst + d0) = w;
+                }
+            }
+            if (full_tile) {
+                fence_proxy_async_smem();
+                asm volatile("bar.sync %0, 128;" ::"r"(1 + T) : "memory");  // the tile's four softmax warps
+                if ((warp & 3) == 0 && lane == 0) {
+                    for (int sl = 0; sl < 2; ++sl)
+                        tma_store_3d(&tmO, sl * 64, h * a.group, q0 + tok_begin, stage + sl * kTcQSlab);
+                    tma_store_commit_and_wait_read();
                 }
             }
         }
@@ -436,6 +453,7 @@ static pa_status make_q_map(CUtensorMap *map, const void *q, int total_tokens, i
 
 template <int BS>
 static pa_status launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                           const CUtensorMap &to,
                            const PrefillTcArgs &a, dim3 grid, cudaStream_t stream) {
     auto kern = prefill_tc_kernel<BS>;
     static std::atomic<uint64_t> raised{0};
@@ -449,7 +467,7 @@ static pa_status launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const C
         if (st != PA_OK) return st;
         raised.fetch_or(bit, std::memory_order_release);
     }
-    kern<<<grid, kTcThreads, kTcSmem, stream>>>(tq, tk, tv, a);
+    kern<<<grid, kTcThreads, kTcSmem, stream>>>(tq, tk, tv, to, a);
     return cuda_check(cudaGetLastError(), "prefill tcgen05 launch");
 }
 
@@ -475,8 +493,10 @@ pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_ca
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.err = err;
     const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     pa_status st = make_q_map(&tq, q, total_tokens, num_q_heads, group, a.tile_tokens);
+    if (st != PA_OK) return st;
+    st = make_q_map(&to, out, total_tokens, num_q_heads, group, a.tile_tokens);  // same geometry
     if (st != PA_OK) return st;
     st = make_map(&tk, k_cache, false, 128, rows, block_size);
     if (st != PA_OK) return st;
@@ -484,8 +504,8 @@ pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_ca
     if (st != PA_OK) return st;
     const int tiles = (max_query_len + a.tile_tokens - 1) / a.tile_tokens;
     dim3 grid((tiles + kTcTiles - 1) / kTcTiles, num_kv_heads, num_seqs);
-    return block_size == 16 ? launch_tc<16>(tq, tk, tv, a, grid, stream)
-                            : launch_tc<32>(tq, tk, tv, a, grid, stream);
+    return block_size == 16 ? launch_tc<16>(tq, tk, tv, to, a, grid, stream)
+                            : launch_tc<32>(tq, tk, tv, to, a, grid, stream);
 }
 
 }  // namespace pa
