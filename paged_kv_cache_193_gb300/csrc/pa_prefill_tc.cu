@@ -8,22 +8,24 @@
 //    tiles read every K/V stage, so each SM moves half the page bytes per
 //    FLOP that one tile per CTA would.  One CTA per SM: 225 KB of shared
 //    memory (both query tiles, five K and five V stages of 64 keys) and all
-//    512 TMEM columns (per tile: two S buffers of 64 columns and O).
+//    512 TMEM columns (per tile: S, P, the first half of the query and O).
 //  * Warp 8 streams the queries (3-D TMA) and the K pages of each block of
 //    64 keys, warp 10 the V pages; lane p issues page p's 2-D TMA boxes
 //    (hardware 128-byte swizzle), with the block table read one block ahead.
 //    Warp 10 also zeroes the V rows past the context in the last block.
 //  * Warp 9 + 2 T issues tile T's MMAs (tcgen05.mma.cta_group::1.kind::f16,
-//    one thread): S = Q K^T (M 128 x N 64 x K 128, both operands K-major
-//    in shared memory) into one of two S buffers, and O += P V (P read from
-//    tensor memory, V read MN-major straight from the page layout).  Each
-//    group is committed to an mbarrier.  S(j + 1) is computed while the
-//    softmax works on S(j).
+//    one thread): S = Q K^T (M 128 x N 64 x K 128; K K-major in shared
+//    memory, query dims 0-63 from tensor memory and 64-127 from shared
+//    memory, which halves the shared-memory reads of the query), and
+//    O += P V (P read from tensor memory, V read MN-major straight from the
+//    page layout).  Each group is committed to an mbarrier.  S(j + 1) is
+//    issued as soon as the softmax holds S(j) in registers, before PV(j).
 //  * Warps 4 T .. 4 T + 3 do tile T's softmax, one query row (TMEM lane) per
-//    thread: read S, apply the causal mask, keep the row's sum against a
-//    reference max that only moves when the row max outgrows it by 2^8 (so
-//    O is rescaled in tensor memory rarely), and store P as bf16 pairs over
-//    the first half of S(j), which PV(j) reads.
+//    thread: copy the row's first 64 query dims into tensor memory once,
+//    then per block read S, apply the causal mask, keep the row's sum
+//    against a reference max that only moves when the row max outgrows it
+//    by 2^8 (so O is rescaled in tensor memory rarely), and store P as bf16
+//    pairs in its own columns, which PV(j) reads.
 #include <cudaTypedefs.h>
 #include <limits.h>
 #include <math.h>
@@ -72,10 +74,11 @@ constexpr int kTcSmem = kTcVOff + kTcStages * kTcKVStage + 1024;
 // grows past it by more than this (base-2 units): P <= 2^8, and O is
 // rescaled in tensor memory only then.
 constexpr float kTcRescaleThreshold = 8.f;
-// Tensor memory, tile T at columns [256 T, 256 T + 256): S of even blocks
-// [0, 64), S of odd blocks [64, 128), O [128, 256).  P of a block (bf16
-// pairs, 32 columns) is written over the first half of that block's S.
+// Tensor memory, tile T at columns [256 T, 256 T + 256): S [0, 64), P (bf16
+// pairs) [64, 96), query dims 0-63 (bf16 pairs) [96, 128), O [128, 256).
 constexpr int kTcTmemCols = 512;
+constexpr int kTcPCol = 64;
+constexpr int kTcQCol = 96;
 constexpr int kTcOCol = 128;
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 
@@ -88,9 +91,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t q_full, v_zeroed;
     // kv_full[st]: both the K and the V pages of the stage's block have landed;
-    // kv_empty[st]: every tile's PV of that block is done (its QK came before)
+    // kv_empty[st]: every tile's PV of that block is done (its QK came before),
+    // as seen by one softmax thread of each tile
     __shared__ __align__(8) uint64_t kv_full[kTcStages], kv_empty[kTcStages];
-    __shared__ __align__(8) uint64_t s_full[kTcTiles][2], p_full[kTcTiles][2], pv_done[kTcTiles], drain[kTcTiles];
+    // per tile: S written (s_full), S read into registers (s_free), P
+    // written (p_full), PV done (pv_done), query half in TMEM (q_tmem)
+    __shared__ __align__(8) uint64_t s_full[kTcTiles], s_free[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles],
+        q_tmem[kTcTiles], drain[kTcTiles];
     __shared__ uint32_t tmem_base_s;
     __shared__ int failed_s;
 
@@ -127,10 +134,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(smem_addr(&kv_empty[i]), ntiles);
         }
         for (int t = 0; t < kTcTiles; ++t) {
-            for (int b = 0; b < 2; ++b) {
-                mbar_init(smem_addr(&s_full[t][b]), 1);
-                mbar_init(smem_addr(&p_full[t][b]), 4);
-            }
+            mbar_init(smem_addr(&s_full[t]), 1);
+            mbar_init(smem_addr(&s_free[t]), 4);  // one arrival per softmax warp
+            mbar_init(smem_addr(&p_full[t]), 4);
+            mbar_init(smem_addr(&q_tmem[t]), 4);
             mbar_init(smem_addr(&pv_done[t]), 1);
             mbar_init(smem_addr(&drain[t]), 1);
         }
@@ -226,8 +233,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else if (warp == kTcMmaWarp || warp == kTcMmaWarpB) {
         // ---------------- MMA issue, one thread per tile ----------------
-        // S(j + 1) is computed while the softmax works on S(j); P(j) lives in
-        // S(j)'s columns, so S(j + 2) waits until PV(j) has read it.
+        // S(j + 1) is issued once the softmax has S(j) in registers, then
+        // PV(j) once P(j) is written; P has its own columns, so no S waits
+        // for a PV.
         const int T = warp == kTcMmaWarp ? 0 : 1;
         if (lane == 0 && T < ntiles) {
             constexpr uint32_t idesc_qk = tc_idesc_bf16(kTcRows, kTcKeys, 0, 0);
@@ -235,46 +243,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // a descriptor's start address is its low field (16-byte units,
             // no carry out within shared memory): every operand descriptor is
             // a base descriptor plus an offset, so issuing an MMA costs one add
-            const uint64_t q_desc = tc_smem_desc(base + kTcQOff + T * kTcQTile, 16, 1024, 2);
+            const uint64_t q_desc = tc_smem_desc(base + kTcQOff + T * kTcQTile + kTcQSlab, 16, 1024, 2);
             const uint64_t k_desc = tc_smem_desc(base + kTcKOff, 16, 1024, 2);
             const uint64_t v_desc = tc_smem_desc(base + kTcVOff, kTcKVSlab, 1024, 2);
-            const uint32_t tS = tmem + T * 256, tO = tS + kTcOCol;
-            bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, kTcWaitNs);
+            const uint32_t tS = tmem + T * 256, tP = tS + kTcPCol, tQ = tS + kTcQCol, tO = tS + kTcOCol;
+            bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, kTcWaitNs) &&
+                      mbar_wait_bounded(smem_addr(&q_tmem[T]), 0, kTcWaitNs);
             auto qk = [&](int kb) {  // S(kb) = Q K(kb)^T
-                const int ks = kb % kTcStages, b = kb & 1;
+                const int ks = kb % kTcStages;
                 // K and V of the block: V(kb) is in place for PV(kb) too
                 ok = ok && mbar_wait_bounded(smem_addr(&kv_full[ks]), (kb / kTcStages) & 1, kTcWaitNs);
-                // S(kb)'s columns held P(kb - 2): PV(kb - 2) must have read them
-                if (kb >= 2) ok = ok && mbar_wait_bounded(smem_addr(&pv_done[T]), kb & 1, kTcWaitNs);
                 tc_fence_after();
                 if (ok) {
                     const uint64_t b0 = k_desc + ((ks * kTcKVStage) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 128 / 16; ++kk) {
-                        const uint32_t qoff = ((kk >> 2) * kTcQSlab + (kk & 3) * 32) >> 4;
-                        const uint32_t koff = ((kk >> 2) * kTcKVSlab + (kk & 3) * 32) >> 4;
-                        tc_mma_bf16(tS + b * 64, q_desc + qoff, b0 + koff, idesc_qk, kk > 0);
-                    }
+                    for (int kk = 0; kk < 4; ++kk)  // dims 16 kk .. 16 kk + 15: query from tensor memory
+                        tc_mma_bf16_ts(tS, tQ + kk * 8, b0 + ((kk * 32) >> 4), idesc_qk, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)  // dims 64 + 16 kk ..: both from shared memory
+                        tc_mma_bf16(tS, q_desc + ((kk * 32) >> 4), b0 + ((kTcKVSlab + kk * 32) >> 4), idesc_qk,
+                                    true);
                 }
-                tc_commit(smem_addr(&s_full[T][b]));
+                tc_commit(smem_addr(&s_full[T]));
             };
             qk(0);
-            if (nkb > 1) qk(1);
             for (int kb = 0; kb < nkb; ++kb) {
-                const int vs = kb % kTcStages, b = kb & 1;
-                ok = ok && mbar_wait_bounded(smem_addr(&p_full[T][b]), (kb >> 1) & 1, kTcWaitNs);
+                const int vs = kb % kTcStages;
+                if (kb + 1 < nkb) {
+                    // the softmax holds S(kb) in registers
+                    ok = ok && mbar_wait_bounded(smem_addr(&s_free[T]), kb & 1, kTcWaitNs);
+                    qk(kb + 1);
+                }
+                ok = ok && mbar_wait_bounded(smem_addr(&p_full[T]), kb & 1, kTcWaitNs);
                 if (kb == nkb - 1 && partial) ok = ok && mbar_wait_bounded(smem_addr(&v_zeroed), 0, kTcWaitNs);
                 tc_fence_after();
                 if (ok) {  // O += P(kb) V(kb)
                     const uint64_t b0 = v_desc + ((vs * kTcKVStage) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kTcKeys / 16; ++kk)
-                        tc_mma_bf16_ts(tO, tS + b * 64 + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_pv,
-                                       kb > 0 || kk > 0);
+                        tc_mma_bf16_ts(tO, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_pv, kb > 0 || kk > 0);
                 }
                 tc_commit(smem_addr(&pv_done[T]));
-                tc_commit(smem_addr(&kv_empty[vs]));
-                if (kb + 2 < nkb) qk(kb + 2);
             }
             if (!ok) fail();
             // every MMA issued above is complete before the TMEM is released
@@ -293,21 +302,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // blocks ending at or before every row's position need no mask
             const int warp_min_pos = __reduce_min_sync(0xffffffffu, pos);
             const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-            const uint32_t tS = tmem + lane_addr + T * 256, tO = tS + kTcOCol;
+            const uint32_t tS = tmem + lane_addr + T * 256, tP = tS + kTcPCol, tO = tS + kTcOCol;
             const float scale = a.score_scale;
             float m_ref = -INFINITY, l_run = 0.f;
-            bool ok = true;
+            bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, kTcWaitNs);
+            {
+                // the row's query dims 0-63 (128-byte swizzled in shared
+                // memory) as bf16 pairs in tensor memory: the A operand of
+                // QK's first four MMAs
+                const uint32_t qrow = base + kTcQOff + T * kTcQTile + row * 128;
+                uint32_t w[32];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 c = lds128(qrow + ((j ^ (row & 7)) << 4));
+                    w[4 * j] = c.x;
+                    w[4 * j + 1] = c.y;
+                    w[4 * j + 2] = c.z;
+                    w[4 * j + 3] = c.w;
+                }
+                tc_st32(tS + kTcQCol, w);
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&q_tmem[T]));
+            }
             for (int kb = 0; kb < nkb; ++kb) {
-                const int b = kb & 1;
                 const int key0 = kb * kTcKeys;
                 const bool masked = key0 + kTcKeys - 1 > warp_min_pos;
-                ok = ok && mbar_wait_bounded(smem_addr(&s_full[T][b]), (kb >> 1) & 1, kTcWaitNs);
+                ok = ok && mbar_wait_bounded(smem_addr(&s_full[T]), kb & 1, kTcWaitNs);
                 tc_fence_after();
                 float v[64];
                 {
                     float lo[32], hi[32];
-                    tc_ld32(tS + b * 64, lo);
-                    tc_ld32(tS + b * 64 + 32, hi);
+                    tc_ld32(tS, lo);
+                    tc_ld32(tS + 32, hi);
                     tc_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -315,6 +343,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         v[32 + i] = hi[i];
                     }
                 }
+                // S may now be overwritten by S(kb + 1)
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&s_free[T]));
                 if (masked) {
 #pragma unroll
                     for (int i = 0; i < 64; ++i) v[i] = key0 + i <= pos ? v[i] : -INFINITY;
@@ -339,8 +371,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     rescale = kb > 0;
                 }
                 if (__any_sync(0xffffffffu, rescale)) {
-                    // O must hold PV(kb - 1) before it is scaled (PV(kb - 2)
-                    // finished before S(kb) was computed)
+                    // O must hold PV(kb - 1) before it is scaled
                     ok = ok && mbar_wait_bounded(smem_addr(&pv_done[T]), (kb - 1) & 1, kTcWaitNs);
                     tc_fence_after();
 #pragma unroll
@@ -354,7 +385,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     tc_wait_st();
                 }
-                // P = exp2(scale * s - m_ref) (bf16), over the first half of S(kb)
+                // P = exp2(scale * s - m_ref) (bf16), in P's columns
                 const float neg = m_ref == -INFINITY ? 0.f : -m_ref;
                 float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -371,11 +402,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) pk[i] = pack2<false>(v[2 * i], v[2 * i + 1]);
-                tc_st32(tS + b * 64, pk);
+                if (kb > 0) {  // PV(kb - 1) has read P(kb - 1), and K and V of block kb - 1
+                    ok = ok && mbar_wait_bounded(smem_addr(&pv_done[T]), (kb - 1) & 1, kTcWaitNs);
+                    tc_fence_after();
+                    // the tile's release of that block's stage (the last
+                    // block's stage is never reused, so it is not released)
+                    if ((warp & 3) == 0 && lane == 0) mbar_arrive(smem_addr(&kv_empty[(kb - 1) % kTcStages]));
+                }
+                tc_st32(tP, pk);
                 tc_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&p_full[T][b]));
+                if (lane == 0) mbar_arrive(smem_addr(&p_full[T]));
             }
             // every PV is done once the tile's MMA thread's final commit lands
             ok = ok && mbar_wait_bounded(smem_addr(&drain[T]), 0, kTcWaitNs);
