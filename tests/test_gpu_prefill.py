@@ -60,6 +60,27 @@ def test_prefill_matches_oracle(api, oracle, cuda_device, D, B, G, Hkv, kernel):
     assert api.device_errors() == 0
 
 
+@pytest.mark.parametrize("G,Hkv,B", [(4, 2, 16), (16, 1, 32), (1, 4, 16)])
+def test_prefill_many_items_matches_oracle(api, oracle, cuda_device, G, Hkv, B):
+    """Several waves of (query-tile pair, KV head, sequence) blocks over 48
+    sequences with ragged chunks and prefixes: blocks with no rows, with one
+    tile, with a partial tile and with a partial last key block, all checked
+    against the oracle element by element."""
+    rng = np.random.default_rng(100 + G + B)
+    S = 48
+    chunks = rng.integers(1, 200, size=S, endpoint=True).tolist()
+    prefixes = rng.integers(16, 300, size=S, endpoint=True).tolist()
+    wl = W.make_prefill(cuda_device, seed=G + Hkv + B, num_seqs=S, chunk=chunks, prefixes=prefixes,
+                        num_q_heads=G * Hkv, num_kv_heads=Hkv, head_dim=128, block_size=B)
+    W.poison_prefill(wl)
+    api.device_errors(clear=True)
+    slots_ref, kc_ref, vc_ref, ref = _oracle_step(oracle, wl)
+    slots, out = _gpu_step(api, wl, cuda_device, "auto")
+    assert np.array_equal(slots, slots_ref)
+    compare(out, ref, what=f"prefill many items G{G} B{B}")
+    assert api.device_errors() == 0
+
+
 def test_prefill_last_row_is_decode(api, cuda_device):
     """The last chunk token of every sequence computes what the decode
     kernel computes for that context."""
