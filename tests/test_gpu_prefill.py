@@ -81,6 +81,38 @@ def test_prefill_many_items_matches_oracle(api, oracle, cuda_device, G, Hkv, B):
     assert api.device_errors() == 0
 
 
+@pytest.mark.parametrize("kernel", ["auto", "mma"])
+def test_prefill_empty_chunks(api, oracle, cuda_device, kernel):
+    """Sequences that bring no chunk rows sit between ones that do: their
+    blocks have nothing to compute and nothing of theirs is written."""
+    wl = W.make_prefill(cuda_device, seed=31, num_seqs=6, chunk=[0, 5, 0, 130, 1, 0],
+                        prefixes=[40, 0, 300, 77, 16, 9], num_q_heads=8, num_kv_heads=2,
+                        head_dim=128, block_size=16)
+    W.poison_prefill(wl)
+    api.device_errors(clear=True)
+    slots_ref, kc_ref, vc_ref, ref = _oracle_step(oracle, wl)
+    slots, out = _gpu_step(api, wl, cuda_device, kernel)
+    assert np.array_equal(slots, slots_ref)
+    assert np.array_equal(W.bits(wl.k_cache), kc_ref) and np.array_equal(W.bits(wl.v_cache), vc_ref)
+    compare(out, ref, what=f"prefill empty chunks {kernel}")
+    assert api.device_errors() == 0
+
+
+@pytest.mark.parametrize("B", [16, 32])
+def test_prefill_long_context(api, oracle, cuda_device, B):
+    """A 64-token chunk at the end of a 32,768-token context: 512 key blocks
+    per tile pair, so every stage of the page ring is reused many times."""
+    wl = W.make_prefill(cuda_device, seed=40 + B, num_seqs=2, chunk=[64, 40],
+                        prefixes=[32768 - 64, 20000], num_q_heads=4, num_kv_heads=1,
+                        head_dim=128, block_size=B)
+    W.poison_prefill(wl)
+    api.device_errors(clear=True)
+    _, _, _, ref = _oracle_step(oracle, wl)
+    _, out = _gpu_step(api, wl, cuda_device, "auto")
+    compare(out, ref, what=f"prefill long context B{B}")
+    assert api.device_errors() == 0
+
+
 def test_prefill_last_row_is_decode(api, cuda_device):
     """The last chunk token of every sequence computes what the decode
     kernel computes for that context."""
