@@ -712,6 +712,94 @@ def run_reference(args):
     print(json.dumps(result), flush=True)
 
 
+def run_prefill_e2e(api, wl, bt, K, world, device):
+    """The prefill metric through the public API with the step's inputs in
+    pinned host memory: the queries, the chunk's new K/V rows, the context
+    lengths and the chunk offsets are copied in, the step runs (chunk slots,
+    append, attention) and the output is copied back, all inside the timed
+    region.  Pipelined and double-buffered as the decode's end-to-end loop:
+    step i + 1's inputs go in on a copy stream while step i runs, step i's
+    output comes back on a third stream."""
+    sh = wl.shape
+    T = int(wl.query_start[-1])
+    mq = wl.max_query_len
+    h_in = [wl.q.cpu().pin_memory(), wl.k_new.cpu().pin_memory(), wl.v_new.cpu().pin_memory(),
+            torch.from_numpy(wl.context_lens).pin_memory(), torch.from_numpy(wl.query_start).pin_memory()]
+    h_out = [torch.empty(wl.q.shape, dtype=wl.q.dtype).pin_memory() for _ in range(2)]
+    bufs = [([torch.empty(t.shape, dtype=t.dtype, device=device) for t in h_in],
+             torch.empty(T, dtype=torch.int32, device=device), torch.empty_like(wl.q)) for _ in range(2)]
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev = lambda: torch.cuda.Event()
+    in_done, step_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+
+    def copy_in(i):
+        d_in = bufs[i & 1][0]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(step_done[i & 1])  # step i - 2 has read this buffer
+            for d, h in zip(d_in, h_in):
+                d.copy_(h, non_blocking=True)
+            in_done[i & 1].record(s_in)
+
+    def step_on(d_in, d_slots, d_out):
+        d_q, d_k, d_v, d_cl, d_qs = d_in
+        api.chunk_slot_mapping(bt, d_cl, d_qs, sh.block_size, out=d_slots, stream=comp)
+        api.cache_append(d_k, d_v, d_slots, wl.k_cache, wl.v_cache, stream=comp)
+        api.prefill(d_q, wl.k_cache, wl.v_cache, bt, d_cl, d_qs, mq, wl.softmax_scale, out=d_out,
+                    stream=comp)
+
+    def run(i, n):
+        d_in, d_slots, d_out = bufs[i & 1]
+        if i + 1 < n:
+            copy_in(i + 1)
+        comp.wait_event(in_done[i & 1])
+        if i >= 2:
+            comp.wait_event(out_done[i & 1])  # step i - 2's output is back on the host
+        step_on(d_in, d_slots, d_out)
+        step_done[i & 1].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(step_done[i & 1])
+            h_out[i & 1].copy_(d_out, non_blocking=True)
+            out_done[i & 1].record(s_out)
+
+    def loop(n, start=None, end=None):
+        if start is not None:
+            start.record(comp)
+        s_in.wait_stream(comp)
+        copy_in(0)
+        for i in range(n):
+            run(i, n)
+        comp.wait_stream(s_out)
+        if end is not None:
+            end.record(comp)
+
+    n = max(10, min(K, 200))
+    loop(4)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    loop(n, a, b)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), world, device)
+    # the pipelined steps computed what a plain step computes from the same inputs
+    d_slots = torch.empty(T, dtype=torch.int32, device=device)
+    d_out = torch.empty_like(wl.q)
+    step_on([wl.q, wl.k_new, wl.v_new, torch.from_numpy(wl.context_lens).to(device),
+             torch.from_numpy(wl.query_start).to(device)], d_slots, d_out)
+    torch.cuda.synchronize()
+    if not torch.equal(h_out[(n - 1) & 1], d_out.cpu()):
+        raise RuntimeError("pipelined end-to-end prefill output differs from the plain step's")
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = h_out[0].numel() * h_out[0].element_size()
+    return {"value": round(world * wl.attention_flops() * n / (ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "ms_per_step": round(ms / n, 5),
+            "pipelining": "step i+1's inputs copied in on a second stream while step i runs, "
+                          "outputs copied back on a third; double-buffered"}
+
+
 def run_prefill(args):
     """Chunked prefill step: chunk slots, append of the chunk's K/V, causal
     attention over the paged cache.  value = attention TFLOP/s (QK^T and PV
@@ -808,6 +896,8 @@ def run_prefill(args):
                      "traffic": None},
         "clocks": clocks.summary(t0 - 1.0, t1),
     }
+    if not args.no_e2e:
+        res["e2e"] = run_prefill_e2e(api, wl, bt, K, world, device)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline_prefill(wl, args.cpu_seconds)
     if rank == 0:
