@@ -124,6 +124,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // released once per tile
     const int kend = first_pos + min(tok_begin0 + ntiles * a.tile_tokens, chunk);
     const int nkb = (kend + kTcKeys - 1) / kTcKeys;
+    // Tile T's own blocks end at its last row's position: the earlier tile
+    // skips a trailing block that only the later tile's rows reach (the
+    // blocks a tile skips are among the last two, which no stage reuses, so
+    // no release is missing).
+    auto tile_blocks = [&](int T) {
+        const int tile_end = min(tok_begin0 + (T + 1) * a.tile_tokens, chunk);
+        return (first_pos + tile_end + kTcKeys - 1) / kTcKeys;
+    };
     const bool partial = kend % kTcKeys != 0;  // the last block holds keys past the context
 
     if (tid == 0) {
@@ -266,10 +274,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc_commit(smem_addr(&s_full[T]));
             };
+            const int nkb_t = tile_blocks(T);
             qk(0);
-            for (int kb = 0; kb < nkb; ++kb) {
+            for (int kb = 0; kb < nkb_t; ++kb) {
                 const int vs = kb % kTcStages;
-                if (kb + 1 < nkb) {
+                if (kb + 1 < nkb_t) {
                     // the softmax holds S(kb) in registers
                     ok = ok && mbar_wait_bounded(smem_addr(&s_free[T]), kb & 1, kTcWaitNs);
                     qk(kb + 1);
@@ -326,7 +335,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&q_tmem[T]));
             }
-            for (int kb = 0; kb < nkb; ++kb) {
+            const int nkb_t = tile_blocks(T);
+            for (int kb = 0; kb < nkb_t; ++kb) {
                 const int key0 = kb * kTcKeys;
                 const bool masked = key0 + kTcKeys - 1 > warp_min_pos;
                 ok = ok && mbar_wait_bounded(smem_addr(&s_full[T]), kb & 1, kTcWaitNs);
