@@ -85,6 +85,8 @@ def parse():
                          "blocks on the device (pa_block_alloc), then runs the step")
     ap.add_argument("--prefill", action="store_true",
                     help="time chunked prefill (16 sequences x 512-token chunks) instead of decode")
+    ap.add_argument("--q-heads", type=int, default=32, help="prefill: query heads (default 32)")
+    ap.add_argument("--kv-heads", type=int, default=8, help="prefill: KV heads (default 8)")
     ap.add_argument("--separate", action="store_true",
                     help="time the unfused entry points (3-4 kernels per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -809,7 +811,8 @@ def run_prefill(args):
     device = torch.device("cuda", local)
     init_dist(world, "nccl")
     from paged_kv_cache_193_gb300 import api
-    wl = W.make_prefill(device, num_seqs=args.num_seqs or 16, block_size=args.block_size or 16)
+    wl = W.make_prefill(device, num_seqs=args.num_seqs or 16, block_size=args.block_size or 16,
+                        num_q_heads=args.q_heads, num_kv_heads=args.kv_heads)
     sh = wl.shape
     bt = torch.from_numpy(wl.block_tables).to(device)
     cl = torch.from_numpy(wl.context_lens).to(device)
