@@ -9,9 +9,10 @@
 //    FLOP that one tile per CTA would.  One CTA per SM: 225 KB of shared
 //    memory (both query tiles, five K and five V stages of 64 keys) and all
 //    512 TMEM columns (per tile: S, P, the first half of the query and O).
-//  * Warp 8 streams the queries (3-D TMA) and the K pages of each block of
-//    64 keys, warp 10 the V pages; lane p issues page p's 2-D TMA boxes
-//    (hardware 128-byte swizzle), with the block table read one block ahead.
+//  * Thread 0 requests the query tiles (3-D TMA) as soon as the barriers
+//    exist.  Warp 8 streams the K pages of each block of 64 keys, warp 10
+//    the V pages; lane p issues page p's 2-D TMA boxes (hardware 128-byte
+//    swizzle), with the block table read one block ahead.
 //    Warp 10 also zeroes the V rows past the context in the last block.
 //  * Warp 9 + 2 T issues tile T's MMAs (tcgen05.mma.cta_group::1.kind::f16,
 //    one thread): S = Q K^T (M 128 x N 64 x K 128; K K-major in shared
@@ -134,6 +135,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
     const bool partial = kend % kTcKeys != 0;  // the last block holds keys past the context
 
+    // Loader lanes pg < NPG own page pg of a key block.  The block table
+    // entry is fetched one block ahead and only checked when it is used, so
+    // the fetch overlaps the current block's copies; the first block's
+    // entries are fetched before the barrier and tensor-memory setup.
+    const int32_t *bt = a.block_tables + static_cast<int64_t>(s) * a.max_blocks;
+    constexpr int kPastKeys = INT_MIN;
+    auto page_entry = [&](int kb) {
+        const int pg_idx = kb * NPG + lane;
+        return (lane < NPG && pg_idx * BS < kend) ? __ldg(bt + pg_idx) : kPastKeys;
+    };
+    const bool loader = warp == kTcLoadWarp || warp == kTcVLoadWarp;
+    int e_first = loader ? page_entry(0) : kPastKeys;
+
     if (tid == 0) {
         mbar_init(smem_addr(&q_full), 1);
         mbar_init(smem_addr(&v_zeroed), 1);
@@ -151,7 +165,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         failed_s = 0;
         fence_barrier_init();
-        prefetch_tensormap(&tmQ);
+        // the query tiles are requested before the tensor-memory setup
+        mbar_arrive_expect_tx(smem_addr(&q_full), ntiles * kTcQTile);
+        for (int T = 0; T < ntiles; ++T)
+            for (int sl = 0; sl < 2; ++sl)
+                tma_load_3d(base + kTcQOff + T * kTcQTile + sl * kTcQSlab, &tmQ, sl * 64, h * a.group,
+                            q0 + tok_begin0 + T * a.tile_tokens, smem_addr(&q_full));
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
         prefetch_tensormap(&tmO);
@@ -172,16 +191,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         atomicExch(&failed_s, 1);
     };
 
-    // Loader lanes pg < NPG own page pg of a key block.  The block table
-    // entry is fetched one block ahead and only checked when it is used, so
-    // the fetch overlaps the current block's copies.
-    const int32_t *bt = a.block_tables + static_cast<int64_t>(s) * a.max_blocks;
     const int rows_total = a.num_blocks * a.num_kv_heads * BS;
-    constexpr int kPastKeys = INT_MIN;
-    auto page_entry = [&](int kb) {
-        const int pg_idx = kb * NPG + lane;
-        return (lane < NPG && pg_idx * BS < kend) ? __ldg(bt + pg_idx) : kPastKeys;
-    };
     // the page's first row in the cache; pages past the keys (and bad
     // entries, which are reported) read a row past the end: zeros
     auto page_row = [&](int blk) {
@@ -193,21 +203,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return (blk * a.num_kv_heads + h) * BS;
     };
 
-    if (warp == kTcLoadWarp || warp == kTcVLoadWarp) {
-        // ------------- loads: warp 8 the queries and K, warp 10 V -------------
+    if (loader) {
+        // ------------- loads: warp 8 K, warp 10 V (thread 0 requested the queries) -------------
         const bool is_k = warp == kTcLoadWarp;
         const CUtensorMap *map = is_k ? &tmK : &tmV;
         const uint32_t ring = base + (is_k ? kTcKOff : kTcVOff);
         const uint64_t policy = l2_evict_first_policy();
-        if (is_k && lane == 0) {
-            const uint32_t bar = smem_addr(&q_full);
-            mbar_arrive_expect_tx(bar, ntiles * kTcQTile);
-            for (int T = 0; T < ntiles; ++T)
-                for (int sl = 0; sl < 2; ++sl)
-                    tma_load_3d(base + kTcQOff + T * kTcQTile + sl * kTcQSlab, &tmQ, sl * 64, h * a.group,
-                                q0 + tok_begin0 + T * a.tile_tokens, bar);
-        }
-        int e_next = page_entry(0);
+        int e_next = e_first;
         for (int kb = 0; kb < nkb; ++kb) {
             const int st = kb % kTcStages, ph = (kb / kTcStages) & 1;
             const int y = page_row(e_next);
