@@ -17,7 +17,8 @@
  *     for Llama 3": grouped-query attention, several query heads per KV head.
  *   - "vLLM PagedAttention Optimization: Complete Step-by-Step Tuning Guide",
  *     Step 3: an FP8 KV cache halves the bytes read; the format is E4M3
- *     (first page, "Quantization Without Quality Loss").
+ *     ("Optimizing Llama 3.1 405B Inference with vLLM PagedAttention",
+ *     section "Quantization Without Quality Loss").
  *
  * Conventions for every entry point
  *   - All pointers are DEVICE pointers of the current CUDA device unless a
@@ -84,13 +85,14 @@ typedef enum pa_kv_dtype {
 
 /*
  * pa_slot_mapping -- slot of each sequence's newest token.
- * Source: "PagedAttention Mechanics" (first page): the arriving token is
- * appended at the end of the sequence's logical blocks.
+ * Source: "Optimizing Llama 3.1 405B Inference with vLLM PagedAttention",
+ * section "PagedAttention Mechanics": the arriving token is appended at the
+ * end of the sequence's logical blocks.
  *   slot_mapping[s] = block_tables[s][(n-1) / block_size] * block_size
  *                     + (n-1) % block_size,   n = context_lens[s] > 0
  *   slot_mapping[s] = -1                      n <= 0
  * The host allocator must already have put a block in the table for
- * position n-1 ("a fresh physical page only if needed").
+ * position n-1 (a new block is taken only when a token starts one).
  * block_tables, context_lens: inputs as above.  slot_mapping: int32
  * [num_seqs] output.  One kernel.
  */
@@ -100,8 +102,10 @@ pa_status pa_slot_mapping(const int32_t *block_tables, int max_blocks_per_seq,
 
 /*
  * pa_cache_append -- write each new token's K and V into its cache slot.
- * Source: "PagedAttention Mechanics" (first page, append on token arrival);
- * Step 3 of the tuning guide (FP8 KV cache).
+ * Source: "Optimizing Llama 3.1 405B Inference with vLLM PagedAttention",
+ * section "PagedAttention Mechanics" (append on token arrival); Step 3 of
+ * "vLLM PagedAttention Optimization: Complete Step-by-Step Tuning Guide"
+ * (FP8 KV cache).
  *   k, v          bf16 [num_tokens][num_kv_heads][head_dim] (inputs)
  *   slot_mapping  int32 [num_tokens]; a negative slot skips the token
  *   k_cache, v_cache  written in place at row slot % block_size of block
@@ -248,10 +252,12 @@ pa_status pa_decode_step_scaled(const void *q, const void *k_new, const void *v_
 /*
  * pa_block_alloc -- device-side block allocation for the newest tokens, with
  * copy-on-write of shared blocks.
- * Source: "a fresh physical page only if needed" ("PagedAttention
- * Mechanics", first page) and blocks shared between requests (fourth page,
- * section 2).  Reading for writes into a shared block (the pages are
- * silent): the writer first gets a private copy.
+ * Source: a new block is taken only when a token starts one ("Optimizing
+ * Llama 3.1 405B Inference with vLLM PagedAttention", section
+ * "PagedAttention Mechanics"), and requests may share blocks ("vLLM
+ * PagedAttention: Memory Optimization & High-Throughput LLM Inference
+ * Tuning", section 2).  Reading for writes into a shared block (the pages
+ * are silent): the writer first gets a private copy.
  *   context_lens int32 [num_seqs] (device, in/out): the length including the
  *                token being appended; with advance != 0 every entry > 0 is
  *                first increased by one (one new token per active sequence)
@@ -304,9 +310,11 @@ pa_status pa_decode_step_fp8_qk(const void *q, const void *k_new, const void *v_
 
 /*
  * pa_chunk_slot_mapping / pa_prefill -- chunked prefill over the paged cache.
- * Chunked prefill is named in the first page's "Production Checklist" and in
- * Step 2 of the tuning guide; the attention walks the block table as the
- * decode does (fourth page, section 2).
+ * Chunked prefill is named in the "Production Checklist" of "Optimizing
+ * Llama 3.1 405B Inference with vLLM PagedAttention" and in Step 2 of "vLLM
+ * PagedAttention Optimization: Complete Step-by-Step Tuning Guide"; the
+ * attention walks the block table as the decode does ("vLLM PagedAttention:
+ * Memory Optimization & High-Throughput LLM Inference Tuning", section 2).
  * Sequence s brings C_s = query_start[s+1] - query_start[s] new tokens at the
  * END of its context: context_lens[s] >= C_s counts them, and chunk row i
  * (query_start[s] <= i < query_start[s+1]) is logical position

@@ -22,8 +22,8 @@
  *     head).
  *   - "vLLM PagedAttention Optimization: Complete Step-by-Step Tuning Guide",
  *     Step 1 (KV bytes per token formula) and Step 3 (FP8 KV cache); the
- *     E4M3 format is named in the first page, "Quantization Without Quality
- *     Loss".
+ *     E4M3 format is named in "Optimizing Llama 3.1 405B Inference with vLLM
+ *     PagedAttention", section "Quantization Without Quality Loss".
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *   - cache layout [num_blocks][num_kv_heads][block_size][head_dim];
@@ -551,10 +551,12 @@ void pa_oracle_prefill(const uint16_t *q, const void *k_cache, const void *v_cac
 /* block allocation for the newest tokens, with copy-on-write                */
 /* ------------------------------------------------------------------------ */
 
-/* "When a new token arrives, [the engine] appends to the logical sequence
- * and allocates a fresh physical page only if needed" (first page,
- * "PagedAttention Mechanics"), and sequences may share the physical blocks of
- * a common prompt (fourth page, section 2).  Reading for a shared block that
+/* A token that arrives is added at the end of its sequence, and a new
+ * physical block is taken only when the token starts one ("Optimizing Llama
+ * 3.1 405B Inference with vLLM PagedAttention", section "PagedAttention
+ * Mechanics"); sequences may share the physical blocks of a common prompt
+ * ("vLLM PagedAttention: Memory Optimization & High-Throughput LLM Inference
+ * Tuning", section 2).  Reading for a shared block that
  * is about to be written (the pages are silent): the writer first gets its
  * own copy (copy-on-write).
  *

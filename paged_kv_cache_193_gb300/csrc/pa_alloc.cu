@@ -1,8 +1,9 @@
 // Device-side block allocation for the newest tokens, with copy-on-write.
 //
-// "When a new token arrives, [the engine] appends to the logical sequence and
-// allocates a fresh physical page only if needed" ("Optimizing Llama 3.1 405B
-// Inference with vLLM PagedAttention", section "PagedAttention Mechanics");
+// A token that arrives is added at the end of its sequence, and a new
+// physical block is taken only when the token starts one ("Optimizing Llama
+// 3.1 405B Inference with vLLM PagedAttention", section "PagedAttention
+// Mechanics");
 // sequences may share the blocks of a common prompt ("vLLM PagedAttention:
 // Memory Optimization & High-Throughput LLM Inference Tuning", section 2).  A
 // token written into a block that other sequences also reference first gets a

@@ -5,8 +5,9 @@
 // chunk's earlier tokens), all read through the sequence's block table
 // ("vLLM PagedAttention: Memory Optimization & High-Throughput LLM
 // Inference Tuning", section 2).  Chunked prefill itself is named in the
-// first page's "Production Checklist" and in Step 2 of "vLLM PagedAttention
-// Optimization: Complete Step-by-Step Tuning Guide".
+// "Production Checklist" of "Optimizing Llama 3.1 405B Inference with vLLM
+// PagedAttention" and in Step 2 of "vLLM PagedAttention Optimization:
+// Complete Step-by-Step Tuning Guide".
 //
 // One CTA per (query tile, KV head, sequence).  A query tile is 64 rows of
 // (chunk token, query head of the KV head's group), 16 per consumer warp, so
