@@ -46,6 +46,11 @@ MUTANTS = {
                              "int pos = context_lens[s] - c + (i - query_start[s]) - (c > 1);\n        double *x"),
     "chunk_slots_shifted": ("int pos = context_lens[s] - c + (i - query_start[s]);\n            int32_t block",
                             "int pos = context_lens[s] - c + (i - query_start[s]) + 1 - (i == query_start[s + 1] - 1);\n            int32_t block"),
+    "prefill_gqa_modulo": ("s, hq / group, 0, pos + 1,", "s, hq % num_kv_heads, 0, pos + 1,"),
+    "prefill_query_of_chunk_start": ("attend_range(q + ((int64_t)i * num_q_heads + hq) * head_dim",
+                                     "attend_range(q + ((int64_t)query_start[s] * num_q_heads + hq) * head_dim"),
+    "prefill_heads_reversed": ("out + ((int64_t)i * num_q_heads + hq) * head_dim, &m, &l);",
+                               "out + ((int64_t)i * num_q_heads + (num_q_heads - 1 - hq)) * head_dim, &m, &l);"),
     "partition_short": ("int t1 = t0 + partition_size;", "int t1 = t0 + partition_size - 1;"),
     "last_token_dropped": ("attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s],",
                            "attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s] - (context_lens[s] > 1),"),
