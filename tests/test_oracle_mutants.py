@@ -51,6 +51,12 @@ MUTANTS = {
                                      "attend_range(q + ((int64_t)query_start[s] * num_q_heads + hq) * head_dim"),
     "prefill_heads_reversed": ("out + ((int64_t)i * num_q_heads + hq) * head_dim, &m, &l);",
                                "out + ((int64_t)i * num_q_heads + (num_q_heads - 1 - hq)) * head_dim, &m, &l);"),
+    "e4m3_scale_dropped": ("return pa_oracle_e4m3_to_double(((const uint8_t *)cache)[index]) * kv_scale;",
+                           "return pa_oracle_e4m3_to_double(((const uint8_t *)cache)[index]);"),
+    "kv_head_ignored": ("return ((block * num_kv_heads + h) * block_size + off) * head_dim + d;",
+                        "return ((block * num_kv_heads + 0) * block_size + off) * head_dim + d;"),
+    "dims_reversed": ("return ((block * num_kv_heads + h) * block_size + off) * head_dim + d;",
+                      "return ((block * num_kv_heads + h) * block_size + off) * head_dim + (head_dim - 1 - d);"),
     "partition_short": ("int t1 = t0 + partition_size;", "int t1 = t0 + partition_size - 1;"),
     "last_token_dropped": ("attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s],",
                            "attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s] - (context_lens[s] > 1),"),
