@@ -57,6 +57,12 @@ MUTANTS = {
                         "return ((block * num_kv_heads + 0) * block_size + off) * head_dim + d;"),
     "dims_reversed": ("return ((block * num_kv_heads + h) * block_size + off) * head_dim + d;",
                       "return ((block * num_kv_heads + h) * block_size + off) * head_dim + (head_dim - 1 - d);"),
+    "append_kv_swapped": ("((uint16_t *)k_cache)[dst] = k[src];\n                    ((uint16_t *)v_cache)[dst] = v[src];",
+                          "((uint16_t *)k_cache)[dst] = v[src];\n                    ((uint16_t *)v_cache)[dst] = k[src];"),
+    "append_head_of_token_zero": ("int64_t src = ((int64_t)i * num_kv_heads + h) * head_dim + d;",
+                                  "int64_t src = ((int64_t)0 * num_kv_heads + h) * head_dim + d;"),
+    "append_fp8_unscaled": ("((uint8_t *)v_cache)[dst] = pa_oracle_e4m3_from_float(vf / scale);",
+                            "((uint8_t *)v_cache)[dst] = pa_oracle_e4m3_from_float(vf);"),
     "partition_short": ("int t1 = t0 + partition_size;", "int t1 = t0 + partition_size - 1;"),
     "last_token_dropped": ("attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s],",
                            "attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s] - (context_lens[s] > 1),"),
