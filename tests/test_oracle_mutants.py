@@ -63,6 +63,10 @@ MUTANTS = {
                                   "int64_t src = ((int64_t)0 * num_kv_heads + h) * head_dim + d;"),
     "append_fp8_unscaled": ("((uint8_t *)v_cache)[dst] = pa_oracle_e4m3_from_float(vf / scale);",
                             "((uint8_t *)v_cache)[dst] = pa_oracle_e4m3_from_float(vf);"),
+    "merge_unnormalised": ("double w = (double)l[base + p] * exp((double)m[base + p] - big) / total;",
+                           "double w = (double)l[base + p] * exp((double)m[base + p] - big);"),
+    "merge_last_partition_dropped": ("for (int p = 0; p < n; ++p) {\n                double w",
+                                     "for (int p = 0; p < n - (n > 1); ++p) {\n                double w"),
     "partition_short": ("int t1 = t0 + partition_size;", "int t1 = t0 + partition_size - 1;"),
     "last_token_dropped": ("attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s],",
                            "attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s] - (context_lens[s] > 1),"),
