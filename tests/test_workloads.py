@@ -99,3 +99,61 @@ def test_seeded_reproducible():
     a, b = W.make("tiny"), W.make("tiny")
     assert torch.equal(a.q.view(torch.int16), b.q.view(torch.int16))
     assert np.array_equal(a.block_tables, b.block_tables)
+
+
+def test_prefill_workload_shapes():
+    """The chunked-prefill step: chunk offsets are the prefix sums of the
+    chunks, each context is its prefix plus its chunk, and the query / new
+    K/V rows are the chunk rows."""
+    chunks, prefixes = [0, 5, 130, 1, 64], [40, 0, 77, 300, 16]
+    wl = W.make_prefill("cpu", seed=3, num_seqs=5, chunk=chunks, prefixes=prefixes, num_q_heads=8,
+                        num_kv_heads=2, head_dim=128, block_size=16)
+    assert wl.query_start.tolist() == [0, 0, 5, 135, 136, 200]
+    assert wl.context_lens.tolist() == [p + c for p, c in zip(prefixes, chunks)]
+    assert wl.max_query_len == 130
+    assert tuple(wl.q.shape) == (200, 8, 128) and tuple(wl.k_new.shape) == (200, 2, 128)
+    assert wl.q.dtype == torch.bfloat16
+    seen = _check_tables(wl)
+    assert all(len(v) == 1 for v in seen.values())  # no block is shared between sequences
+
+
+def test_prefill_default_is_the_8192_token_step():
+    wl = W.make_prefill("cpu")
+    assert wl.shape.num_seqs == 16 and int(wl.query_start[-1]) == 8192
+    assert np.all(np.diff(wl.query_start) == 512)
+    prefixes = wl.context_lens - 512
+    assert prefixes.min() >= 0 and prefixes.max() <= 2048
+    assert (wl.shape.num_q_heads, wl.shape.num_kv_heads, wl.shape.head_dim) == (32, 8, 128)
+
+
+def test_prefill_flops_count_the_causal_pairs():
+    """4 * D * Hq multiply-adds x 2 per (query, key) pair the causal mask
+    keeps, against a brute-force walk over every chunk row and every key."""
+    wl = W.make_prefill("cpu", seed=4, num_seqs=3, chunk=[7, 1, 20], prefixes=[0, 33, 5],
+                        num_q_heads=4, num_kv_heads=1, head_dim=64, block_size=16)
+    pairs = 0
+    for s in range(3):
+        n = int(wl.context_lens[s])
+        c = int(wl.query_start[s + 1] - wl.query_start[s])
+        for i in range(c):
+            pos = n - c + i
+            pairs += sum(1 for t in range(n) if t <= pos)
+    assert wl.attention_flops() == 4 * 64 * 4 * pairs
+
+
+def test_prefill_poison_marks_only_rows_outside_the_prefixes():
+    """After poisoning, exactly the cached-prefix rows of every sequence are
+    finite: the chunk rows (which the append writes) and unused rows hold NaN."""
+    wl = W.make_prefill("cpu", seed=6, num_seqs=3, chunk=[10, 3, 40], prefixes=[20, 0, 47],
+                        num_q_heads=4, num_kv_heads=2, head_dim=64, block_size=16)
+    W.poison_prefill(wl)
+    B = wl.shape.block_size
+    finite = torch.isfinite(wl.k_cache.float()).all(dim=3).all(dim=1).numpy()  # [NB, B]
+    expect = np.zeros_like(finite)
+    for s in range(3):
+        n = int(wl.context_lens[s])
+        c = int(wl.query_start[s + 1] - wl.query_start[s])
+        for t in range(n - c):
+            expect[wl.block_tables[s, t // B], t % B] = True
+    assert np.array_equal(finite, expect)
+    assert np.array_equal(torch.isfinite(wl.v_cache.float()).all(dim=3).all(dim=1).numpy(), expect)
