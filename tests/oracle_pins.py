@@ -488,7 +488,81 @@ def pin_fp8_qk(o):
     assert np.array_equal(b1, b2)
 
 
+
+def _pairs_for(S, Hq, rng):
+    """Every (sequence, query head) pair in shuffled order, then a sampled
+    run with repeats."""
+    every = np.array([(s_, h) for s_ in range(S) for h in range(Hq)], np.int32)
+    every = every[rng.permutation(len(every))]
+    sampled = np.stack([rng.integers(0, S, 3 * S), rng.integers(0, Hq, 3 * S)], 1).astype(np.int32)
+    return every, sampled
+
+
+def pin_decode_pairs(o):
+    """Decode attention for listed (sequence, query head) pairs -- the oracle
+    of every sampled full-size comparison -- row for row against torch SDPA
+    over the logical K/V (bf16 and E4M3 caches; groups 1, 4 and 16; page
+    sizes 16 and 32; contexts 0 and 1 among them), and bit for bit against
+    the whole-batch decode.  The per-head-scaled and E4M3-query variants'
+    pair lists equal their whole-batch results row for row."""
+    rng = np.random.default_rng(18)
+    ctx = (0, 1, 5, 16, 17, 40)
+    for B, (Hq, Hkv) in ((16, (8, 8)), (32, (8, 2)), (16, (16, 1))):
+        c = _case(ctx=ctx, Hq=Hq, Hkv=Hkv, seed=B + 3 * Hq + Hkv)
+        tables, kc, vc = c.paged(B, 24, rng)
+        cl = np.array(c.ctx)
+        G = Hq // Hkv
+        ref = c.sdpa(0.3)
+        full = o.decode(c.q, kc, vc, tables, cl, Hkv, B, 0.3)
+        for pairs in _pairs_for(len(ctx), Hq, rng):
+            got = o.decode_pairs(c.q, kc, vc, tables, cl, Hkv, B, 0.3, pairs)
+            want = ref[pairs[:, 0], pairs[:, 1]]
+            assert got.shape == want.shape
+            assert np.abs(got - want).max() < 1e-12, np.abs(got - want).max()
+            assert np.array_equal(got, full[pairs[:, 0], pairs[:, 1]])
+            empty = cl[pairs[:, 0]] == 0
+            assert np.array_equal(got[empty], np.zeros_like(got[empty]))
+            one = cl[pairs[:, 0]] == 1
+            for (s_, h), row in zip(pairs[one], got[one]):
+                assert np.array_equal(row, bits_to_f64(c.v[s_][h // G, 0]))
+        # E4M3 cache with one scale: decoded by torch's float8_e4m3fn
+        scale = 0.021
+        kq = np.full(kc.shape, 0x7F, np.uint8)
+        vq = np.full_like(kq, 0x7F)
+        codes_k, codes_v = [], []
+        for s_, n in enumerate(c.ctx):
+            ck = np.array([[[_byte(o, x, scale) for x in row] for row in h] for h in c.k[s_]],
+                          np.uint8).reshape(Hkv, n, c.D)
+            cv = np.array([[[_byte(o, x, scale) for x in row] for row in h] for h in c.v[s_]],
+                          np.uint8).reshape(Hkv, n, c.D)
+            for t in range(n):
+                kq[tables[s_, t // B], :, t % B, :] = ck[:, t, :]
+                vq[tables[s_, t // B], :, t % B, :] = cv[:, t, :]
+            codes_k.append(ck)
+            codes_v.append(cv)
+        logical = LogicalCase(c.ctx, Hq, Hkv, c.D, B + 3 * Hq + Hkv)
+        logical.k, logical.v = codes_k, codes_v
+        ref8 = logical.sdpa(0.3, deq_k=lambda a: _e4m3_torch(a) * scale,
+                            deq_v=lambda a: _e4m3_torch(a) * scale)
+        every, sampled = _pairs_for(len(ctx), Hq, rng)
+        for pairs in (every, sampled):
+            got = o.decode_pairs(c.q, kq, vq, tables, cl, Hkv, B, 0.3, pairs, kv_dtype=1,
+                                 kv_scale=scale)
+            assert np.abs(got - ref8[pairs[:, 0], pairs[:, 1]]).max() < 1e-12
+        # per-head scales and the E4M3 query: pair lists against whole batches
+        ks = np.linspace(0.01, 0.03, Hkv).astype(np.float32)
+        vs = np.linspace(0.02, 0.005, Hkv).astype(np.float32)
+        whole = o.decode_scaled(c.q, kq, vq, tables, cl, Hkv, B, 0.3, ks, vs)
+        whole_qk = o.decode_fp8_qk(c.q, kq, vq, tables, cl, Hkv, B, 0.3, 0.013, ks, vs)
+        for pairs in (every, sampled):
+            got = o.decode_scaled(c.q, kq, vq, tables, cl, Hkv, B, 0.3, ks, vs, pairs=pairs)
+            assert np.array_equal(got, whole[pairs[:, 0], pairs[:, 1]])
+            got = o.decode_fp8_qk(c.q, kq, vq, tables, cl, Hkv, B, 0.3, 0.013, ks, vs, pairs=pairs)
+            assert np.array_equal(got, whole_qk[pairs[:, 0], pairs[:, 1]])
+
+
 ALL = [pin_kv_formula, pin_e4m3_decode, pin_e4m3_encode, pin_e4m3_roundtrip, pin_attention_sdpa,
        pin_attention_fp8, pin_extreme_scores, pin_permutation, pin_prefix_sharing, pin_context_one,
        pin_identical_keys, pin_empty_context, pin_slot_mapping, pin_append_readback,
-       pin_partition_merge, pin_fp8_per_head_scales, pin_block_alloc, pin_prefill, pin_fp8_qk]
+       pin_partition_merge, pin_fp8_per_head_scales, pin_block_alloc, pin_prefill, pin_fp8_qk,
+       pin_decode_pairs]

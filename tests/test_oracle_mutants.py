@@ -67,6 +67,13 @@ MUTANTS = {
                            "double w = (double)l[base + p] * exp((double)m[base + p] - big);"),
     "merge_last_partition_dropped": ("for (int p = 0; p < n; ++p) {\n                double w",
                                      "for (int p = 0; p < n - (n > 1); ++p) {\n                double w"),
+    "pairs_fields_swapped": ("int s = pairs[2 * i], hq = pairs[2 * i + 1];",
+                             "int s = pairs[2 * i + 1], hq = pairs[2 * i];"),
+    "pairs_gqa_modulo": ("s, hq / group, 0, n, num_kv_heads,", "s, hq % num_kv_heads, 0, n, num_kv_heads,"),
+    "pairs_head_from_sequence": ("int hq = pairs ? pairs[2 * i + 1] : i % num_q_heads;",
+                                 "int hq = pairs ? pairs[2 * i] % num_q_heads : i % num_q_heads;"),
+    "pairs_output_row_of_sequence": ("kv_dtype, kv_scale, kv_scale, x,\n                     out + (int64_t)i * head_dim, &m, &l);",
+                                     "kv_dtype, kv_scale, kv_scale, x,\n                     out + (int64_t)s * head_dim, &m, &l);"),
     "partition_short": ("int t1 = t0 + partition_size;", "int t1 = t0 + partition_size - 1;"),
     "last_token_dropped": ("attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s],",
                            "attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s] - (context_lens[s] > 1),"),
