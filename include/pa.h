@@ -170,6 +170,15 @@ pa_status pa_decode_partitions(const void *q, const void *k_cache, const void *v
 
 /*
  * pa_decode_reduce -- log-sum-exp merge of the partitions into the output.
+ * Source: the pages motivate contexts of 128K tokens ("vLLM PagedAttention
+ * Optimization: Complete Step-by-Step Tuning Guide", Step 1: ~40 GB of KV
+ * per 128k-token sequence; "Optimizing Llama 3.1 405B Inference with vLLM
+ * PagedAttention", "Why Standard Attention Fails at Scale") but give no
+ * split; cutting a long context into partitions and merging them by the
+ * log-sum-exp identity is this library's design for such contexts, and the
+ * merge reproduces exactly the softmax over the whole context that section 2
+ * of "vLLM PagedAttention: Memory Optimization & High-Throughput LLM
+ * Inference Tuning" computes through the block table.
  * For each (s, hq) with n = ceil(context_lens[s] / partition_size) > 0:
  *   M = max_p m_p,  w_p = l_p * exp(m_p - M),
  *   out[s][hq] = bf16_rn( sum_p w_p o_p / sum_p w_p )
@@ -184,6 +193,14 @@ pa_status pa_decode_reduce(const void *workspace, size_t workspace_bytes,
 
 /*
  * pa_decode -- single-query paged decode attention, bf16 output.
+ * Source: "vLLM PagedAttention: Memory Optimization & High-Throughput LLM
+ * Inference Tuning", section 2 (the kernel gathers each token's K and V by
+ * walking the sequence's block table; only the last block is partly
+ * filled) and section 1 (the new token attends to every cached token);
+ * grouped-query heads as in "Optimizing vLLM Throughput with PagedAttention
+ * and Continuous Batching for Llama 3"; the E4M3 cache of Step 3 of the
+ * tuning guide.  The optional split (partition_size > 0) is this library's
+ * design for long contexts, merged as pa_decode_reduce states.
  *   out[s][hq] = bf16_rn( softmax_t(softmax_scale * kscale * q[s][hq] . K[t])
  *                         . vscale * V )  over the n_s cached tokens of KV head
  *                hq / group; zeros when n_s = 0.
@@ -368,8 +385,9 @@ pa_status pa_prefill_mma(const void *q, const void *k_cache, const void *v_cache
  *   > 0.  A call whose scratch (pa_decode_workspace_size) would exceed
  *   PA_STATIC_WORKSPACE_BYTES returns PA_ERR_WORKSPACE before launching.
  *   The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before capturing any stream.
+ *   (cudaGetSymbolAddress) with that device current, and looks it up again
+ *   when the device's context has been re-created (after cudaDeviceReset);
+ *   make that first call before capturing any stream.
  *   All calls share the one array and nothing in it needs to start at zero;
  *   calls that can overlap on the GPU (other streams, other host threads)
  *   race on it and must be serialised by the caller.  Two kernels.
@@ -389,6 +407,22 @@ pa_status pa_decode_static_workspace(const void *q, const void *k_cache, const v
  * synchronises the device.  flags is a HOST pointer.
  */
 pa_status pa_device_errors(unsigned int *flags, int clear);
+
+/*
+ * pa_test_set_wait -- TEST HOOK for the kernels' bounded waits; not for
+ * production use.  The pages have no counterpart: every wait of a kernel on
+ * a page copy gives up after a time limit, sets PA_DEVERR_TIMEOUT, waits for
+ * the copies still in flight and finishes with zeros for the affected rows,
+ * so a copy that never lands cannot hang the GPU.  This call sets that
+ * limit for kernels launched afterwards (limit_ns = 0 restores the default
+ * of 2 s; above 60 s is refused).  With stall_first_wait != 0 every
+ * pa_decode* kernel makes each warp's first wait on a barrier that no copy
+ * completes, so the wait runs out after limit_ns: tests use this to drive
+ * the give-up path without a real fault.  The drain of the copies already
+ * issued always keeps the 2 s limit.  Process-wide; read at launch time on
+ * the host, so set it while none of the library's calls is being made.
+ */
+pa_status pa_test_set_wait(uint64_t limit_ns, int stall_first_wait);
 
 /* Static description of a status code (never NULL). */
 const char *pa_status_string(pa_status status);

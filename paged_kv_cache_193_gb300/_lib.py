@@ -55,6 +55,7 @@ SIGNATURES = {
                             _P, _P]),
     "pa_decode_static_workspace": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                         _F, _I, _P, _P]),
+    "pa_test_set_wait": (_I, [ctypes.c_uint64, _I]),
     "pa_device_errors": (_I, [ctypes.POINTER(ctypes.c_uint), _I]),
     "pa_status_string": (ctypes.c_char_p, [_I]),
     "pa_last_error": (ctypes.c_char_p, []),

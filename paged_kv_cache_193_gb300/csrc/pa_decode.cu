@@ -70,9 +70,13 @@ struct DecodeArgs {
     const float *v_scales;
     float softmax_log2;  // softmax_scale * log2(e)
     float q_scale;       // E4M3 query scale of the E4M3 x E4M3 score product
+    uint64_t wait_limit_ns;  // give up on a page copy after this long
+    int stall_first_wait;    // test hook: each warp's first wait is on a barrier nothing completes
 };
 
-// Give up on a page copy after this long (normal waits are microseconds).
+// Drain limit after a wait gave up: the copies still in flight into a
+// warp's stages are always waited for with this (normal waits are
+// microseconds), so no CTA leaves with a copy landing in its shared memory.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kLn2 = 0.693147180559945309f;
 
@@ -122,6 +126,7 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
     using C = Cfg<D, BS, FP8, NT, NW, SPW>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[C::NSTAGE];
+    __shared__ __align__(8) uint64_t stall_bar;  // never completed (wait-limit test hook)
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t ring = (raw + 1023u) & ~1023u;
@@ -237,6 +242,7 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
     if (tid == 0) {
 #pragma unroll
         for (int i = 0; i < C::NSTAGE; ++i) mbar_init(smem_addr(&bars[i]), 1);
+        mbar_init(smem_addr(&stall_bar), 1);
         fence_barrier_init();
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
@@ -304,9 +310,14 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
     // ---- main loop over this warp's pages ---------------------------------
     bool ok = true;
     int k_fail = 0;
-    for (int k = 0; k < my_pages; ++k) {
+    // Test hook: give up on a barrier that no copy completes, exactly as if
+    // the first page never arrived (the copies already issued still land
+    // and are drained below).
+    if (a.stall_first_wait && my_pages > 0)
+        ok = mbar_wait_bounded(smem_addr(&stall_bar), 0, a.wait_limit_ns);
+    for (int k = 0; ok && k < my_pages; ++k) {
         const int st = warp * SPW + k % SPW;
-        if (!mbar_wait_bounded(smem_addr(&bars[st]), (k / SPW) & 1, kWaitLimitNs)) {
+        if (!mbar_wait_bounded(smem_addr(&bars[st]), (k / SPW) & 1, a.wait_limit_ns)) {
             ok = false;
             k_fail = k;
             break;
@@ -806,6 +817,8 @@ static pa_status run_decode(const void *q, const void *k_cache, const void *v_ca
     a.v_scales = app ? app->v_scales : nullptr;
     a.softmax_log2 = softmax_scale * 1.4426950408889634f;
     a.q_scale = app ? app->q_scale : 0.f;
+    a.wait_limit_ns = wait_limit_ns();
+    a.stall_first_wait = stall_first_wait();
 
     if (parts > 0x7fffffffLL) return fail(PA_ERR_UNSUPPORTED, "too many partitions");
     dim3 grid(static_cast<unsigned>(split ? parts : 1), sh.num_kv_heads, sh.num_seqs);

@@ -26,6 +26,11 @@ pa_status cuda_check(cudaError_t e, const char *what);
 void clear_error();
 // Device address of the library's error word on the current device.
 unsigned int *device_error_word();
+// Limit of a kernel's wait for a page copy (nanoseconds; 2 s unless a test
+// set another), and whether the decode kernel's first waits are made to run
+// out on purpose (test hook); both read when a kernel is launched.
+uint64_t wait_limit_ns();
+int stall_first_wait();
 // Launch the partition merge (arguments already validated).
 pa_status launch_reduce(const void *workspace, const int32_t *context_lens, int num_seqs,
                         int num_q_heads, int head_dim, int partition_size, int max_partitions,

@@ -12,6 +12,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "pa_device.cuh"
 
 namespace pa {
@@ -47,6 +49,15 @@ unsigned int *device_error_word() {
     if (dev < 64) cache[dev] = static_cast<unsigned int *>(p);
     return static_cast<unsigned int *>(p);
 }
+
+// Wait limit of the kernels and the test hook that makes the decode
+// kernel's first waits run out (pa_test_set_wait).
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+static std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
+static std::atomic<int> g_stall_first_wait{0};
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+int stall_first_wait() { return g_stall_first_wait.load(std::memory_order_relaxed); }
 
 // ---------------------------------------------------------------------------
 // slot mapping
@@ -178,6 +189,8 @@ __global__ void __launch_bounds__(kReduceThreads)
         for (int p = lane; p < n; p += 32) mx = fmaxf(mx, __ldcg(m + p));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        // no partition holds a token (every one gave up on a wait): zeros
+        if (mx == -INFINITY) n = 0;
         for (int p = lane; p < n; p += 32) total += __ldcg(l + p) * __expf(__ldcg(m + p) - mx);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
@@ -285,6 +298,16 @@ const char *pa_status_string(pa_status status) {
 }
 
 const char *pa_last_error(void) { return g_msg; }
+
+pa_status pa_test_set_wait(uint64_t limit_ns, int stall_first_wait) {
+    clear_error();
+    if (limit_ns > 60ull * 1000000000ull)
+        return fail(PA_ERR_INVALID_ARG, "wait limit %llu ns is above 60 s",
+                    static_cast<unsigned long long>(limit_ns));
+    g_wait_limit_ns.store(limit_ns ? limit_ns : kDefaultWaitNs, std::memory_order_relaxed);
+    g_stall_first_wait.store(stall_first_wait ? 1 : 0, std::memory_order_relaxed);
+    return PA_OK;
+}
 
 pa_status pa_device_errors(unsigned int *flags, int clear) {
     clear_error();

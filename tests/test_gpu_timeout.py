@@ -1,0 +1,74 @@
+"""The decode kernel's bounded waits give up cleanly.
+
+Every wait of the decode kernel for a page copy has a time limit; when it
+runs out the kernel sets PA_DEVERR_TIMEOUT, waits (with the full limit) for
+the copies it has already issued, and finishes with zeros for the rows it
+could not compute, so a lost copy can never hang the GPU.  Here the test
+hook makes each warp's first wait go to a barrier that no copy ever
+completes, with a 1 ms limit: nothing faults and nothing hangs, the call
+returns, the flag is raised, and the next call at the default limit is
+correct against the oracle (the context is still usable)."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import compare, device_tables
+from paged_kv_cache_193_gb300 import _lib
+from paged_kv_cache_193_gb300 import workloads as W
+from test_gpu_kernels import _oracle_step
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api(cuda_device):
+    from paged_kv_cache_193_gb300 import api as a
+    a._lib_handle()
+    return a
+
+
+def _stalled(lib, fn):
+    assert lib.pa_test_set_wait(1_000_000, 1) == _lib.PA_OK
+    try:
+        out = fn()
+        torch.cuda.synchronize()
+    finally:
+        assert lib.pa_test_set_wait(0, 0) == _lib.PA_OK
+    return out
+
+
+@pytest.mark.parametrize("name,num_seqs,ps", [("tiny", None, 0), ("tiny", None, 32),
+                                              ("llama8b", 24, 0), ("llama8b", 24, 512)])
+def test_wait_runs_out_then_recovers(api, oracle, cuda_device, name, num_seqs, ps):
+    lib = _lib.load()
+    wl = W.make(name, device=cuda_device, num_seqs=num_seqs)
+    W.poison(wl, pending=True)
+    slots_ref, kc_ref, vc_ref, out_ref = _oracle_step(oracle, wl)
+    bt, cl = device_tables(wl, cuda_device)
+    api.device_errors(clear=True)
+    step = api.DecodeStep(wl.k_cache, wl.v_cache, bt, cl, wl.shape.num_q_heads,
+                          wl.softmax_scale, wl.kv_scale, ps)
+    step.out.fill_(float("nan"))
+    out = _stalled(lib, lambda: step(wl.q, wl.k_new, wl.v_new).clone())
+    flags = api.device_errors(clear=True)
+    assert flags & _lib.PA_DEVERR_TIMEOUT, hex(flags)
+    assert flags & ~_lib.PA_DEVERR_TIMEOUT == 0, hex(flags)
+    # every warp with pages gave up before reading one: all rows are zeros
+    assert torch.count_nonzero(out) == 0
+    # the append runs before any wait, so it happened all the same
+    assert np.array_equal(W.bits(wl.k_cache), kc_ref)
+    assert np.array_equal(W.bits(wl.v_cache), vc_ref)
+    # the next call, at the default limit, is correct
+    W.poison(wl, pending=True)
+    out = step(wl.q, wl.k_new, wl.v_new).clone()
+    torch.cuda.synchronize()
+    assert np.array_equal(step.slots.cpu().numpy(), slots_ref)
+    assert np.array_equal(W.bits(wl.k_cache), kc_ref)
+    compare(out, out_ref, what=f"{name} ps={ps} after a timed-out call")
+    assert api.device_errors() == 0
+
+
+def test_wait_limit_is_validated():
+    lib = _lib.load()
+    assert lib.pa_test_set_wait(61 * 10**9, 0) == _lib.PA_ERR_INVALID_ARG
+    assert lib.pa_test_set_wait(0, 0) == _lib.PA_OK
