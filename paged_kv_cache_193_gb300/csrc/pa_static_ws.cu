@@ -32,11 +32,35 @@ pa_status decode_split_into(const void *q, const void *k_cache, const void *v_ca
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) float g_static_scratch[PA_STATIC_WORKSPACE_BYTES / sizeof(float)];
 
-// Device address of g_static_scratch, resolved once per device on the first
-// call made with that device current.
+// The driver's cuCtxGetCurrent, taken from the runtime so the library needs
+// no link against libcuda.
+static CUresult current_context(CUcontext *ctx) {
+    using Fn = CUresult (*)(CUcontext *);
+    static Fn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<Fn>(p);
+    });
+    return fn ? fn(ctx) : CUDA_ERROR_NOT_FOUND;
+}
+
+// Device address of g_static_scratch in the current device's context,
+// looked up on the first call in that context.  The context handle is kept
+// beside the address: after cudaDeviceReset (or any other teardown of the
+// primary context) the module is loaded again at a possibly different
+// address, and the changed handle triggers a fresh lookup.
 static pa_status static_scratch_address(void **addr) {
     constexpr int kMaxDevices = 64;
-    static void *cache[kMaxDevices];
+    struct Entry {
+        CUcontext ctx;
+        void *ptr;
+    };
+    static Entry cache[kMaxDevices];
     static std::mutex lock;
     int dev = -1;
     pa_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
@@ -44,15 +68,23 @@ static pa_status static_scratch_address(void **addr) {
     if (dev < 0 || dev >= kMaxDevices)
         return fail(PA_ERR_UNSUPPORTED, "device ordinal %d is beyond the %d this entry point tracks",
                     dev, kMaxDevices);
+    // Before the runtime's first real call on this thread no context may be
+    // current yet (null handle); the symbol lookup creates and binds the
+    // device's primary context, after which the handle is read again.
+    CUcontext ctx = nullptr;
+    if (current_context(&ctx) != CUDA_SUCCESS)
+        return fail(PA_ERR_CUDA, "cannot read the current CUDA context");
     std::lock_guard<std::mutex> guard(lock);
-    if (!cache[dev]) {
+    if (!ctx || cache[dev].ctx != ctx || !cache[dev].ptr) {
         void *p = nullptr;
         st = cuda_check(cudaGetSymbolAddress(&p, g_static_scratch),
                         "cudaGetSymbolAddress(static scratch)");
         if (st != PA_OK) return st;
-        cache[dev] = p;
+        if (current_context(&ctx) != CUDA_SUCCESS || !ctx)
+            return fail(PA_ERR_CUDA, "cannot read the current CUDA context");
+        cache[dev] = Entry{ctx, p};
     }
-    *addr = cache[dev];
+    *addr = cache[dev].ptr;
     return PA_OK;
 }
 

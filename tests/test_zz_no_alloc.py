@@ -5,17 +5,20 @@ point keeps its scratch in a fixed array inside the library, so the call
 allocates nothing.
 
 Checked here through the C ABI: two calls in a row (with different partition
-sizes, so the second reuses the shared array the first one filled) must agree
-with pa_decode given a caller-owned workspace, and a call whose scratch would
-not fit must be refused before anything is launched.  This file is collected
-last so a failure here leaves every other test already run."""
+sizes, so the second reuses the shared array the first one filled) must give
+bit for bit what pa_decode gives with a caller-owned workspace (the same
+kernels run on the same inputs), and must match the fp64 oracle on sampled
+(sequence, query head) pairs within the attention tolerance; a call whose
+scratch would not fit must be refused before anything is launched.  This
+file is collected last so a failure here leaves every other test already
+run."""
 import ctypes
 
 import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import compare, device_tables
+from gpu_helpers import compare, device_tables, oracle_sampled
 from paged_kv_cache_193_gb300 import _lib
 from paged_kv_cache_193_gb300 import workloads as W
 
@@ -49,12 +52,22 @@ def _reference_call(lib, wl, bt, cl, ps, out, stream):
     return st
 
 
-def test_static_workspace_matches_pa_decode(cuda_device):
+def test_static_workspace_matches_pa_decode(cuda_device, oracle):
     lib = _lib.load()
     wl = W.make("llama8b", device=cuda_device, num_seqs=48)
     W.poison(wl)
     bt, cl = device_tables(wl, cuda_device)
     stream = torch.cuda.current_stream().cuda_stream
+    rng = np.random.default_rng(48)
+    sh = wl.shape
+    # every query head of four sequences (the shortest and longest among
+    # them), plus 64 random (sequence, head) pairs
+    order = np.argsort(wl.context_lens)
+    seqs = [int(order[0]), int(order[1]), int(order[-2]), int(order[-1])]
+    pairs = [(s, h) for s in seqs for h in range(sh.num_q_heads)]
+    pairs += [(int(rng.integers(sh.num_seqs)), int(rng.integers(sh.num_q_heads))) for _ in range(64)]
+    pairs = np.array(pairs, np.int32)
+    want = oracle_sampled(oracle, wl, pairs, wl.k_cache, wl.v_cache, wl.q)
     for ps in (512, 256):
         ref = torch.empty_like(wl.q)
         assert _reference_call(lib, wl, bt, cl, ps, ref, stream) == 0
@@ -62,7 +75,10 @@ def test_static_workspace_matches_pa_decode(cuda_device):
         st = _static_call(lib, wl, bt, cl, ps, out, stream)
         assert st == 0, lib.pa_last_error()
         torch.cuda.synchronize()
-        compare(out, ref.float().cpu().numpy().astype(np.float64), what=f"static scratch ps={ps}")
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"ps={ps}: differs from pa_decode"
+        sel = out[torch.from_numpy(pairs[:, 0]).long().to(cuda_device),
+                  torch.from_numpy(pairs[:, 1]).long().to(cuda_device)]
+        compare(sel, want, what=f"static scratch ps={ps} vs oracle")
     flags = ctypes.c_uint(0)
     assert lib.pa_device_errors(ctypes.byref(flags), 1) == 0 and flags.value == 0
 
