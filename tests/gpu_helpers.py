@@ -32,6 +32,57 @@ def compare(out: torch.Tensor, ref: np.ndarray, max_abs=MAX_ABS, mean_abs=MEAN_A
     return float(err.max()), float(err.mean())
 
 
+# Bytes of margin before and after each guarded buffer, and their fill: 0xFF
+# bytes read as NaN in bf16 and in fp32, and no kernel writes that pattern.
+GUARD_BYTES = 4096
+GUARD_FILL = 0xFF
+
+
+class Guarded:
+    """A device tensor of ``shape`` and ``dtype`` placed between two margins
+    of GUARD_BYTES filled with GUARD_FILL.  ``check()`` asserts that no byte
+    of either margin changed, i.e. that no kernel wrote before the start or
+    past the end of the buffer it was given (a stand-in for a memory
+    checker).  The tensor itself starts 16-byte aligned."""
+
+    def __init__(self, shape, dtype, device, fill=None):
+        self.shape = tuple(int(x) for x in shape)
+        elem = torch.empty(0, dtype=dtype).element_size()
+        self.nbytes = int(np.prod(self.shape, dtype=np.int64)) * elem
+        body = (self.nbytes + 15) // 16 * 16
+        self.raw = torch.full((GUARD_BYTES + body + GUARD_BYTES,), GUARD_FILL, dtype=torch.uint8,
+                              device=device)
+        self.tail_start = GUARD_BYTES + self.nbytes
+        self.tensor = self.raw[GUARD_BYTES:GUARD_BYTES + self.nbytes].view(dtype).view(self.shape)
+        if fill is not None:
+            self.tensor.fill_(fill)
+
+    def check(self, what=""):
+        head = self.raw[:GUARD_BYTES]
+        tail = self.raw[self.tail_start:]
+        bad_head = int((head != GUARD_FILL).sum())
+        bad_tail = int((tail != GUARD_FILL).sum())
+        assert bad_head == 0, f"{what}: {bad_head} bytes written before the buffer"
+        assert bad_tail == 0, f"{what}: {bad_tail} bytes written past the end of the buffer"
+
+
+def guard_step(step):
+    """Give a DecodeStep guarded output, slot and workspace buffers (the
+    step writes through these views); returns a function that checks every
+    margin."""
+    dev = step.out.device
+    g = {"out": Guarded(step.out.shape, step.out.dtype, dev, fill=float("nan")),
+         "slots": Guarded(step.slots.shape, torch.int32, dev, fill=-7),
+         "workspace": Guarded(step.workspace.shape, torch.uint8, dev)}
+    step.out, step.slots, step.workspace = g["out"].tensor, g["slots"].tensor, g["workspace"].tensor
+
+    def check(what=""):
+        torch.cuda.synchronize()
+        for name, buf in g.items():
+            buf.check(f"{what} {name}")
+    return check
+
+
 def device_tables(wl: W.Workload, device):
     bt = torch.from_numpy(np.ascontiguousarray(wl.block_tables)).to(device)
     cl = torch.from_numpy(np.ascontiguousarray(wl.context_lens)).to(device)

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import compact, compare, device_tables, quantize_with_torch
+from gpu_helpers import compact, compare, device_tables, guard_step, quantize_with_torch
 from paged_kv_cache_193_gb300 import workloads as W
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -76,8 +76,10 @@ def _check_step(api, oracle, wl, partition_size, n_seqs=6, heads_per_seq=6, seed
     api.device_errors(clear=True)
     step = api.DecodeStep(wl.k_cache, wl.v_cache, bt, cl, sh.num_q_heads, wl.softmax_scale,
                           wl.kv_scale, partition_size)
+    check_guards = guard_step(step)
     out = step(wl.q, wl.k_new, wl.v_new)
     torch.cuda.synchronize()
+    check_guards(f"{wl.name} B{sh.block_size} ps{partition_size}")
     assert api.device_errors() == 0
     # slots and appended rows, bit for bit
     slots = step.slots.cpu().numpy()
@@ -99,6 +101,17 @@ def test_config_sampled(api, oracle, cuda_device, name, bs, ps):
     wl = W.make(name, device=cuda_device, block_size=bs)
     if wl.shape.kv_dtype == W.KV_FP8_E4M3:
         quantize_with_torch(wl)
+    _check_step(api, oracle, wl, ps)
+
+
+@pytest.mark.parametrize("ps", [0, 512])
+def test_llama8b_e4m3_sampled(api, oracle, cuda_device, ps):
+    """The Llama-3-8B-shape layer with its cache in E4M3 (one per-tensor
+    scale), as the benchmark also times it."""
+    wl = W.make("llama8b", device=cuda_device)
+    wl.shape.kv_dtype = W.KV_FP8_E4M3
+    wl.kv_scale = W.fp8_scale_from(wl.k_cache, wl.v_cache, wl.k_new, wl.v_new)
+    quantize_with_torch(wl)
     _check_step(api, oracle, wl, ps)
 
 

@@ -1,11 +1,14 @@
-"""Decode steps captured in a CUDA graph (one graph for several layers)
-replay bit for bit like the same steps run eagerly, and read the context
-lengths and block tables afresh at every replay."""
+"""Decode steps captured in a CUDA graph (one graph for several layers):
+every replayed layer's output, slots and appended cache rows match the
+oracle, also on a later replay after the captured input buffers, the
+context lengths and the block tables were overwritten; replays are also bit
+for bit the same steps run eagerly."""
 import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import device_tables
+from gpu_helpers import compare, device_tables, guard_step
+from test_gpu_kernels import _oracle_step
 from paged_kv_cache_193_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -106,3 +109,66 @@ def test_graph_reads_buffers_at_replay(api, oracle, cuda_device):
         assert torch.equal(wl.k_cache.view(torch.int16), kc1.view(torch.int16))
         want = oracle.slot_mapping(wl.block_tables, wl.context_lens, B)
         assert np.array_equal(got_slots.cpu().numpy(), want)
+
+
+def _grow_contexts(wls, bt, cl, gen):
+    """Every sequence gains one token (a fresh block from the host allocator
+    when the token starts one; all layers share the tables), and every
+    layer's captured q / new K / new V buffers get fresh values in place."""
+    lead = wls[0]
+    B = lead.shape.block_size
+    alloc = lead.notes["allocator"]
+    ctx = lead.context_lens + 1
+    tables = lead.block_tables.copy()
+    for s in range(lead.shape.num_seqs):
+        pos = int(ctx[s]) - 1
+        if pos % B == 0:
+            tables[s, pos // B] = alloc.allocate(1)[0]
+    for wl in wls:
+        wl.context_lens = ctx.copy()
+        wl.block_tables = tables.copy()
+        for t in (wl.q, wl.k_new, wl.v_new):
+            t.copy_(torch.randn(t.shape, generator=gen, device=t.device))
+        W.poison(wl, pending=True)
+    bt.copy_(torch.from_numpy(tables))
+    cl.copy_(torch.from_numpy(ctx))
+
+
+@pytest.mark.parametrize("name,num_seqs,layers,ps", [("tiny", None, 4, 0), ("tiny", None, 4, 32),
+                                                     ("llama8b", 16, 2, 0), ("llama8b", 16, 2, 512)])
+def test_graph_replay_matches_oracle(api, oracle, cuda_device, name, num_seqs, layers, ps):
+    wls = []
+    for i in range(layers):
+        wl = W.make(name, device=cuda_device, num_seqs=num_seqs, data_seed=20 + i, extra_steps=2)
+        W.poison(wl, pending=True)
+        wls.append(wl)
+    bt, cl = device_tables(wls[0], cuda_device)  # one set of tables for all layers
+    refs = [_oracle_step(oracle, wl) for wl in wls]
+    before = [(wl.k_cache.clone(), wl.v_cache.clone()) for wl in wls]
+    steps = [api.DecodeStep(wl.k_cache, wl.v_cache, bt, cl, wl.shape.num_q_heads, wl.softmax_scale,
+                            wl.kv_scale, ps) for wl in wls]
+    guards = [guard_step(st) for st in steps]
+    g = api.StepGraph(steps, [(wl.q, wl.k_new, wl.v_new) for wl in wls])
+    # the capture's eager warm-up appended once: go back to the state the
+    # oracle saw
+    for st, (kc, vc) in zip(steps, before):
+        st.k_cache.copy_(kc)
+        st.v_cache.copy_(vc)
+        st.out.fill_(float("nan"))
+        st.slots.fill_(-7)
+    gen = torch.Generator(device=cuda_device).manual_seed(99)
+    api.device_errors(clear=True)
+    for replay in range(2):
+        if replay:
+            _grow_contexts(wls, bt, cl, gen)
+            refs = [_oracle_step(oracle, wl) for wl in wls]
+        g.replay()
+        torch.cuda.synchronize()
+        for i, (st, wl, (slots_ref, kc_ref, vc_ref, out_ref)) in enumerate(zip(steps, wls, refs)):
+            what = f"{name} ps={ps} replay {replay} layer {i}"
+            guards[i](what)
+            assert np.array_equal(st.slots.cpu().numpy(), slots_ref), what
+            assert np.array_equal(W.bits(st.k_cache), kc_ref), what
+            assert np.array_equal(W.bits(st.v_cache), vc_ref), what
+            compare(st.out, out_ref, what=what)
+    assert api.device_errors() == 0

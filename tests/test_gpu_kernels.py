@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import compare, device_tables, quantize_with_oracle, bf16_to_f64
+from gpu_helpers import bf16_to_f64, compare, device_tables, guard_step, quantize_with_oracle
 from paged_cases import bits_to_f64
 from paged_kv_cache_193_gb300 import workloads as W
 
@@ -54,8 +54,10 @@ def _gpu_step(api, wl, partition_size, fused=True):
     bt, cl = device_tables(wl, wl.k_cache.device)
     step = api.DecodeStep(wl.k_cache, wl.v_cache, bt, cl, wl.shape.num_q_heads,
                           wl.softmax_scale, wl.kv_scale, partition_size, fused=fused)
+    check_guards = guard_step(step)
     out = step(wl.q, wl.k_new, wl.v_new).clone()
     torch.cuda.synchronize()
+    check_guards(f"decode step ps={partition_size} fused={fused}")
     return step.slots.cpu().numpy(), out
 
 

@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import compare
+from gpu_helpers import Guarded, compare
 from paged_kv_cache_193_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -34,11 +34,15 @@ def _oracle_step(oracle, wl):
 
 def _gpu_step(api, wl, device, kernel="auto"):
     bt, cl, qs = _dev(wl, device)
-    slots = api.chunk_slot_mapping(bt, cl, qs, wl.shape.block_size)
+    g_slots = Guarded((int(wl.query_start[-1]),), torch.int32, device, fill=-7)
+    g_out = Guarded(wl.q.shape, torch.bfloat16, device, fill=float("nan"))
+    slots = api.chunk_slot_mapping(bt, cl, qs, wl.shape.block_size, out=g_slots.tensor)
     api.cache_append(wl.k_new, wl.v_new, slots, wl.k_cache, wl.v_cache)
     out = api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, wl.max_query_len, wl.softmax_scale,
-                      kernel=kernel)
+                      out=g_out.tensor, kernel=kernel)
     torch.cuda.synchronize()
+    g_slots.check(f"prefill {kernel} chunk slots")
+    g_out.check(f"prefill {kernel} out")
     return slots.cpu().numpy(), out
 
 
