@@ -55,6 +55,16 @@ DESCRIPTION = {
     "ctx128k": "405B-head 128K context: 8 seqs x 131072 tokens, 128q/8kv heads, head_dim 128, "
                "block 16, bf16 KV, split context + log-sum-exp merge",
 }
+# Workloads the default run times after the headline one, with the same
+# protocol: (label, workload, block size, partition size, E4M3 cache).
+SECONDARY = [
+    ("long70b_B16_P512", "long70b", 16, 512, False),
+    ("long70b_B32_P512", "long70b", 32, 512, False),
+    ("ctx128k_P512", "ctx128k", 16, 512, False),
+    ("ctx128k_P2048", "ctx128k", 16, 2048, False),
+    ("prefix_fp8", "prefix_fp8", 16, 0, False),
+    ("llama8b_e4m3", "llama8b", 16, 0, True),
+]
 DECODE_SOURCES = ["paged_kv_cache_193_gb300/csrc/pa_decode.cu",
                   "paged_kv_cache_193_gb300/csrc/pa_device.cuh"]
 
@@ -89,6 +99,12 @@ def parse():
     ap.add_argument("--kv-heads", type=int, default=8, help="prefill: KV heads (default 8)")
     ap.add_argument("--separate", action="store_true",
                     help="time the unfused entry points (3-4 kernels per step)")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the other workloads the default run also times (long70b at "
+                         "16/32-token pages, ctx128k at 512/2048-token partitions, prefix_fp8, "
+                         "llama8b with the E4M3 cache)")
+    ap.add_argument("--secondary-steps", type=int, default=200,
+                    help="timed steps of each secondary workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--min-warmup-seconds", type=float, default=1.0,
@@ -575,7 +591,9 @@ def run_ours(args):
                      "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "algorithmic_bytes_per_launch": kv_launch, "traffic": traffic},
+                     "algorithmic_bytes_per_launch": kv_launch, "traffic": traffic,
+                     "statistic": "algorithmic bytes / mean of the kernel's per-launch "
+                                  "CUDA-event durations"},
     }
     result["clocks"] = clocks.summary(t_wall0 - 1.0, t_wall1)
 
@@ -583,10 +601,112 @@ def run_ours(args):
         result["e2e"] = run_e2e(api, wl, step, ps, K, world, device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.device_alloc:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if default_run(args):
+        del steps, inputs, layers, step, wl
+        torch.cuda.empty_cache()
+        result["secondary"] = {label: time_secondary(api, label, name, bs, ps, fp8, args, world, local,
+                                                     device, hbm)
+                               for label, name, bs, ps, fp8 in SECONDARY}
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def default_run(args) -> bool:
+    """The plain headline run (no variant flags): it also times SECONDARY."""
+    return (not args.no_secondary and args.config == "llama8b" and not args.fp8 and not args.graph
+            and args.layers == 1 and not args.per_head_scales and not args.fp8_qk
+            and not args.device_alloc and not args.separate and args.num_seqs is None
+            and args.block_size is None and args.partition_size is None)
+
+
+def time_secondary(api, label, name, bs, ps, fp8, args, world, local, device, hbm):
+    """One more workload with the headline's protocol: fused step (slot
+    mapping + append + attention, merge when split), warm-up of at least
+    0.3 s, then ``--secondary-steps`` steps timed with CUDA events between
+    barriers; the attention kernel timed alone the same way as the
+    headline's; clocks sampled over the timed region."""
+    wl = W.make(name, device=device, block_size=bs)
+    if fp8 and wl.shape.kv_dtype != W.KV_FP8_E4M3:
+        wl.shape.kv_dtype = W.KV_FP8_E4M3
+        wl.kv_scale = W.fp8_scale_from(wl.k_cache, wl.v_cache, wl.k_new, wl.v_new)
+    if wl.shape.kv_dtype == W.KV_FP8_E4M3:
+        quantize_fp8_pool(api, wl)
+        wl.notes.pop("bf16_pool", None)
+    sh = wl.shape
+    bt = torch.from_numpy(wl.block_tables).to(device)
+    cl = torch.from_numpy(wl.context_lens).to(device)
+    step = api.DecodeStep(wl.k_cache, wl.v_cache, bt, cl, sh.num_q_heads, wl.softmax_scale,
+                          wl.kv_scale, ps)
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    clocks.start()
+    api.device_errors(clear=True)
+    t_w, done = time.time(), 0
+    while done < args.warmup or time.time() - t_w < 0.3:
+        step(wl.q, wl.k_new, wl.v_new)
+        done += 1
+        if done % 50 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    K = args.secondary_steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        step(wl.q, wl.k_new, wl.v_new)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    total_ms = max_over_ranks(start.elapsed_time(end), world, device)
+    t_step = np.array([a.elapsed_time(b) for a, b in ev])
+    if ps == 0:
+        dec_ms, red_ms = float(np.mean(t_step)), 0.0
+    else:
+        e = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(min(K, 100))]
+        for x in e:
+            x[0].record(stream)
+            api.decode_partitions(wl.q, wl.k_cache, wl.v_cache, bt, cl, wl.softmax_scale,
+                                  wl.kv_scale, ps, step.workspace)
+            x[1].record(stream)
+            api.decode_reduce(step.workspace, cl, sh.num_q_heads, sh.head_dim, bt.shape[1],
+                              sh.block_size, ps, step.out)
+            x[2].record(stream)
+        torch.cuda.synchronize()
+        dec_ms = float(np.mean([x[0].elapsed_time(x[1]) for x in e]))
+        red_ms = float(np.mean([x[1].elapsed_time(x[2]) for x in e]))
+    clocks.stop()
+    assert api.device_errors() == 0, f"device error flags raised on {label}"
+    kv = wl.kv_bytes()
+    value = world * kv * K / (total_ms / 1e3) / 1e9
+    achieved = kv / (dec_ms / 1e3) / 1e9
+    res = {
+        "workload": f"{name}: {DESCRIPTION[name]}" + ("; E4M3 cache, one scale" if fp8 else ""),
+        "block_size": sh.block_size, "partition_size": ps,
+        "kv_dtype": "bf16" if sh.kv_dtype == W.KV_BF16 else "fp8_e4m3, one scale",
+        "kv_bytes_per_step": kv, "unique_kv_bytes_per_step": wl.unique_kv_bytes(),
+        "value": round(value, 2), "unit": "GB/s", "steps": K, "ms_per_step": round(total_ms / K, 5),
+        "step_median_ms": round(float(np.median(t_step)), 5),
+        "decode_kernel_ms": round(dec_ms, 5), "merge_kernel_ms": round(red_ms, 5),
+        "decode_kernel_gbs": round(achieved, 1), "frac": round(achieved / hbm, 4),
+        "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "tokens_per_s": round(world * sh.num_seqs * K / (total_ms / 1e3), 1),
+        "gpu_launches": K * step.launches(),
+        "clocks": clocks.summary(t0 - 1.0, t1),
+    }
+    if name == "prefix_fp8":
+        res["note"] = "logical bytes; the 2048-token shared prefix is read from L2 by design"
+    del step, wl, bt, cl
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_e2e(api, wl, step, ps, K, world, device):
