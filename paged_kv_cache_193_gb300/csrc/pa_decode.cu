@@ -87,14 +87,18 @@ struct Cfg {
     static constexpr int SLAB = ROWB >= 128 ? 128 : ROWB;     // TMA box width in bytes = swizzle span
     static constexpr int NSLAB = ROWB / SLAB;
     static constexpr int PAGE = BS * ROWB;                    // one K (or V) page of one head
-    static constexpr int STAGE = 2 * PAGE;                    // K page, then V page
+    // pages per iteration of a warp: two 16-token E4M3 pages (32 tokens per
+    // pass amortise the per-pass work over twice the bytes), else one
+    static constexpr int PPI = (FP8 && BS == 16) ? 2 : 1;
+    static constexpr int STAGE = 2 * PPI * PAGE;              // PPI K pages, then PPI V pages
     static constexpr int NSTAGE = NW * SPW;
     static constexpr int RING = NSTAGE * STAGE;
     static constexpr int NP = 8 * NT;                         // group rows padded to the MMA N
     static constexpr int OSTR = D + 4;                        // epilogue row stride (floats)
-    static constexpr int EPI = (NW * NP * OSTR + 3 * NW * NP + 2 * NP) * 4;
+    static constexpr int EPI = (NW * NP * OSTR + 4 * NW * NP + 2 * NP) * 4;
     static constexpr int SMEM = (RING > EPI ? RING : EPI) + 1024;  // + 1 KB for base alignment
     static constexpr int MT = BS / 16;                        // 16-token m-tiles per page
+    static constexpr int MI = PPI * MT;                       // m-tiles per iteration
     static constexpr int KSTEPS = D / 16;
     static constexpr int DT = D / 16;                         // 16-dim tiles of the output
     static constexpr int CPT = D / 64;                        // fp8: 16-byte chunks per thread and row
@@ -250,7 +254,11 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
     __syncthreads();
 
     // ---- this warp's pages ----------------------------------------------------
+    // The warp owns pages warp, warp + NW, ...; iteration i takes its pages
+    // PPI*i .. PPI*i + PPI - 1 (MI m-tiles of 16 tokens) from one stage.
+    constexpr int PPI = C::PPI, MI = C::MI;
     const int my_pages = npages > warp ? (npages - warp + NW - 1) / NW : 0;
+    const int my_iters = (my_pages + PPI - 1) / PPI;
     int chunk_cur = 0;
     const uint64_t policy = l2_evict_first_policy();
     const int rows_total = a.num_blocks * a.num_kv_heads * BS;
@@ -266,32 +274,42 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
         }
         return __shfl_sync(0xffffffffu, ent_cur, k & 31);
     };
-    // Lane 0: start the copies of the warp's k-th page (physical block blk).
-    auto issue = [&](int k, int blk) {
-        const int st = warp * SPW + k % SPW;
+    // All lanes: the physical blocks of iteration it's pages; lane 0 starts
+    // their copies (pages past the warp's last are not copied: their rows
+    // are masked and their V rows zeroed before use).
+    auto fetch = [&](int it) {
+        int blk[PPI];
+#pragma unroll
+        for (int p = 0; p < PPI; ++p) blk[p] = entry(PPI * it + p);
+        if (lane != 0) return;
+        const int st = warp * SPW + it % SPW;
         const uint32_t bar = smem_addr(&bars[st]);
         const uint32_t kdst = ring + st * C::STAGE;
-        const uint32_t vdst = kdst + C::PAGE;
-        int y;
-        if (blk < 0 || blk >= a.num_blocks) {
-            set_device_error(a.err, PA_DEVERR_BAD_BLOCK);
-            y = rows_total;  // wholly outside the tensor: the TMA fills zeros
-        } else {
-            y = (blk * a.num_kv_heads + h) * BS;
-        }
-        mbar_arrive_expect_tx(bar, C::STAGE);
+        const uint32_t vdst = kdst + PPI * C::PAGE;
+        const int live = min(PPI, my_pages - PPI * it);
+        mbar_arrive_expect_tx(bar, live * 2 * C::PAGE);
 #pragma unroll
-        for (int sl = 0; sl < C::NSLAB; ++sl) {
-            tma_load_2d(kdst + sl * (BS * C::SLAB), &tmK, sl * (C::SLAB / C::ELEM), y, bar, policy);
-            tma_load_2d(vdst + sl * (BS * C::SLAB), &tmV, sl * (C::SLAB / C::ELEM), y, bar, policy);
+        for (int p = 0; p < PPI; ++p) {
+            if (p >= live) break;
+            int y;
+            if (blk[p] < 0 || blk[p] >= a.num_blocks) {
+                set_device_error(a.err, PA_DEVERR_BAD_BLOCK);
+                y = rows_total;  // wholly outside the tensor: the TMA fills zeros
+            } else {
+                y = (blk[p] * a.num_kv_heads + h) * BS;
+            }
+#pragma unroll
+            for (int sl = 0; sl < C::NSLAB; ++sl) {
+                tma_load_2d(kdst + p * C::PAGE + sl * (BS * C::SLAB), &tmK, sl * (C::SLAB / C::ELEM),
+                            y, bar, policy);
+                tma_load_2d(vdst + p * C::PAGE + sl * (BS * C::SLAB), &tmV, sl * (C::SLAB / C::ELEM),
+                            y, bar, policy);
+            }
         }
     };
 
-    const int prolog = my_pages < SPW ? my_pages : SPW;
-    for (int k = 0; k < prolog; ++k) {
-        const int blk = entry(k);
-        if (lane == 0) issue(k, blk);
-    }
+    const int prolog = my_iters < SPW ? my_iters : SPW;
+    for (int it = 0; it < prolog; ++it) fetch(it);
 
     float o[C::DT][NT][4];
 #pragma unroll
@@ -300,79 +318,107 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) o[dt][nt][e] = 0.f;
-    float m_run[NT][2], l_run[NT][2];
+    // Per group column: m_ref is the reference the probabilities are taken
+    // against (it moves only when a tile's maximum exceeds it by more than
+    // kLazy in base-2 units, so probabilities stay below 2^kLazy and the
+    // accumulator is rescaled rarely), m_max the true running maximum, l
+    // the sum of probabilities relative to m_ref.
+    constexpr float kLazy = 8.f;
+    float m_ref[NT][2], m_max[NT][2], l_run[NT][2];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        m_run[nt][0] = m_run[nt][1] = -INFINITY;
-        l_run[nt][0] = l_run[nt][1] = 0.f;
-    }
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            m_ref[nt][j] = m_max[nt][j] = -INFINITY;
+            l_run[nt][j] = 0.f;
+        }
+
+    // Token (within its 16-token m-tile) of MMA row r and of row r + 8.  The
+    // E4M3 path reads V with a transposing byte-matrix load whose fragment
+    // pairs rows 4c, 4c+1 and 4c+2, 4c+3; the sum over tokens is
+    // order-free, so the scores take the matching order: MMA row 2c + e + 8h
+    // holds token 4c + 2h + e.
+    const int tok_r = FP8 ? (r >> 1) * 4 + (r & 1) : r;
+    const int tok_dh = FP8 ? 2 : 8;
 
     // ---- main loop over this warp's pages ---------------------------------
     bool ok = true;
-    int k_fail = 0;
+    int it_fail = 0;
     // Test hook: give up on a barrier that no copy completes, exactly as if
     // the first page never arrived (the copies already issued still land
     // and are drained below).
-    if (a.stall_first_wait && my_pages > 0)
+    if (a.stall_first_wait && my_iters > 0)
         ok = mbar_wait_bounded(smem_addr(&stall_bar), 0, a.wait_limit_ns);
-    for (int k = 0; ok && k < my_pages; ++k) {
-        const int st = warp * SPW + k % SPW;
-        if (!mbar_wait_bounded(smem_addr(&bars[st]), (k / SPW) & 1, a.wait_limit_ns)) {
+    for (int it = 0; ok && it < my_iters; ++it) {
+        const int st = warp * SPW + it % SPW;
+        if (!mbar_wait_bounded(smem_addr(&bars[st]), (it / SPW) & 1, a.wait_limit_ns)) {
             ok = false;
-            k_fail = k;
+            it_fail = it;
             break;
         }
         const uint32_t kbase = ring + st * C::STAGE;
-        const uint32_t vbase = kbase + C::PAGE;
-        const int tok0 = (page0 + warp + k * NW) * BS;
-        const int valid = min(BS, t_end - tok0);
+        const uint32_t vbase = kbase + PPI * C::PAGE;
+        int valid[PPI];
+#pragma unroll
+        for (int p = 0; p < PPI; ++p) {
+            const int k = PPI * it + p;
+            const int tok0 = (page0 + warp + k * NW) * BS;
+            valid[p] = k < my_pages ? min(BS, t_end - tok0) : 0;
+        }
 
-        if (valid < BS) {
-            // Rows past the context hold whatever the pool held (never read
+        if (valid[PPI - 1] < BS) {
+            // Rows past the context hold whatever the stage held (never read
             // as tokens): zero the V rows so 0-probability x garbage is 0.
             constexpr int CH = C::NSLAB * (C::SLAB / 16);
-            for (int i = lane; i < (BS - valid) * CH; i += 32) {
-                const int row = valid + i / CH;
-                const int rem = i % CH;
-                sts128_zero(vbase + (rem / (C::SLAB / 16)) * (BS * C::SLAB) + row * C::SLAB +
-                            (rem % (C::SLAB / 16)) * 16);
+#pragma unroll
+            for (int p = 0; p < PPI; ++p) {
+                const uint32_t vb = vbase + p * C::PAGE;
+                for (int i = lane; i < (BS - valid[p]) * CH; i += 32) {
+                    const int row = valid[p] + i / CH;
+                    const int rem = i % CH;
+                    sts128_zero(vb + (rem / (C::SLAB / 16)) * (BS * C::SLAB) + row * C::SLAB +
+                                (rem % (C::SLAB / 16)) * 16);
+                }
             }
             __syncwarp();
         }
 
-        // S^T[t][g] for the page's tokens
-        float sc[C::MT][NT][4];
+        // S^T[t][g] for the iteration's tokens; m-tile mi is m-tile mi % MT
+        // of page mi / MT
+        float sc[MI][NT][4];
 #pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt)
+        for (int mi = 0; mi < MI; ++mi)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
+                for (int e = 0; e < 4; ++e) sc[mi][nt][e] = 0.f;
 
         if constexpr (!FP8) {
 #pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) {
-                const int t = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            for (int mi = 0; mi < MI; ++mi) {
+                const uint32_t kb = kbase + (mi / C::MT) * C::PAGE;
+                const int t = (mi % C::MT) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
                 for (int kk = 0; kk < C::KSTEPS; ++kk) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4(swz<C, BS>(kbase, t, (kk * 16 + (lane >> 4) * 8) * 2), a0, a1, a2, a3);
+                    ldsm_x4(swz<C, BS>(kb, t, (kk * 16 + (lane >> 4) * 8) * 2), a0, a1, a2, a3);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
-                        mma16816<false>(sc[mt][nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
+                        mma16816<false>(sc[mi][nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
                 }
             }
         } else if constexpr (FQ) {
             // E4M3 x E4M3: this thread's 8 bytes of a row per 32-dim step are
             // A fragment words as they lie in shared memory
 #pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) {
-                const int t0 = mt * 16 + r, t1 = t0 + 8;
+            for (int mi = 0; mi < MI; ++mi) {
+                const uint32_t kb = kbase + (mi / C::MT) * C::PAGE;
+                const int t0 = (mi % C::MT) * 16 + tok_r, t1 = t0 + tok_dh;
                 uint4 ra[C::CPT], rb[C::CPT];
 #pragma unroll
                 for (int j = 0; j < C::CPT; ++j) {
-                    ra[j] = lds128(swz<C, BS>(kbase, t0, (c * C::CPT + j) * 16));
-                    rb[j] = lds128(swz<C, BS>(kbase, t1, (c * C::CPT + j) * 16));
+                    ra[j] = lds128(swz<C, BS>(kb, t0, (c * C::CPT + j) * 16));
+                    rb[j] = lds128(swz<C, BS>(kb, t1, (c * C::CPT + j) * 16));
                 }
                 auto word = [](const uint4 &u, int i) { return i == 0 ? u.x : i == 1 ? u.y : i == 2 ? u.z : u.w; };
 #pragma unroll
@@ -382,18 +428,19 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
                     const uint32_t a1 = word(rb[w / 4], w % 4), a3 = word(rb[w / 4], w % 4 + 1);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
-                        mma16832_e4m3(sc[mt][nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
+                        mma16832_e4m3(sc[mi][nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
                 }
             }
         } else {
 #pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) {
-                const int t0 = mt * 16 + r, t1 = t0 + 8;
+            for (int mi = 0; mi < MI; ++mi) {
+                const uint32_t kb = kbase + (mi / C::MT) * C::PAGE;
+                const int t0 = (mi % C::MT) * 16 + tok_r, t1 = t0 + tok_dh;
                 uint4 ra[C::CPT], rb[C::CPT];
 #pragma unroll
                 for (int j = 0; j < C::CPT; ++j) {
-                    ra[j] = lds128(swz<C, BS>(kbase, t0, (c * C::CPT + j) * 16));
-                    rb[j] = lds128(swz<C, BS>(kbase, t1, (c * C::CPT + j) * 16));
+                    ra[j] = lds128(swz<C, BS>(kb, t0, (c * C::CPT + j) * 16));
+                    rb[j] = lds128(swz<C, BS>(kb, t1, (c * C::CPT + j) * 16));
                 }
 #pragma unroll
                 for (int kk = 0; kk < C::KSTEPS; ++kk) {
@@ -406,119 +453,141 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
                     e4m3x4_to_f16x2x2(wb, a1, a3);  // row t1
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
-                        mma16816<true>(sc[mt][nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
+                        mma16816<true>(sc[mi][nt], a0, a1, a2, a3, qf[kk][nt][0], qf[kk][nt][1]);
                 }
             }
         }
 
-        // online softmax over the page's tokens, per group column
-        uint32_t pb[C::MT][NT][2];
+        // online softmax over the iteration's tokens, per group column
+        float mx[NT][2];
+        bool grow = false;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                float mx = -INFINITY;
+                float m = -INFINITY;
 #pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) {
+                for (int mi = 0; mi < MI; ++mi) {
+                    const int lim = valid[mi / C::MT] - (mi % C::MT) * 16;
 #pragma unroll
                     for (int hi = 0; hi < 2; ++hi) {
-                        const int row = mt * 16 + r + hi * 8;
-                        float x = sc[mt][nt][hi * 2 + j] * score_scale;
-                        x = row < valid ? x : -INFINITY;
-                        sc[mt][nt][hi * 2 + j] = x;
-                        mx = fmaxf(mx, x);
+                        float x = sc[mi][nt][hi * 2 + j] * score_scale;
+                        x = tok_r + hi * tok_dh < lim ? x : -INFINITY;
+                        sc[mi][nt][hi * 2 + j] = x;
+                        m = fmaxf(m, x);
                     }
                 }
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float m_new = fmaxf(m_run[nt][j], mx);
-                const float alpha = fast_exp2(m_run[nt][j] - m_new);
-                m_run[nt][j] = m_new;
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                mx[nt][j] = m;
+                m_max[nt][j] = fmaxf(m_max[nt][j], m);
+                grow |= m > m_ref[nt][j] + kLazy;
+            }
+        }
+        if (__any_sync(0xffffffffu, grow)) {
+            // move the reference to the running maximum and rescale
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float m_new = fmaxf(m_ref[nt][j], mx[nt][j]);
+                    const float alpha = fast_exp2(m_ref[nt][j] - m_new);
+                    m_ref[nt][j] = m_new;
+                    l_run[nt][j] *= alpha;
+#pragma unroll
+                    for (int dt = 0; dt < C::DT; ++dt) {
+                        o[dt][nt][j] *= alpha;
+                        o[dt][nt][j + 2] *= alpha;
+                    }
+                }
+        }
+        uint32_t pb[MI][NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
                 float sum = 0.f;
 #pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) {
+                for (int mi = 0; mi < MI; ++mi) {
 #pragma unroll
                     for (int hi = 0; hi < 2; ++hi) {
-                        const float pr = fast_exp2(sc[mt][nt][hi * 2 + j] - m_new);
-                        sc[mt][nt][hi * 2 + j] = pr;
+                        const float pr = fast_exp2(sc[mi][nt][hi * 2 + j] - m_ref[nt][j]);
+                        sc[mi][nt][hi * 2 + j] = pr;
                         sum += pr;
                     }
                 }
-                l_run[nt][j] = l_run[nt][j] * alpha + sum;
-#pragma unroll
-                for (int dt = 0; dt < C::DT; ++dt) {
-                    o[dt][nt][j] *= alpha;
-                    o[dt][nt][j + 2] *= alpha;
-                }
+                l_run[nt][j] += sum;
             }
 #pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) {
-                pb[mt][nt][0] = movmatrix_trans(pack2<FP8>(sc[mt][nt][0], sc[mt][nt][1]));
-                pb[mt][nt][1] = movmatrix_trans(pack2<FP8>(sc[mt][nt][2], sc[mt][nt][3]));
+            for (int mi = 0; mi < MI; ++mi) {
+                pb[mi][nt][0] = movmatrix_trans(pack2<FP8>(sc[mi][nt][0], sc[mi][nt][1]));
+                pb[mi][nt][1] = movmatrix_trans(pack2<FP8>(sc[mi][nt][2], sc[mi][nt][3]));
             }
         }
 
         // O^T += V^T P^T
         if constexpr (!FP8) {
 #pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) {
-                const int t = mt * 16 + (lane & 7) + (lane >> 4) * 8;
+            for (int mi = 0; mi < MI; ++mi) {
+                const uint32_t vb = vbase + (mi / C::MT) * C::PAGE;
+                const int t = (mi % C::MT) * 16 + (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
                 for (int dt = 0; dt < C::DT; ++dt) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4_trans(swz<C, BS>(vbase, t, (dt * 16 + ((lane >> 3) & 1) * 8) * 2), a0, a1,
+                    ldsm_x4_trans(swz<C, BS>(vb, t, (dt * 16 + ((lane >> 3) & 1) * 8) * 2), a0, a1,
                                   a2, a3);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
-                        mma16816<false>(o[dt][nt], a0, a1, a2, a3, pb[mt][nt][0], pb[mt][nt][1]);
+                        mma16816<false>(o[dt][nt], a0, a1, a2, a3, pb[mi][nt][0], pb[mi][nt][1]);
                 }
             }
         } else {
+            // Byte matrices of 16 tokens x 16 head dims, transposed: this
+            // thread gets tokens 4c..4c+3 of dims r and r + 8, which widen to
+            // the A fragment for MMA rows (2c, 2c+1 | 2c+8, 2c+9) = tokens
+            // (4c, 4c+1 | 4c+2, 4c+3), the order the scores took.
 #pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) {
-                const int tb = mt * 16 + 2 * c;
+            for (int mi = 0; mi < MI; ++mi) {
+                const uint32_t vb = vbase + (mi / C::MT) * C::PAGE;
+                const int t = (mi % C::MT) * 16 + (lane & 15);
 #pragma unroll
-                for (int gi = 0; gi < D / 32; ++gi) {
-                    const int b = gi * 32 + 4 * r;
-                    const uint32_t w0 = lds32(swz<C, BS>(vbase, tb, b));
-                    const uint32_t w1 = lds32(swz<C, BS>(vbase, tb + 1, b));
-                    const uint32_t w2 = lds32(swz<C, BS>(vbase, tb + 8, b));
-                    const uint32_t w3 = lds32(swz<C, BS>(vbase, tb + 9, b));
+                for (int cp = 0; cp < D / 32; ++cp) {
+                    uint32_t w0, w1, w2, w3;
+                    ldsm_x2_trans_b8(swz<C, BS>(vb, t, (2 * cp + (lane >> 4)) * 16), w0, w1, w2, w3);
+                    uint32_t a0, a1, a2, a3;
+                    e4m3x4_to_f16x2x2(w0, a0, a2);
+                    e4m3x4_to_f16x2x2(w1, a1, a3);
 #pragma unroll
-                    for (int mu = 0; mu < 2; ++mu) {
-                        const uint32_t sel = mu ? 0x7362u : 0x5140u;
-                        uint32_t a0, a1, a2, a3;
-                        e4m3x4_to_f16x2x2(__byte_perm(w0, w1, sel), a0, a1);
-                        e4m3x4_to_f16x2x2(__byte_perm(w2, w3, sel), a2, a3);
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma16816<true>(o[2 * cp][nt], a0, a1, a2, a3, pb[mi][nt][0], pb[mi][nt][1]);
+                    e4m3x4_to_f16x2x2(w2, a0, a2);
+                    e4m3x4_to_f16x2x2(w3, a1, a3);
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            mma16816<true>(o[gi * 2 + mu][nt], a0, a1, a2, a3, pb[mt][nt][0],
-                                           pb[mt][nt][1]);
-                    }
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma16816<true>(o[2 * cp + 1][nt], a0, a1, a2, a3, pb[mi][nt][0],
+                                       pb[mi][nt][1]);
                 }
             }
         }
 
-        // hand the stage back to the TMA: refill with the page SPW ahead
+        // hand the stage back to the TMA: refill with the iteration SPW ahead
         __syncwarp();
         fence_proxy_async_smem();
         __syncwarp();
-        if (k + SPW < my_pages) {
-            const int blk = entry(k + SPW);
-            if (lane == 0) issue(k + SPW, blk);
-        }
+        if (it + SPW < my_iters) fetch(it + SPW);
     }
     if (!ok) {
         // A copy never arrived: flag it, wait (bounded) for the copies still
         // in flight into this warp's stages, and fall through with zeros.
         if (lane == 0) set_device_error(a.err, PA_DEVERR_TIMEOUT);
-        const int issued = min(my_pages, k_fail + SPW);
-        for (int k = k_fail; k < issued; ++k)
-            mbar_wait_bounded(smem_addr(&bars[warp * SPW + k % SPW]), (k / SPW) & 1, kWaitLimitNs);
+        const int issued = min(my_iters, it_fail + SPW);
+        for (int it = it_fail; it < issued; ++it)
+            mbar_wait_bounded(smem_addr(&bars[warp * SPW + it % SPW]), (it / SPW) & 1, kWaitLimitNs);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            m_run[nt][0] = m_run[nt][1] = -INFINITY;
+            m_ref[nt][0] = m_ref[nt][1] = -INFINITY;
+            m_max[nt][0] = m_max[nt][1] = -INFINITY;
             l_run[nt][0] = l_run[nt][1] = 0.f;
         }
     }
@@ -536,10 +605,11 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
         }
     __syncthreads();  // every warp is done with the page ring
     float *osm = epi;                               // [NW][NP][OSTR]
-    float *msm = osm + NW * C::NP * C::OSTR;        // [NW][NP]
+    float *msm = osm + NW * C::NP * C::OSTR;        // [NW][NP] reference maxima
     float *lsm = msm + NW * C::NP;                  // [NW][NP]
-    float *wsm = lsm + NW * C::NP;                  // [NW][NP]
-    float *fin = wsm + NW * C::NP;                  // [2][NP]: M, L
+    float *xsm = lsm + NW * C::NP;                  // [NW][NP] true maxima
+    float *wsm = xsm + NW * C::NP;                  // [NW][NP]
+    float *fin = wsm + NW * C::NP;                  // [2][NP]: true max, sum relative to it
 #pragma unroll
     for (int dt = 0; dt < C::DT; ++dt) {
 #pragma unroll
@@ -547,11 +617,7 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int g = nt * 8 + 2 * c + (e & 1);
-                int d;
-                if constexpr (!FP8)
-                    d = dt * 16 + r + (e >> 1) * 8;
-                else
-                    d = (dt >> 1) * 32 + 4 * r + 2 * (dt & 1) + (e >> 1);
+                const int d = dt * 16 + r + (e >> 1) * 8;
                 osm[(warp * C::NP + g) * C::OSTR + d] = o[dt][nt][e];
             }
         }
@@ -562,16 +628,20 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int g = nt * 8 + 2 * c + j;
-                msm[warp * C::NP + g] = m_run[nt][j];
+                msm[warp * C::NP + g] = m_ref[nt][j];
                 lsm[warp * C::NP + g] = l_run[nt][j];
+                xsm[warp * C::NP + g] = m_max[nt][j];
             }
     }
     __syncthreads();
     if (tid < C::NP) {
         const int g = tid;
-        float M = -INFINITY;
+        float M = -INFINITY, X = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, msm[w * C::NP + g]);
+        for (int w = 0; w < NW; ++w) {
+            M = fmaxf(M, msm[w * C::NP + g]);
+            X = fmaxf(X, xsm[w * C::NP + g]);
+        }
         float L = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
@@ -581,8 +651,9 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
 #pragma unroll
         for (int w = 0; w < NW; ++w)
             wsm[w * C::NP + g] = L > 0.f ? fast_exp2(msm[w * C::NP + g] - M) * inv : 0.f;
-        fin[g] = M;
-        fin[C::NP + g] = L;
+        // the workspace holds the true maximum and the sum relative to it
+        fin[g] = X;
+        fin[C::NP + g] = L > 0.f ? L * fast_exp2(M - X) : 0.f;
     }
     __syncthreads();
 
@@ -663,7 +734,8 @@ constexpr int kRingBytes = PA_DECODE_RING_KB * 1024;
 
 template <int D, int BS, bool FP8>
 constexpr int stages_per_warp() {
-    constexpr int stage = 2 * BS * D * (FP8 ? 1 : 2);
+    constexpr int ppi = (FP8 && BS == 16) ? 2 : 1;  // Cfg::PPI
+    constexpr int stage = 2 * ppi * BS * D * (FP8 ? 1 : 2);
     constexpr int spw = kRingBytes / (kWarps * stage);
     return spw < 1 ? 1 : spw;
 }

@@ -152,6 +152,19 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint3
                  : "memory");
 }
 
+// Two 16 x 16 matrices of bytes, transposed: lanes 0-15 give the addresses
+// of matrix 0's sixteen 16-byte rows, lanes 16-31 those of matrix 1.  Lane
+// (g = lane / 4, c = lane % 4) receives in r0 bytes (rows 4c..4c+3, column
+// g) of matrix 0, in r1 the same rows at column g + 8, and in r2, r3 the
+// same of matrix 1 (lowest row in the lowest byte).
+__device__ __forceinline__ void ldsm_x2_trans_b8(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                                 uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
