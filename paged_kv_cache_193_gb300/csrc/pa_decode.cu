@@ -274,37 +274,36 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
         }
         return __shfl_sync(0xffffffffu, ent_cur, k & 31);
     };
-    // All lanes: the physical blocks of iteration it's pages; lane 0 starts
-    // their copies (pages past the warp's last are not copied: their rows
-    // are masked and their V rows zeroed before use).
+    // All lanes: the physical blocks of iteration it's pages; lanes 0 ..
+    // PPI-1 start their copies (pages past the warp's last are not copied:
+    // their rows are masked and their V rows zeroed before use).
     auto fetch = [&](int it) {
         int blk[PPI];
 #pragma unroll
         for (int p = 0; p < PPI; ++p) blk[p] = entry(PPI * it + p);
-        if (lane != 0) return;
+        const int live = min(PPI, my_pages - PPI * it);
+        if (lane >= live) return;
         const int st = warp * SPW + it % SPW;
         const uint32_t bar = smem_addr(&bars[st]);
-        const uint32_t kdst = ring + st * C::STAGE;
+        // lane 0 arms the barrier for every live page; lane p copies page p
+        if (lane == 0) mbar_arrive_expect_tx(bar, live * 2 * C::PAGE);
+        const uint32_t kdst = ring + st * C::STAGE + lane * C::PAGE;
         const uint32_t vdst = kdst + PPI * C::PAGE;
-        const int live = min(PPI, my_pages - PPI * it);
-        mbar_arrive_expect_tx(bar, live * 2 * C::PAGE);
+        int b = blk[0];
 #pragma unroll
-        for (int p = 0; p < PPI; ++p) {
-            if (p >= live) break;
-            int y;
-            if (blk[p] < 0 || blk[p] >= a.num_blocks) {
-                set_device_error(a.err, PA_DEVERR_BAD_BLOCK);
-                y = rows_total;  // wholly outside the tensor: the TMA fills zeros
-            } else {
-                y = (blk[p] * a.num_kv_heads + h) * BS;
-            }
+        for (int p = 1; p < PPI; ++p)
+            if (lane == p) b = blk[p];
+        int y;
+        if (b < 0 || b >= a.num_blocks) {
+            set_device_error(a.err, PA_DEVERR_BAD_BLOCK);
+            y = rows_total;  // wholly outside the tensor: the TMA fills zeros
+        } else {
+            y = (b * a.num_kv_heads + h) * BS;
+        }
 #pragma unroll
-            for (int sl = 0; sl < C::NSLAB; ++sl) {
-                tma_load_2d(kdst + p * C::PAGE + sl * (BS * C::SLAB), &tmK, sl * (C::SLAB / C::ELEM),
-                            y, bar, policy);
-                tma_load_2d(vdst + p * C::PAGE + sl * (BS * C::SLAB), &tmV, sl * (C::SLAB / C::ELEM),
-                            y, bar, policy);
-            }
+        for (int sl = 0; sl < C::NSLAB; ++sl) {
+            tma_load_2d(kdst + sl * (BS * C::SLAB), &tmK, sl * (C::SLAB / C::ELEM), y, bar, policy);
+            tma_load_2d(vdst + sl * (BS * C::SLAB), &tmV, sl * (C::SLAB / C::ELEM), y, bar, policy);
         }
     };
 
@@ -380,6 +379,8 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
                                 (rem % (C::SLAB / 16)) * 16);
                 }
             }
+            // these generic-proxy stores precede the stage's next TMA write
+            fence_proxy_async_smem();
             __syncwarp();
         }
 
@@ -571,9 +572,10 @@ __global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
             }
         }
 
-        // hand the stage back to the TMA: refill with the iteration SPW ahead
-        __syncwarp();
-        fence_proxy_async_smem();
+        // hand the stage back to the TMA: refill with the iteration SPW
+        // ahead.  The stage was only read by generic loads whose values the
+        // MMAs above have consumed; once every lane is past them the copy
+        // may overwrite it (stores made into it were fenced where made).
         __syncwarp();
         if (it + SPW < my_iters) fetch(it + SPW);
     }
@@ -729,21 +731,31 @@ pa_status make_map(CUtensorMap *map, const void *cache, bool fp8, int head_dim, 
 #ifndef PA_DECODE_RING_KB
 #define PA_DECODE_RING_KB 64
 #endif
+// Groups above 8 (two MMA column tiles) at head dim 128 need so many
+// registers that only two CTAs fit on an SM; their ring is larger at no
+// cost in occupancy (more pages in flight per warp).
+#ifndef PA_DECODE_RING_KB_WIDE
+#define PA_DECODE_RING_KB_WIDE 96
+#endif
 constexpr int kWarps = PA_DECODE_WARPS;
-constexpr int kRingBytes = PA_DECODE_RING_KB * 1024;
 
-template <int D, int BS, bool FP8>
+template <int D, int NT>
+constexpr int ring_bytes() {
+    return (D == 128 && NT == 2 ? PA_DECODE_RING_KB_WIDE : PA_DECODE_RING_KB) * 1024;
+}
+
+template <int D, int BS, bool FP8, int NT>
 constexpr int stages_per_warp() {
     constexpr int ppi = (FP8 && BS == 16) ? 2 : 1;  // Cfg::PPI
     constexpr int stage = 2 * ppi * BS * D * (FP8 ? 1 : 2);
-    constexpr int spw = kRingBytes / (kWarps * stage);
+    constexpr int spw = ring_bytes<D, NT>() / (kWarps * stage);
     return spw < 1 ? 1 : spw;
 }
 
 template <int D, int BS, bool FP8, int NT, bool FQ>
 static pa_status launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
                                dim3 grid, cudaStream_t stream) {
-    constexpr int SPW = stages_per_warp<D, BS, FP8>();
+    constexpr int SPW = stages_per_warp<D, BS, FP8, NT>();
     using C = Cfg<D, BS, FP8, NT, kWarps, SPW>;
     auto kern = decode_kernel<D, BS, FP8, NT, kWarps, SPW, FQ>;
     // Raise the kernel's shared-memory limit once per device (the first call

@@ -127,10 +127,27 @@ __global__ void append_kernel(const uint4 *__restrict__ k, const uint4 *__restri
 }
 
 // ---------------------------------------------------------------------------
-// partition merge: WPR warps per (sequence, query head), 128 threads per CTA
+// partition merge: WPR warps per (sequence, query head)
 // ---------------------------------------------------------------------------
 
-constexpr int kReduceThreads = 128;
+// Merge launch shape (build-time): warps per row and partitions in flight
+// per warp, for rows of 17-64 partitions (MID) and of more (WIDE).
+#ifndef PA_REDUCE_MID_WPR
+#define PA_REDUCE_MID_WPR 4
+#endif
+#ifndef PA_REDUCE_MID_U
+#define PA_REDUCE_MID_U 4
+#endif
+#ifndef PA_REDUCE_WIDE_WPR
+#define PA_REDUCE_WIDE_WPR 8
+#endif
+#ifndef PA_REDUCE_WIDE_U
+#define PA_REDUCE_WIDE_U 8
+#endif
+
+// threads of a merge CTA: at least 128, and at least one row's WPR warps
+template <int WPR>
+constexpr int reduce_threads() { return WPR * 32 > 128 ? WPR * 32 : 128; }
 
 // Wait until the grid this one depends on (programmatic dependent launch)
 // has finished and its writes are visible; a no-op otherwise.
@@ -138,105 +155,135 @@ __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Cache-global loads as ordered asm statements: a chunk's loads are all
+// issued before any of their values is used, so they are in flight
+// together (left to itself the compiler interleaves each load with its use).
 template <int VEC>
-__device__ __forceinline__ void fma_vec(float (&acc)[VEC], float w, const float *src) {
+__device__ __forceinline__ void load_vec(float (&x)[VEC], const float *src) {
     if constexpr (VEC == 4) {
-        const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
-        acc[0] += w * x.x;
-        acc[1] += w * x.y;
-        acc[2] += w * x.z;
-        acc[3] += w * x.w;
+        asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"
+                     : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3])
+                     : "l"(src));
     } else {
-        const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
-        acc[0] += w * x.x;
-        acc[1] += w * x.y;
+        asm volatile("ld.global.cg.v2.f32 {%0,%1}, [%2];" : "=f"(x[0]), "=f"(x[1]) : "l"(src));
     }
 }
 
-// Each warp covers all D dims of its row (VEC per lane); the WPR warps of a
-// row take partitions p = sub, sub + WPR, ... with four independent
-// accumulators so four partition loads are in flight per warp.
-template <int D, int WPR>
-__global__ void __launch_bounds__(kReduceThreads)
+__device__ __forceinline__ float load_cg(const float *src) {
+    float x;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(x) : "l"(src));
+    return x;
+}
+
+// One pass over the partitions.  Each warp covers all D dims of its row
+// (VEC per lane); each of the WPR warps of a row takes a contiguous range of
+// partitions, U at a time with every load of the chunk in flight together,
+// and keeps a running (max, sum, accumulator) rescaled when the max grows.
+// The row's warps then combine their triples through shared memory.
+template <int D, int WPR, int U>
+__global__ void __launch_bounds__(reduce_threads<WPR>())
     reduce_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_m,
                   const float *__restrict__ ws_l, const int32_t *__restrict__ context_lens,
                   int num_rows, int num_q_heads, int partition_size, int max_partitions,
                   __nv_bfloat16 *__restrict__ out) {
     constexpr int VEC = D / 32;
-    constexpr int ROWS = kReduceThreads / 32 / WPR;
-    __shared__ float part_s[WPR > 1 ? ROWS * WPR : 1][WPR > 1 ? D : 1];
-    grid_dependency_wait();
+    constexpr int ROWS = reduce_threads<WPR>() / 32 / WPR;
+    __shared__ float part_o[WPR > 1 ? ROWS * WPR : 1][WPR > 1 ? D : 1];
+    __shared__ float part_ml[WPR > 1 ? ROWS * WPR : 1][2];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = warp % WPR;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * ROWS + warp / WPR;
     const bool live = row < num_rows;
+    // the context lengths are inputs of the step, not results of the
+    // attention kernel: read them before waiting for that kernel
     int n = 0;
     if (live) {
         const int ctx = context_lens[row / num_q_heads];
         n = ctx > 0 ? (ctx + partition_size - 1) / partition_size : 0;
         if (n > max_partitions) n = max_partitions;
     }
-    float acc[4][VEC];
+    grid_dependency_wait();
+    float acc[VEC];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
+    float mx = -INFINITY, tot = 0.f;
+    const float *m = ws_m + row * max_partitions;
+    const float *l = ws_l + row * max_partitions;
+    const float *o = ws_o + row * max_partitions * D + lane * VEC;
+    // warp sub takes the contiguous partitions [p_begin, p_end): every chunk
+    // reads U consecutive partition rows, one contiguous run of memory
+    const int per = (n + WPR - 1) / WPR;
+    const int p_begin = sub * per, p_end = min(n, p_begin + per);
+    for (int p0 = p_begin; p0 < p_end; p0 += U) {
+        float mv[U], lv[U], ov[U][VEC];
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) acc[u][j] = 0.f;
-    float total = 0.f;
-    if (n > 0) {
-        const float *m = ws_m + row * max_partitions;
-        const float *l = ws_l + row * max_partitions;
-        float mx = -INFINITY;
-        for (int p = lane; p < n; p += 32) mx = fmaxf(mx, __ldcg(m + p));
+        for (int u = 0; u < U; ++u) {
+            const int p = p0 + u;
+            if (p < p_end) {
+                mv[u] = load_cg(m + p);
+                lv[u] = load_cg(l + p);
+                load_vec<VEC>(ov[u], o + static_cast<int64_t>(p) * D);
+            } else {
+                mv[u] = -INFINITY;
+                lv[u] = 0.f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        // no partition holds a token (every one gave up on a wait): zeros
-        if (mx == -INFINITY) n = 0;
-        for (int p = lane; p < n; p += 32) total += __ldcg(l + p) * __expf(__ldcg(m + p) - mx);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-        const float *o = ws_o + row * max_partitions * D + lane * VEC;
-        int p = sub;
-        for (; p + 3 * WPR < n; p += 4 * WPR) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int q = p + u * WPR;
-                const float w = __ldcg(l + q) * __expf(__ldcg(m + q) - mx);
-                fma_vec<VEC>(acc[u], w, o + static_cast<int64_t>(q) * D);
+                for (int j = 0; j < VEC; ++j) ov[u][j] = 0.f;
             }
         }
-        for (; p < n; p += WPR) {
-            const float w = __ldcg(l + p) * __expf(__ldcg(m + p) - mx);
-            fma_vec<VEC>(acc[0], w, o + static_cast<int64_t>(p) * D);
-        }
-    }
-    float res[VEC];
+        float cmax = mx;
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) res[j] = acc[0][j] + acc[1][j] + acc[2][j] + acc[3][j];
+        for (int u = 0; u < U; ++u) cmax = fmaxf(cmax, mv[u]);
+        // a partition that holds tokens has l > 0 and a finite max; one
+        // that gave up on a wait has l = 0 and weighs nothing
+        const float keep = mx > -INFINITY ? __expf(mx - cmax) : 0.f;
+        tot *= keep;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) acc[j] *= keep;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const float w = lv[u] > 0.f ? lv[u] * __expf(mv[u] - cmax) : 0.f;
+            tot += w;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) acc[j] += w * ov[u][j];
+        }
+        mx = cmax;
+    }
     if constexpr (WPR > 1) {
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) part_s[warp][lane * VEC + j] = res[j];
+        for (int j = 0; j < VEC; ++j) part_o[warp][lane * VEC + j] = acc[j];
+        if (lane == 0) {
+            part_ml[warp][0] = mx;
+            part_ml[warp][1] = tot;
+        }
         __syncthreads();
         if (sub != 0) return;
+        float M = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-            float a = 0.f;
+        for (int w = 0; w < WPR; ++w) M = fmaxf(M, part_ml[warp + w][0]);
+        tot = 0.f;
 #pragma unroll
-            for (int w = 0; w < WPR; ++w) a += part_s[warp + w][lane * VEC + j];
-            res[j] = a;
+        for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
+#pragma unroll
+        for (int w = 0; w < WPR; ++w) {
+            const float tw = part_ml[warp + w][1];
+            const float f = tw > 0.f ? __expf(part_ml[warp + w][0] - M) : 0.f;
+            tot += f * tw;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) acc[j] += f * part_o[warp + w][lane * VEC + j];
         }
     }
     if (!live) return;
-    const float inv = total > 0.f ? 1.f / total : 0.f;
+    const float inv = tot > 0.f ? 1.f / tot : 0.f;
     __nv_bfloat16 *dst = out + row * D + lane * VEC;
     if constexpr (VEC == 4) {
-        __nv_bfloat162 a = __floats2bfloat162_rn(res[0] * inv, res[1] * inv);
-        __nv_bfloat162 b = __floats2bfloat162_rn(res[2] * inv, res[3] * inv);
+        __nv_bfloat162 a = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+        __nv_bfloat162 b = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
         uint2 v;
         v.x = *reinterpret_cast<uint32_t *>(&a);
         v.y = *reinterpret_cast<uint32_t *>(&b);
         *reinterpret_cast<uint2 *>(dst) = v;
     } else {
-        *reinterpret_cast<__nv_bfloat162 *>(dst) = __floats2bfloat162_rn(res[0] * inv, res[1] * inv);
+        *reinterpret_cast<__nv_bfloat162 *>(dst) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
     }
 }
 
@@ -251,12 +298,18 @@ pa_status launch_reduce(const void *workspace, const int32_t *context_lens, int 
     const int64_t rows = static_cast<int64_t>(num_seqs) * num_q_heads;
     const float *ws_m = ws_o + rows * max_partitions * head_dim;
     const float *ws_l = ws_m + rows * max_partitions;
-    // one warp per row while partitions are few, four when there are many
-    const int wpr = max_partitions > 16 ? 4 : 1;
-    const int rows_per_cta = kReduceThreads / 32 / wpr;
+    // one warp per row while partitions are few; more, each with several
+    // partitions in flight, when there are many
+    constexpr int kMidW = PA_REDUCE_MID_WPR, kMidU = PA_REDUCE_MID_U;
+    constexpr int kWideW = PA_REDUCE_WIDE_WPR, kWideU = PA_REDUCE_WIDE_U;
+    const int wpr = max_partitions > 64 ? kWideW : max_partitions > 16 ? kMidW : 1;
+    const int threads = max_partitions > 64   ? reduce_threads<kWideW>()
+                        : max_partitions > 16 ? reduce_threads<kMidW>()
+                                              : reduce_threads<1>();
+    const int rows_per_cta = threads / 32 / wpr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta));
-    cfg.blockDim = dim3(kReduceThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -266,17 +319,19 @@ pa_status launch_reduce(const void *workspace, const int32_t *context_lens, int 
     cfg.numAttrs = 1;
     const int nrows = static_cast<int>(rows);
     __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(out);
+    auto launch = [&](auto kern) {
+        return cudaLaunchKernelEx(&cfg, kern, ws_o, ws_m, ws_l, context_lens, nrows, num_q_heads,
+                                  partition_size, max_partitions, o);
+    };
     cudaError_t e;
     if (head_dim == 128)
-        e = wpr == 4 ? cudaLaunchKernelEx(&cfg, reduce_kernel<128, 4>, ws_o, ws_m, ws_l, context_lens,
-                                          nrows, num_q_heads, partition_size, max_partitions, o)
-                     : cudaLaunchKernelEx(&cfg, reduce_kernel<128, 1>, ws_o, ws_m, ws_l, context_lens,
-                                          nrows, num_q_heads, partition_size, max_partitions, o);
+        e = max_partitions > 64   ? launch(reduce_kernel<128, kWideW, kWideU>)
+            : max_partitions > 16 ? launch(reduce_kernel<128, kMidW, kMidU>)
+                                  : launch(reduce_kernel<128, 1, 8>);
     else
-        e = wpr == 4 ? cudaLaunchKernelEx(&cfg, reduce_kernel<64, 4>, ws_o, ws_m, ws_l, context_lens,
-                                          nrows, num_q_heads, partition_size, max_partitions, o)
-                     : cudaLaunchKernelEx(&cfg, reduce_kernel<64, 1>, ws_o, ws_m, ws_l, context_lens,
-                                          nrows, num_q_heads, partition_size, max_partitions, o);
+        e = max_partitions > 64   ? launch(reduce_kernel<64, kWideW, kWideU>)
+            : max_partitions > 16 ? launch(reduce_kernel<64, kMidW, kMidU>)
+                                  : launch(reduce_kernel<64, 1, 8>);
     return cuda_check(e, "reduce launch");
 }
 

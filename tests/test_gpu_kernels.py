@@ -191,11 +191,15 @@ def test_fp8_decode_lanes(api, oracle, cuda_device):
     compare(out, ref, max_abs=0.0, mean_abs=0.0, what="fp8 code lanes")
 
 
-def test_reduce_alone(api, oracle, cuda_device):
-    rng = np.random.default_rng(21)
-    S, Hq, D, B, PS, MB = 5, 6, 128, 16, 64, 40
+@pytest.mark.parametrize("D,MB,PS", [(128, 40, 64), (64, 40, 64), (128, 40, 32), (64, 70, 16),
+                                     (128, 200, 16), (64, 300, 16)])
+def test_reduce_alone(api, oracle, cuda_device, D, MB, PS):
+    """The merge alone on random partials: 10, 20, 70, 200 and 300
+    partitions per row cover one, four and eight warps per row."""
+    rng = np.random.default_rng(21 + MB + D)
+    S, Hq, B = 5, 6, 16
     P = api.max_partitions(MB, B, PS)
-    ctx = np.array([0, 1, 64, 65, MB * B], np.int32)
+    ctx = np.array([0, 1, PS, PS + 1, MB * B], np.int32)
     o = rng.standard_normal((S, Hq, P, D)).astype(np.float32)
     m = (rng.standard_normal((S, Hq, P)) * 4).astype(np.float32)
     l = rng.uniform(1, 50, (S, Hq, P)).astype(np.float32)
