@@ -410,17 +410,20 @@ pa_status pa_device_errors(unsigned int *flags, int clear);
 
 /*
  * pa_test_set_wait -- TEST HOOK for the kernels' bounded waits; not for
- * production use.  The pages have no counterpart: every wait of a kernel on
- * a page copy gives up after a time limit, sets PA_DEVERR_TIMEOUT, waits for
- * the copies still in flight and finishes with zeros for the affected rows,
- * so a copy that never lands cannot hang the GPU.  This call sets that
- * limit for kernels launched afterwards (limit_ns = 0 restores the default
- * of 2 s; above 60 s is refused).  With stall_first_wait != 0 every
- * pa_decode* kernel makes each warp's first wait on a barrier that no copy
- * completes, so the wait runs out after limit_ns: tests use this to drive
- * the give-up path without a real fault.  The drain of the copies already
- * issued always keeps the 2 s limit.  Process-wide; read at launch time on
- * the host, so set it while none of the library's calls is being made.
+ * production use.  The pages have no counterpart: every wait of the decode
+ * kernel and of the tensor-memory prefill kernel gives up after a time
+ * limit, sets PA_DEVERR_TIMEOUT, waits for the copies still in flight and
+ * finishes (the decode with zeros for the affected rows, the prefill with
+ * an invalid output), so a copy that never lands cannot hang the GPU.
+ * This call sets that limit for kernels launched afterwards (limit_ns = 0
+ * restores the default of 2 s; above 60 s is refused).  With
+ * stall_first_wait != 0 the first wait (each warp's in a pa_decode*
+ * kernel, the MMA threads' in pa_prefill's tensor-memory kernel) is made on
+ * a barrier that nothing completes, so it runs out after limit_ns: tests use
+ * this to drive the give-up path without a real fault.  The drain of the
+ * copies already issued always keeps the 2 s limit.  Process-wide; read at
+ * launch time on the host, so set it while none of the library's calls is
+ * being made.
  */
 pa_status pa_test_set_wait(uint64_t limit_ns, int stall_first_wait);
 

@@ -48,6 +48,8 @@ struct PrefillTcArgs {
     int group;
     int tile_tokens;  // 128 / group
     float score_scale;
+    uint64_t wait_limit_ns;  // give up on a wait after this long
+    int stall_first_wait;    // test hook: the MMA threads' first wait is on a barrier nothing completes
     __nv_bfloat16 *out;
     unsigned int *err;
 };
@@ -81,6 +83,8 @@ constexpr int kTcTmemCols = 512;
 constexpr int kTcPCol = 64;
 constexpr int kTcQCol = 96;
 constexpr int kTcOCol = 128;
+// Drain limit: after a wait gave up, the copies already issued are still
+// waited for with this before the CTA ends.
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 
 template <int BS>
@@ -99,11 +103,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // written (p_full), PV done (pv_done), query half in TMEM (q_tmem)
     __shared__ __align__(8) uint64_t s_full[kTcTiles], s_free[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles],
         q_tmem[kTcTiles], drain[kTcTiles];
+    __shared__ __align__(8) uint64_t stall_bar;  // never completed (wait-limit test hook)
     __shared__ uint32_t tmem_base_s;
     __shared__ int failed_s;
 
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint64_t limit = a.wait_limit_ns;
 
     const int pair = gridDim.x - 1 - blockIdx.x;  // tiles 2 pair and 2 pair + 1
     const int h = blockIdx.y, s = blockIdx.z;
@@ -151,6 +157,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
         mbar_init(smem_addr(&q_full), 1);
         mbar_init(smem_addr(&v_zeroed), 1);
+        mbar_init(smem_addr(&stall_bar), 1);
         for (int i = 0; i < kTcStages; ++i) {
             mbar_init(smem_addr(&kv_full[i]), 2);  // the K loader and the V loader
             mbar_init(smem_addr(&kv_empty[i]), ntiles);
@@ -215,7 +222,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int y = page_row(e_next);
             if (kb + 1 < nkb) e_next = page_entry(kb + 1);
             if (lane == 0) {
-                if (!mbar_wait_bounded(smem_addr(&kv_empty[st]), ph ^ 1, kTcWaitNs)) fail();
+                if (!mbar_wait_bounded(smem_addr(&kv_empty[st]), ph ^ 1, limit)) fail();
                 mbar_arrive_expect_tx(smem_addr(&kv_full[st]), kTcKVStage);
             }
             __syncwarp();
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // zero those V rows before a PV reads them (P is 0 there, but
             // 0 x garbage could be NaN)
             const int kb = nkb - 1, st = kb % kTcStages;
-            if (lane == 0 && !mbar_wait_bounded(smem_addr(&kv_full[st]), (kb / kTcStages) & 1, kTcWaitNs)) fail();
+            if (lane == 0 && !mbar_wait_bounded(smem_addr(&kv_full[st]), (kb / kTcStages) & 1, limit)) fail();
             __syncwarp();
             const uint32_t vbase = base + kTcVOff + st * kTcKVStage;
             for (int r2 = kend - kb * kTcKeys + lane; r2 < kTcKeys; r2 += 32)
@@ -241,6 +248,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&v_zeroed));
         }
+        // Both loaders issue every block, so each stage's phase completes
+        // once its copies land; issuing block kb needed block kb - kTcStages
+        // released, so only the last kTcStages blocks can still be in flight.
+        // Wait for them (2 s) before the CTA may end, whatever gave up.
+        if (lane == 0)
+            for (int kb = max(0, nkb - kTcStages); kb < nkb; ++kb)
+                mbar_wait_bounded(smem_addr(&kv_full[kb % kTcStages]), (kb / kTcStages) & 1, kTcWaitNs);
     } else if (warp == kTcMmaWarp || warp == kTcMmaWarpB) {
         // ---------------- MMA issue, one thread per tile ----------------
         // S(j + 1) is issued once the softmax has S(j) in registers, then
@@ -257,12 +271,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint64_t k_desc = tc_smem_desc(base + kTcKOff, 16, 1024, 2);
             const uint64_t v_desc = tc_smem_desc(base + kTcVOff, kTcKVSlab, 1024, 2);
             const uint32_t tS = tmem + T * 256, tP = tS + kTcPCol, tQ = tS + kTcQCol, tO = tS + kTcOCol;
-            bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, kTcWaitNs) &&
-                      mbar_wait_bounded(smem_addr(&q_tmem[T]), 0, kTcWaitNs);
+            // test hook: give up at once on a barrier that nothing completes
+            bool ok = !a.stall_first_wait || mbar_wait_bounded(smem_addr(&stall_bar), 0, limit);
+            ok = ok && mbar_wait_bounded(smem_addr(&q_full), 0, limit) &&
+                 mbar_wait_bounded(smem_addr(&q_tmem[T]), 0, limit);
             auto qk = [&](int kb) {  // S(kb) = Q K(kb)^T
                 const int ks = kb % kTcStages;
                 // K and V of the block: V(kb) is in place for PV(kb) too
-                ok = ok && mbar_wait_bounded(smem_addr(&kv_full[ks]), (kb / kTcStages) & 1, kTcWaitNs);
+                ok = ok && mbar_wait_bounded(smem_addr(&kv_full[ks]), (kb / kTcStages) & 1, limit);
                 tc_fence_after();
                 if (ok) {
                     const uint64_t b0 = k_desc + ((ks * kTcKVStage) >> 4);
@@ -282,11 +298,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int vs = kb % kTcStages;
                 if (kb + 1 < nkb_t) {
                     // the softmax holds S(kb) in registers
-                    ok = ok && mbar_wait_bounded(smem_addr(&s_free[T]), kb & 1, kTcWaitNs);
+                    ok = ok && mbar_wait_bounded(smem_addr(&s_free[T]), kb & 1, limit);
                     qk(kb + 1);
                 }
-                ok = ok && mbar_wait_bounded(smem_addr(&p_full[T]), kb & 1, kTcWaitNs);
-                if (kb == nkb - 1 && partial) ok = ok && mbar_wait_bounded(smem_addr(&v_zeroed), 0, kTcWaitNs);
+                ok = ok && mbar_wait_bounded(smem_addr(&p_full[T]), kb & 1, limit);
+                if (kb == nkb - 1 && partial) ok = ok && mbar_wait_bounded(smem_addr(&v_zeroed), 0, limit);
                 tc_fence_after();
                 if (ok) {  // O += P(kb) V(kb)
                     const uint64_t b0 = v_desc + ((vs * kTcKVStage) >> 4);
@@ -316,7 +332,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t tS = tmem + lane_addr + T * 256, tP = tS + kTcPCol, tO = tS + kTcOCol;
             const float scale = a.score_scale;
             float m_ref = -INFINITY, l_run = 0.f;
-            bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, kTcWaitNs);
+            bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, limit);
             {
                 // the row's query dims 0-63 (128-byte swizzled in shared
                 // memory) as bf16 pairs in tensor memory: the A operand of
@@ -341,7 +357,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int kb = 0; kb < nkb_t; ++kb) {
                 const int key0 = kb * kTcKeys;
                 const bool masked = key0 + kTcKeys - 1 > warp_min_pos;
-                ok = ok && mbar_wait_bounded(smem_addr(&s_full[T]), kb & 1, kTcWaitNs);
+                ok = ok && mbar_wait_bounded(smem_addr(&s_full[T]), kb & 1, limit);
                 tc_fence_after();
                 float v[64];
                 {
@@ -384,7 +400,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 if (__any_sync(0xffffffffu, rescale)) {
                     // O must hold PV(kb - 1) before it is scaled
-                    ok = ok && mbar_wait_bounded(smem_addr(&pv_done[T]), (kb - 1) & 1, kTcWaitNs);
+                    ok = ok && mbar_wait_bounded(smem_addr(&pv_done[T]), (kb - 1) & 1, limit);
                     tc_fence_after();
 #pragma unroll
                     for (int c = 0; c < 128; c += 32) {
@@ -415,7 +431,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) pk[i] = pack2<false>(v[2 * i], v[2 * i + 1]);
                 if (kb > 0) {  // PV(kb - 1) has read P(kb - 1), and K and V of block kb - 1
-                    ok = ok && mbar_wait_bounded(smem_addr(&pv_done[T]), (kb - 1) & 1, kTcWaitNs);
+                    ok = ok && mbar_wait_bounded(smem_addr(&pv_done[T]), (kb - 1) & 1, limit);
                     tc_fence_after();
                     // the tile's release of that block's stage (the last
                     // block's stage is never reused, so it is not released)
@@ -428,7 +444,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (lane == 0) mbar_arrive(smem_addr(&p_full[T]));
             }
             // every PV is done once the tile's MMA thread's final commit lands
-            ok = ok && mbar_wait_bounded(smem_addr(&drain[T]), 0, kTcWaitNs);
+            ok = ok && mbar_wait_bounded(smem_addr(&drain[T]), 0, limit);
             tc_fence_after();
             if (!ok) fail();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -470,6 +486,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
     }
+    // the query tiles thread 0 requested have landed before the CTA ends
+    if (tid == 0) mbar_wait_bounded(smem_addr(&q_full), 0, kTcWaitNs);
     tc_fence_before();
     __syncthreads();
     if (warp == kTcMmaWarp) {
@@ -540,6 +558,8 @@ pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_ca
     a.group = group;
     a.tile_tokens = kTcRows / group;
     a.score_scale = softmax_scale * 1.4426950408889634f;
+    a.wait_limit_ns = wait_limit_ns();
+    a.stall_first_wait = stall_first_wait();
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.err = err;
     const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;

@@ -1,13 +1,15 @@
-"""The decode kernel's bounded waits give up cleanly.
+"""The kernels' bounded waits give up cleanly.
 
-Every wait of the decode kernel for a page copy has a time limit; when it
-runs out the kernel sets PA_DEVERR_TIMEOUT, waits (with the full limit) for
-the copies it has already issued, and finishes with zeros for the rows it
-could not compute, so a lost copy can never hang the GPU.  Here the test
-hook makes each warp's first wait go to a barrier that no copy ever
-completes, with a 1 ms limit: nothing faults and nothing hangs, the call
-returns, the flag is raised, and the next call at the default limit is
-correct against the oracle (the context is still usable)."""
+Every wait of the decode kernel and of the tensor-memory prefill kernel has
+a time limit; when it runs out the kernel sets PA_DEVERR_TIMEOUT, waits
+(with the full 2 s limit) for the copies it has already issued, and
+finishes (decode: with zeros for the rows it could not compute; prefill:
+with an invalid output), so a lost copy can never hang the GPU.  Here the
+test hook makes the first wait (decode: every warp's; prefill: the MMA
+threads') go to a barrier that nothing ever completes, with a 1 ms limit:
+nothing faults and nothing hangs, the call returns, the flag is raised, and
+the next call at the default limit is correct against the oracle (the
+context is still usable)."""
 import numpy as np
 import pytest
 import torch
@@ -16,6 +18,7 @@ from gpu_helpers import compare, device_tables
 from paged_kv_cache_193_gb300 import _lib
 from paged_kv_cache_193_gb300 import workloads as W
 from test_gpu_kernels import _oracle_step
+from test_gpu_prefill import _dev, _oracle_step as _oracle_prefill
 
 pytestmark = pytest.mark.gpu
 
@@ -72,3 +75,28 @@ def test_wait_limit_is_validated():
     lib = _lib.load()
     assert lib.pa_test_set_wait(61 * 10**9, 0) == _lib.PA_ERR_INVALID_ARG
     assert lib.pa_test_set_wait(0, 0) == _lib.PA_OK
+
+
+@pytest.mark.parametrize("G,Hkv,B", [(4, 2, 16), (1, 4, 32), (16, 1, 16)])
+def test_prefill_wait_runs_out_then_recovers(api, oracle, cuda_device, G, Hkv, B):
+    lib = _lib.load()
+    wl = W.make_prefill(cuda_device, seed=40 + G + B, num_seqs=5, chunk=[1, 7, 64, 300, 33],
+                        prefixes=[0, 5, 33, 300, 16], num_q_heads=G * Hkv, num_kv_heads=Hkv,
+                        head_dim=128, block_size=B)
+    W.poison_prefill(wl)
+    _, _, _, ref = _oracle_prefill(oracle, wl)
+    bt, cl, qs = _dev(wl, cuda_device)
+    slots = api.chunk_slot_mapping(bt, cl, qs, wl.shape.block_size)
+    api.cache_append(wl.k_new, wl.v_new, slots, wl.k_cache, wl.v_cache)
+    torch.cuda.synchronize()
+    api.device_errors(clear=True)
+    _stalled(lib, lambda: api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, wl.max_query_len,
+                                      wl.softmax_scale))
+    flags = api.device_errors(clear=True)
+    assert flags & _lib.PA_DEVERR_TIMEOUT, hex(flags)
+    assert flags & ~_lib.PA_DEVERR_TIMEOUT == 0, hex(flags)
+    # the next call, at the default limit, is correct
+    out = api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, wl.max_query_len, wl.softmax_scale)
+    torch.cuda.synchronize()
+    compare(out, ref, what=f"prefill G{G} B{B} after a timed-out call")
+    assert api.device_errors() == 0
