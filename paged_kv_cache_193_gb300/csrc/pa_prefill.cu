@@ -431,6 +431,11 @@ static pa_status prefill_impl(const void *q, const void *k_cache, const void *v_
         return fail(PA_ERR_UNSUPPORTED, "pool exceeds 2^31 rows");
     if (num_seqs > 65535 || num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "grid too large");
     if (!isfinite(softmax_scale)) return fail(PA_ERR_INVALID_ARG, "softmax_scale is not finite");
+    // The prefill kernels take each row's maximum over the raw scores and
+    // scale it afterwards, which keeps the order only for a positive scale.
+    if (!(softmax_scale > 0.f))
+        return fail(PA_ERR_UNSUPPORTED, "prefill needs softmax_scale > 0 (got %g)",
+                    static_cast<double>(softmax_scale));
     if (num_seqs == 0 || max_query_len == 0 || num_tokens == 0) return PA_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start || !out)
         return fail(PA_ERR_INVALID_ARG, "null pointer");

@@ -135,6 +135,8 @@ def _prefill(lib, fn="pa_prefill", **kw):
     (dict(S=70000), 2),
     (dict(NB=1 << 27), 2),                          # pool rows past 2^31
     (dict(sm=float("nan")), 1),
+    (dict(sm=0.0), 2),                              # the prefill kernels need a positive scale
+    (dict(sm=-0.088), 2),
     (dict(q=None), 1),
     (dict(out=ctypes.c_void_p((1 << 20) + 8)), 1),  # not 16-byte aligned
 ])
