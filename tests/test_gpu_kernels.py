@@ -188,7 +188,7 @@ def test_fp8_decode_lanes(api, oracle, cuda_device):
                      torch.from_numpy(ctx).to(cuda_device), 0.1, kv_scale=0.5)
     ref = oracle.decode(W.bits(q), kc, vc, tables, ctx, Hkv, B, 0.1, kv_dtype=1, kv_scale=0.5)
     # a one-token softmax is exactly 1, so out = bf16(V * 0.5)
-    compare(out, ref, max_abs=0.0, mean_abs=0.0, what="fp8 code lanes")
+    compare(out, ref, max_abs=0.0, mean_abs=0.0, what="fp8 code lanes", ulp_rel=0.0)
 
 
 @pytest.mark.parametrize("D,MB,PS", [(128, 40, 64), (64, 40, 64), (128, 40, 32), (64, 70, 16),

@@ -1,0 +1,91 @@
+"""Edge cases at the limits of the decode path, against the oracle:
+
+* degenerate softmax scales: 0 weighs every cached token equally (the step
+  returns the mean of V, checked here without the oracle too), a negative
+  scale reverses the preference;
+* the largest grid a launch takes: 65,535 sequences (the grid's z limit), of
+  0 to 40 tokens each, unsplit and in partitions of 16 tokens;
+* one context of 2^20 tokens (65,536 pages of one KV head, group 16) beside a
+  short one, unsplit (one CTA walks the whole table) and in 2,048 partitions
+  of 512 (the merge's widest shape), checked on sampled heads.
+Slots and appended rows are compared bit for bit, outputs within the
+attention tolerance, all through guarded buffers."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import compare, device_tables, guard_step
+from paged_kv_cache_193_gb300 import workloads as W
+from test_gpu_configs import _check_step
+from test_gpu_kernels import _oracle_step, _random_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api(cuda_device):
+    from paged_kv_cache_193_gb300 import api as a
+    a._lib_handle()
+    return a
+
+
+def _full_step(api, wl, ps):
+    bt, cl = device_tables(wl, wl.k_cache.device)
+    step = api.DecodeStep(wl.k_cache, wl.v_cache, bt, cl, wl.shape.num_q_heads, wl.softmax_scale,
+                          wl.kv_scale, ps)
+    check = guard_step(step)
+    api.device_errors(clear=True)
+    out = step(wl.q, wl.k_new, wl.v_new)
+    torch.cuda.synchronize()
+    check(f"ps={ps}")
+    assert api.device_errors() == 0
+    return step.slots.cpu().numpy(), out
+
+
+def _bf16_rows(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.3])
+@pytest.mark.parametrize("ps", [0, 32])
+def test_degenerate_softmax_scales(api, oracle, cuda_device, scale, ps):
+    ctx = [1, 15, 16, 17, 200]
+    B, G = 16, 4
+    wl = _random_case(77, len(ctx), 8, 2, 64, B, ctx, W.KV_BF16, oracle, cuda_device)
+    wl.softmax_scale = scale
+    W.poison(wl, pending=True)
+    slots_ref, kc_ref, vc_ref, out_ref = _oracle_step(oracle, wl)
+    if scale == 0.0:
+        # uniform weights: each output row is the mean of its KV head's V rows
+        for s, n in enumerate(ctx):
+            for hq in range(8):
+                rows = [vc_ref[wl.block_tables[s, t // B], hq // G, t % B] for t in range(n)]
+                mean = _bf16_rows(np.stack(rows)).mean(axis=0)
+                assert np.abs(mean - out_ref[s, hq]).max() < 1e-9
+    slots, out = _full_step(api, wl, ps)
+    assert np.array_equal(slots, slots_ref)
+    assert np.array_equal(W.bits(wl.k_cache), kc_ref) and np.array_equal(W.bits(wl.v_cache), vc_ref)
+    compare(out, out_ref, what=f"softmax_scale {scale} ps={ps}")
+
+
+@pytest.mark.parametrize("ps", [0, 16])
+def test_largest_grid(api, oracle, cuda_device, ps):
+    S = 65535
+    ctx = [0 if s % 97 == 0 else 1 + (s * 7919) % 40 for s in range(S)]
+    wl = _random_case(65535, S, 8, 2, 64, 16, ctx, W.KV_BF16, oracle, cuda_device, nb_extra=64)
+    W.poison(wl, pending=True)
+    slots_ref, kc_ref, vc_ref, out_ref = _oracle_step(oracle, wl)
+    slots, out = _full_step(api, wl, ps)
+    assert np.array_equal(slots, slots_ref)
+    assert np.array_equal(W.bits(wl.k_cache), kc_ref) and np.array_equal(W.bits(wl.v_cache), vc_ref)
+    compare(out, out_ref, what=f"65535 sequences ps={ps}")
+
+
+@pytest.mark.parametrize("ps", [0, 512])
+def test_million_token_context(api, oracle, cuda_device, ps):
+    B = 16
+    ctx = np.array([1 << 20, 37], np.int64)
+    nb = sum(-(-int(c) // B) for c in ctx) + 8
+    tables, _ = W.build_tables(ctx, B, nb, np.random.default_rng(20))
+    wl = W._finish("million", W.Shape(2, 16, 1, 128, B), ctx, tables, nb, cuda_device, 20)
+    _check_step(api, oracle, wl, ps, n_seqs=2, heads_per_seq=5, seed=20)
