@@ -7,6 +7,34 @@
 
 namespace pa {
 
+// try_wait that lets the hardware suspend the thread until the phase
+// completes (or `hint_ns` passes), instead of returning at once: a waiting
+// warp then takes no issue slots from the warps of its SM sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait built on the suspending try_wait: gives up once `limit_ns`
+// of wall time has passed since the first unsuccessful try (checked after
+// every try; one try suspends for at most kSuspendHintNs).
+constexpr uint32_t kSuspendHintNs = 100000;
+__device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
 }
@@ -148,6 +176,7 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+
 // 3-D tiled TMA store of one box from shared memory (bulk group), and the
 // wait until every store this thread issued has finished READING shared
 // memory (the global writes may still be in flight).

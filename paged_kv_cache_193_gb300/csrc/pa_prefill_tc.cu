@@ -27,6 +27,11 @@
 //    against a reference max that only moves when the row max outgrows it
 //    by 2^8 (so O is rescaled in tensor memory rarely), and store P as bf16
 //    pairs in its own columns, which PV(j) reads.
+//  * Every wait lets the hardware suspend the waiting thread until the phase
+//    completes (try_wait with a time hint) rather than spin: the MMA threads
+//    share their SM sub-partitions with softmax warps, and a spinning waiter
+//    takes issue slots from them.  Each wait is still bounded by the runtime
+//    limit (2 s by default).
 #include <cudaTypedefs.h>
 #include <limits.h>
 #include <math.h>
@@ -222,7 +227,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int y = page_row(e_next);
             if (kb + 1 < nkb) e_next = page_entry(kb + 1);
             if (lane == 0) {
-                if (!mbar_wait_bounded(smem_addr(&kv_empty[st]), ph ^ 1, limit)) fail();
+                if (!mbar_wait_suspend(smem_addr(&kv_empty[st]), ph ^ 1, limit)) fail();
                 mbar_arrive_expect_tx(smem_addr(&kv_full[st]), kTcKVStage);
             }
             __syncwarp();
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // zero those V rows before a PV reads them (P is 0 there, but
             // 0 x garbage could be NaN)
             const int kb = nkb - 1, st = kb % kTcStages;
-            if (lane == 0 && !mbar_wait_bounded(smem_addr(&kv_full[st]), (kb / kTcStages) & 1, limit)) fail();
+            if (lane == 0 && !mbar_wait_suspend(smem_addr(&kv_full[st]), (kb / kTcStages) & 1, limit)) fail();
             __syncwarp();
             const uint32_t vbase = base + kTcVOff + st * kTcKVStage;
             for (int r2 = kend - kb * kTcKeys + lane; r2 < kTcKeys; r2 += 32)
@@ -254,7 +259,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // Wait for them (2 s) before the CTA may end, whatever gave up.
         if (lane == 0)
             for (int kb = max(0, nkb - kTcStages); kb < nkb; ++kb)
-                mbar_wait_bounded(smem_addr(&kv_full[kb % kTcStages]), (kb / kTcStages) & 1, kTcWaitNs);
+                mbar_wait_suspend(smem_addr(&kv_full[kb % kTcStages]), (kb / kTcStages) & 1, kTcWaitNs);
     } else if (warp == kTcMmaWarp || warp == kTcMmaWarpB) {
         // ---------------- MMA issue, one thread per tile ----------------
         // S(j + 1) is issued once the softmax has S(j) in registers, then
@@ -272,13 +277,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint64_t v_desc = tc_smem_desc(base + kTcVOff, kTcKVSlab, 1024, 2);
             const uint32_t tS = tmem + T * 256, tP = tS + kTcPCol, tQ = tS + kTcQCol, tO = tS + kTcOCol;
             // test hook: give up at once on a barrier that nothing completes
-            bool ok = !a.stall_first_wait || mbar_wait_bounded(smem_addr(&stall_bar), 0, limit);
-            ok = ok && mbar_wait_bounded(smem_addr(&q_full), 0, limit) &&
-                 mbar_wait_bounded(smem_addr(&q_tmem[T]), 0, limit);
+            bool ok = !a.stall_first_wait || mbar_wait_suspend(smem_addr(&stall_bar), 0, limit);
+            ok = ok && mbar_wait_suspend(smem_addr(&q_full), 0, limit) &&
+                 mbar_wait_suspend(smem_addr(&q_tmem[T]), 0, limit);
             auto qk = [&](int kb) {  // S(kb) = Q K(kb)^T
                 const int ks = kb % kTcStages;
                 // K and V of the block: V(kb) is in place for PV(kb) too
-                ok = ok && mbar_wait_bounded(smem_addr(&kv_full[ks]), (kb / kTcStages) & 1, limit);
+                ok = ok && mbar_wait_suspend(smem_addr(&kv_full[ks]), (kb / kTcStages) & 1, limit);
                 tc_fence_after();
                 if (ok) {
                     const uint64_t b0 = k_desc + ((ks * kTcKVStage) >> 4);
@@ -298,11 +303,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int vs = kb % kTcStages;
                 if (kb + 1 < nkb_t) {
                     // the softmax holds S(kb) in registers
-                    ok = ok && mbar_wait_bounded(smem_addr(&s_free[T]), kb & 1, limit);
+                    ok = ok && mbar_wait_suspend(smem_addr(&s_free[T]), kb & 1, limit);
                     qk(kb + 1);
                 }
-                ok = ok && mbar_wait_bounded(smem_addr(&p_full[T]), kb & 1, limit);
-                if (kb == nkb - 1 && partial) ok = ok && mbar_wait_bounded(smem_addr(&v_zeroed), 0, limit);
+                ok = ok && mbar_wait_suspend(smem_addr(&p_full[T]), kb & 1, limit);
+                if (kb == nkb - 1 && partial) ok = ok && mbar_wait_suspend(smem_addr(&v_zeroed), 0, limit);
                 tc_fence_after();
                 if (ok) {  // O += P(kb) V(kb)
                     const uint64_t b0 = v_desc + ((vs * kTcKVStage) >> 4);
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!ok) fail();
             // every MMA issued above is complete before the TMEM is released
             tc_commit(smem_addr(&drain[T]));
-            mbar_wait_bounded(smem_addr(&drain[T]), 0, kTcWaitNs);
+            mbar_wait_suspend(smem_addr(&drain[T]), 0, kTcWaitNs);
         }
     } else {
         // ------------- softmax: one query row per thread, 64 keys a block -------------
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t tS = tmem + lane_addr + T * 256, tP = tS + kTcPCol, tO = tS + kTcOCol;
             const float scale = a.score_scale;
             float m_ref = -INFINITY, l_run = 0.f;
-            bool ok = mbar_wait_bounded(smem_addr(&q_full), 0, limit);
+            bool ok = mbar_wait_suspend(smem_addr(&q_full), 0, limit);
             {
                 // the row's query dims 0-63 (128-byte swizzled in shared
                 // memory) as bf16 pairs in tensor memory: the A operand of
@@ -357,7 +362,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int kb = 0; kb < nkb_t; ++kb) {
                 const int key0 = kb * kTcKeys;
                 const bool masked = key0 + kTcKeys - 1 > warp_min_pos;
-                ok = ok && mbar_wait_bounded(smem_addr(&s_full[T]), kb & 1, limit);
+                ok = ok && mbar_wait_suspend(smem_addr(&s_full[T]), kb & 1, limit);
                 tc_fence_after();
                 float v[64];
                 {
@@ -400,7 +405,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 if (__any_sync(0xffffffffu, rescale)) {
                     // O must hold PV(kb - 1) before it is scaled
-                    ok = ok && mbar_wait_bounded(smem_addr(&pv_done[T]), (kb - 1) & 1, limit);
+                    ok = ok && mbar_wait_suspend(smem_addr(&pv_done[T]), (kb - 1) & 1, limit);
                     tc_fence_after();
 #pragma unroll
                     for (int c = 0; c < 128; c += 32) {
@@ -431,7 +436,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) pk[i] = pack2<false>(v[2 * i], v[2 * i + 1]);
                 if (kb > 0) {  // PV(kb - 1) has read P(kb - 1), and K and V of block kb - 1
-                    ok = ok && mbar_wait_bounded(smem_addr(&pv_done[T]), (kb - 1) & 1, limit);
+                    ok = ok && mbar_wait_suspend(smem_addr(&pv_done[T]), (kb - 1) & 1, limit);
                     tc_fence_after();
                     // the tile's release of that block's stage (the last
                     // block's stage is never reused, so it is not released)
@@ -444,7 +449,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (lane == 0) mbar_arrive(smem_addr(&p_full[T]));
             }
             // every PV is done once the tile's MMA thread's final commit lands
-            ok = ok && mbar_wait_bounded(smem_addr(&drain[T]), 0, limit);
+            ok = ok && mbar_wait_suspend(smem_addr(&drain[T]), 0, limit);
             tc_fence_after();
             if (!ok) fail();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -487,7 +492,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     }
     // the query tiles thread 0 requested have landed before the CTA ends
-    if (tid == 0) mbar_wait_bounded(smem_addr(&q_full), 0, kTcWaitNs);
+    if (tid == 0) mbar_wait_suspend(smem_addr(&q_full), 0, kTcWaitNs);
     tc_fence_before();
     __syncthreads();
     if (warp == kTcMmaWarp) {
