@@ -1,4 +1,4 @@
-"""Edge cases at the limits of the decode path, against the oracle:
+"""Edge cases at the limits of the decode and prefill paths, against the oracle:
 
 * degenerate softmax scales: 0 weighs every cached token equally (the step
   returns the mean of V, checked here without the oracle too), a negative
@@ -7,7 +7,9 @@
   0 to 40 tokens each, unsplit and in partitions of 16 tokens;
 * one context of 2^20 tokens (65,536 pages of one KV head, group 16) beside a
   short one, unsplit (one CTA walks the whole table) and in 2,048 partitions
-  of 512 (the merge's widest shape), checked on sampled heads.
+  of 512 (the merge's widest shape), checked on sampled heads;
+* prefill: one 2,048-token chunk (32 tile pairs of one sequence), 2,000
+  sequences of 1-3-token chunks, and chunks with no cached prefix.
 Slots and appended rows are compared bit for bit, outputs within the
 attention tolerance, all through guarded buffers."""
 import numpy as np
@@ -89,3 +91,47 @@ def test_million_token_context(api, oracle, cuda_device, ps):
     tables, _ = W.build_tables(ctx, B, nb, np.random.default_rng(20))
     wl = W._finish("million", W.Shape(2, 16, 1, 128, B), ctx, tables, nb, cuda_device, 20)
     _check_step(api, oracle, wl, ps, n_seqs=2, heads_per_seq=5, seed=20)
+
+
+# ---------------------------------------------------------------------------
+# chunked prefill at its limits
+# ---------------------------------------------------------------------------
+
+def _prefill_case(api, oracle, cuda_device, what, **kw):
+    from test_gpu_prefill import _gpu_step as prefill_step, _oracle_step as prefill_oracle
+    wl = W.make_prefill(cuda_device, **kw)
+    W.poison_prefill(wl)
+    api.device_errors(clear=True)
+    slots_ref, kc_ref, vc_ref, ref = prefill_oracle(oracle, wl)
+    slots, out = prefill_step(api, wl, cuda_device, "auto")
+    assert np.array_equal(slots, slots_ref)
+    assert np.array_equal(W.bits(wl.k_cache), kc_ref) and np.array_equal(W.bits(wl.v_cache), vc_ref)
+    compare(out, ref, what=what)
+    assert api.device_errors() == 0
+
+
+def test_prefill_long_chunk(api, oracle, cuda_device):
+    """One 2,048-token chunk after a 1,500-token prefix (32 tile pairs of one
+    sequence, keys up to 3,548) beside a 5-token chunk."""
+    _prefill_case(api, oracle, cuda_device, "prefill long chunk", seed=61, num_seqs=2, chunk=[2048, 5],
+                  prefixes=[1500, 0], num_q_heads=4, num_kv_heads=1, head_dim=128, block_size=16)
+
+
+def test_prefill_many_sequences(api, oracle, cuda_device):
+    """2,000 sequences with chunks of 1-3 tokens after prefixes of 0-100:
+    2,000 x 2 work items of one partial tile each."""
+    rng = np.random.default_rng(62)
+    S = 2000
+    chunks = rng.integers(1, 3, size=S, endpoint=True).tolist()
+    prefixes = rng.integers(0, 100, size=S, endpoint=True).tolist()
+    _prefill_case(api, oracle, cuda_device, "prefill 2000 sequences", seed=62, num_seqs=S, chunk=chunks,
+                  prefixes=prefixes, num_q_heads=16, num_kv_heads=2, head_dim=128, block_size=16)
+
+
+@pytest.mark.parametrize("G,B", [(4, 16), (1, 32)])
+def test_prefill_without_prefix(api, oracle, cuda_device, G, B):
+    """Chunks that are the whole context (no cached prefix): causal
+    self-attention, the first row attending to itself only."""
+    _prefill_case(api, oracle, cuda_device, f"prefill no prefix G{G} B{B}", seed=63 + G, num_seqs=4,
+                  chunk=[1, 64, 129, 300], prefixes=[0, 0, 0, 0], num_q_heads=2 * G, num_kv_heads=2,
+                  head_dim=128, block_size=B)
