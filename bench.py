@@ -67,6 +67,9 @@ SECONDARY = [
 ]
 DECODE_SOURCES = ["paged_kv_cache_193_gb300/csrc/pa_decode.cu",
                   "paged_kv_cache_193_gb300/csrc/pa_device.cuh"]
+PREFILL_SOURCES = ["paged_kv_cache_193_gb300/csrc/pa_prefill_tc.cu",
+                   "paged_kv_cache_193_gb300/csrc/pa_prefill.cuh",
+                   "paged_kv_cache_193_gb300/csrc/pa_device.cuh"]
 
 
 def parse():
@@ -377,9 +380,9 @@ def cpu_baseline_prefill(wl, budget_s: float):
 # GPU arm
 # --------------------------------------------------------------------------
 
-def source_digest() -> str:
+def source_digest(sources=DECODE_SOURCES) -> str:
     h = hashlib.sha256()
-    for p in DECODE_SOURCES:
+    for p in sources:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -402,6 +405,21 @@ def recorded_traffic(wl, ps, args):
         key += "/e4m3"
     entry = rec.get(key)
     if not entry or entry.get("source_digest") != source_digest():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def recorded_prefill_traffic(sh, mq, num_seqs):
+    """DRAM bytes per tcgen05 prefill launch from a committed ncu capture of
+    the same kernel source and workload shape, else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "prefill_traffic.json")) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    key = f"S{num_seqs}/C{mq}/H{sh.num_q_heads}/KV{sh.num_kv_heads}/D{sh.head_dim}/B{sh.block_size}"
+    entry = rec.get(key)
+    if not entry or entry.get("source_digest") != source_digest(PREFILL_SOURCES):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -1016,7 +1034,7 @@ def run_prefill(args):
                      "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
                      "peak_kind": f"{kind} cuBLAS bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
-                     "traffic": None},
+                     "traffic": recorded_prefill_traffic(sh, mq, sh.num_seqs)},
         "clocks": clocks.summary(t0 - 1.0, t1),
     }
     if not args.no_e2e:
