@@ -4,10 +4,12 @@
   returns the mean of V, checked here without the oracle too), a negative
   scale reverses the preference;
 * the largest grid a launch takes: 65,535 sequences (the grid's z limit), of
-  0 to 40 tokens each, unsplit and in partitions of 16 tokens;
+  0 to 40 tokens each, unsplit and in partitions of 16 tokens, and with the
+  E4M3 cache;
 * one context of 2^20 tokens (65,536 pages of one KV head, group 16) beside a
-  short one, unsplit (one CTA walks the whole table) and in 2,048 partitions
-  of 512 (the merge's widest shape), checked on sampled heads;
+  short one, unsplit (one CTA walks the whole table), in 2,048 partitions of
+  512 (the merge's widest shape), with 32-token pages and with the E4M3
+  cache, checked on sampled heads;
 * prefill: one 2,048-token chunk (32 tile pairs of one sequence), 2,000
   sequences of 1-3-token chunks, and chunks with no cached prefix.
 Slots and appended rows are compared bit for bit, outputs within the
@@ -16,7 +18,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import compare, device_tables, guard_step
+from gpu_helpers import compare, device_tables, guard_step, quantize_with_torch
 from paged_kv_cache_193_gb300 import workloads as W
 from test_gpu_configs import _check_step
 from test_gpu_kernels import _oracle_step, _random_case
@@ -50,14 +52,16 @@ def _bf16_rows(bits):
 
 @pytest.mark.parametrize("scale", [0.0, -0.3])
 @pytest.mark.parametrize("ps", [0, 32])
-def test_degenerate_softmax_scales(api, oracle, cuda_device, scale, ps):
+@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_FP8_E4M3])
+def test_degenerate_softmax_scales(api, oracle, cuda_device, scale, ps, kv):
     ctx = [1, 15, 16, 17, 200]
     B, G = 16, 4
-    wl = _random_case(77, len(ctx), 8, 2, 64, B, ctx, W.KV_BF16, oracle, cuda_device)
+    D = 64 if kv == W.KV_BF16 else 128
+    wl = _random_case(77, len(ctx), 8, 2, D, B, ctx, kv, oracle, cuda_device)
     wl.softmax_scale = scale
     W.poison(wl, pending=True)
     slots_ref, kc_ref, vc_ref, out_ref = _oracle_step(oracle, wl)
-    if scale == 0.0:
+    if scale == 0.0 and kv == W.KV_BF16:
         # uniform weights: each output row is the mean of its KV head's V rows
         for s, n in enumerate(ctx):
             for hq in range(8):
@@ -70,11 +74,17 @@ def test_degenerate_softmax_scales(api, oracle, cuda_device, scale, ps):
     compare(out, out_ref, what=f"softmax_scale {scale} ps={ps}")
 
 
-@pytest.mark.parametrize("ps", [0, 16])
-def test_largest_grid(api, oracle, cuda_device, ps):
+@pytest.mark.parametrize("ps,kv", [(0, W.KV_BF16), (16, W.KV_BF16), (0, W.KV_FP8_E4M3)])
+def test_largest_grid(api, oracle, cuda_device, ps, kv):
     S = 65535
     ctx = [0 if s % 97 == 0 else 1 + (s * 7919) % 40 for s in range(S)]
-    wl = _random_case(65535, S, 8, 2, 64, 16, ctx, W.KV_BF16, oracle, cuda_device, nb_extra=64)
+    B = 16
+    need = sum(-(-c // B) for c in ctx)
+    tables, _ = W.build_tables(np.array(ctx, np.int64), B, need + 64, np.random.default_rng(65535))
+    wl = W._finish("grid", W.Shape(S, 8, 2, 64, B, kv_dtype=kv), np.array(ctx, np.int64), tables, need + 64,
+                   cuda_device, 65535)
+    if kv == W.KV_FP8_E4M3:
+        quantize_with_torch(wl)  # a library conversion, only to make the E4M3 input pool
     W.poison(wl, pending=True)
     slots_ref, kc_ref, vc_ref, out_ref = _oracle_step(oracle, wl)
     slots, out = _full_step(api, wl, ps)
@@ -83,13 +93,15 @@ def test_largest_grid(api, oracle, cuda_device, ps):
     compare(out, out_ref, what=f"65535 sequences ps={ps}")
 
 
-@pytest.mark.parametrize("ps", [0, 512])
-def test_million_token_context(api, oracle, cuda_device, ps):
-    B = 16
+@pytest.mark.parametrize("ps,B,kv", [(0, 16, W.KV_BF16), (512, 16, W.KV_BF16), (0, 32, W.KV_BF16),
+                                     (512, 16, W.KV_FP8_E4M3)])
+def test_million_token_context(api, oracle, cuda_device, ps, B, kv):
     ctx = np.array([1 << 20, 37], np.int64)
     nb = sum(-(-int(c) // B) for c in ctx) + 8
     tables, _ = W.build_tables(ctx, B, nb, np.random.default_rng(20))
-    wl = W._finish("million", W.Shape(2, 16, 1, 128, B), ctx, tables, nb, cuda_device, 20)
+    wl = W._finish("million", W.Shape(2, 16, 1, 128, B, kv_dtype=kv), ctx, tables, nb, cuda_device, 20)
+    if kv == W.KV_FP8_E4M3:
+        quantize_with_torch(wl)  # a library conversion, only to make the E4M3 input pool
     _check_step(api, oracle, wl, ps, n_seqs=2, heads_per_seq=5, seed=20)
 
 
