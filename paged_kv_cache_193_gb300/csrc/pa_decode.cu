@@ -122,8 +122,11 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int t, int b) {
 // FQ (E4M3 cache only): the query is rounded to E4M3 (x / q_scale) and the
 // scores are an E4M3 x E4M3 tensor-core product over the cache bytes as
 // they lie in shared memory.
+// Groups above 8 with a bf16 cache of 16-token pages are held to three CTAs
+// per SM (at most 168 registers, a 64 KB ring): their CTAs are short when the
+// context is split, and a third CTA per SM hides more of each one's start.
 template <int D, int BS, bool FP8, int NT, int NW, int SPW, bool FQ = false>
-__global__ void __launch_bounds__(NW * 32, NW >= 8 ? 1 : 8 / NW)
+__global__ void __launch_bounds__(NW * 32, (NT == 2 && BS == 16 && !FP8) ? 3 : (NW >= 8 ? 1 : 8 / NW))
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeArgs a) {
     static_assert(!FQ || FP8, "the E4M3 score product needs the E4M3 cache");
@@ -733,22 +736,25 @@ pa_status make_map(CUtensorMap *map, const void *cache, bool fp8, int head_dim, 
 #endif
 // Groups above 8 (two MMA column tiles) at head dim 128 need so many
 // registers that only two CTAs fit on an SM; their ring is larger at no
-// cost in occupancy (more pages in flight per warp).
+// cost in occupancy (more pages in flight per warp).  Except with a bf16
+// cache of 16-token pages: those are held to three CTAs per SM and keep the
+// 64 KB ring.
 #ifndef PA_DECODE_RING_KB_WIDE
 #define PA_DECODE_RING_KB_WIDE 96
 #endif
 constexpr int kWarps = PA_DECODE_WARPS;
 
-template <int D, int NT>
+template <int D, int NT, int BS, bool FP8>
 constexpr int ring_bytes() {
-    return (D == 128 && NT == 2 ? PA_DECODE_RING_KB_WIDE : PA_DECODE_RING_KB) * 1024;
+    constexpr bool wide = D == 128 && NT == 2 && !(BS == 16 && !FP8);
+    return (wide ? PA_DECODE_RING_KB_WIDE : PA_DECODE_RING_KB) * 1024;
 }
 
 template <int D, int BS, bool FP8, int NT>
 constexpr int stages_per_warp() {
     constexpr int ppi = (FP8 && BS == 16) ? 2 : 1;  // Cfg::PPI
     constexpr int stage = 2 * ppi * BS * D * (FP8 ? 1 : 2);
-    constexpr int spw = ring_bytes<D, NT>() / (kWarps * stage);
+    constexpr int spw = ring_bytes<D, NT, BS, FP8>() / (kWarps * stage);
     return spw < 1 ? 1 : spw;
 }
 
