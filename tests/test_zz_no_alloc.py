@@ -18,7 +18,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import compare, device_tables, oracle_sampled
+from gpu_helpers import compare, device_tables, oracle_sampled, quantize_with_torch
 from paged_kv_cache_193_gb300 import _lib
 from paged_kv_cache_193_gb300 import workloads as W
 
@@ -52,23 +52,33 @@ def _reference_call(lib, wl, bt, cl, ps, out, stream):
     return st
 
 
-def test_static_workspace_matches_pa_decode(cuda_device, oracle):
+@pytest.mark.parametrize("name,fp8,num_seqs,sizes", [
+    ("llama8b", False, 48, (512, 256)),
+    ("llama8b", True, 48, (512, 256)),          # E4M3 cache
+    ("ctx128k", False, 1, (512, 1024)),        # group 16, 256 and 128 partitions
+])
+def test_static_workspace_matches_pa_decode(cuda_device, oracle, name, fp8, num_seqs, sizes):
     lib = _lib.load()
-    wl = W.make("llama8b", device=cuda_device, num_seqs=48)
+    wl = W.make(name, device=cuda_device, num_seqs=num_seqs)
+    if fp8:
+        wl.shape.kv_dtype = W.KV_FP8_E4M3
+        wl.kv_scale = W.fp8_scale_from(wl.k_cache, wl.v_cache, wl.k_new, wl.v_new)
+        quantize_with_torch(wl)  # a library conversion, only to make the E4M3 input pool
     W.poison(wl)
     bt, cl = device_tables(wl, cuda_device)
     stream = torch.cuda.current_stream().cuda_stream
     rng = np.random.default_rng(48)
     sh = wl.shape
-    # every query head of four sequences (the shortest and longest among
-    # them), plus 64 random (sequence, head) pairs
+    # every query head of up to four sequences (the shortest and longest
+    # among them), plus 64 random (sequence, head) pairs
     order = np.argsort(wl.context_lens)
-    seqs = [int(order[0]), int(order[1]), int(order[-2]), int(order[-1])]
+    seqs = sorted({int(order[0]), int(order[min(1, len(order) - 1)]), int(order[-2 if len(order) > 1 else -1]),
+                   int(order[-1])})
     pairs = [(s, h) for s in seqs for h in range(sh.num_q_heads)]
     pairs += [(int(rng.integers(sh.num_seqs)), int(rng.integers(sh.num_q_heads))) for _ in range(64)]
     pairs = np.array(pairs, np.int32)
     want = oracle_sampled(oracle, wl, pairs, wl.k_cache, wl.v_cache, wl.q)
-    for ps in (512, 256):
+    for ps in sizes:
         ref = torch.empty_like(wl.q)
         assert _reference_call(lib, wl, bt, cl, ps, ref, stream) == 0
         out = torch.full_like(wl.q, float("nan"))
