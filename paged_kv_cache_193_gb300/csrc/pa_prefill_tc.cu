@@ -14,8 +14,9 @@
 //    the V pages; lane p issues page p's 2-D TMA boxes (hardware 128-byte
 //    swizzle), with the block table read one block ahead.
 //    Warp 10 also zeroes the V rows past the context in the last block.
-//  * Warp 9 + 2 T issues tile T's MMAs (tcgen05.mma.cta_group::1.kind::f16,
-//    one thread): S = Q K^T (M 128 x N 64 x K 128; K K-major in shared
+//  * Warp 9 + 2 T issues tile T's MMAs (tcgen05.mma.cta_group::1.kind::f16):
+//    the whole warp runs the issue loop, so the operand arithmetic stays
+//    warp-uniform, and one lane chosen by elect.sync issues: S = Q K^T (M 128 x N 64 x K 128; K K-major in shared
 //    memory, query dims 0-63 from tensor memory and 64-127 from shared
 //    memory, which halves the shared-memory reads of the query), and
 //    O += P V (P read from tensor memory, V read MN-major straight from the
@@ -27,11 +28,14 @@
 //    against a reference max that only moves when the row max outgrows it
 //    by 2^8 (so O is rescaled in tensor memory rarely), and store P as bf16
 //    pairs in its own columns, which PV(j) reads.
-//  * Every wait lets the hardware suspend the waiting thread until the phase
-//    completes (try_wait with a time hint) rather than spin: the MMA threads
+//  * Every wait lets the hardware suspend the waiting threads until the phase
+//    completes (try_wait with a time hint) rather than spin: the MMA warps
 //    share their SM sub-partitions with softmax warps, and a spinning waiter
-//    takes issue slots from them.  Each wait is still bounded by the runtime
-//    limit (2 s by default).
+//    takes issue slots from them.  The MMA and loader warps wait with all 32
+//    lanes, so each parks and wakes as one (a lone waiting lane with the rest
+//    of its warp held at a warp barrier made the issue that follows several
+//    times slower).  Each wait is still bounded by the runtime limit (2 s by
+//    default).
 #include <cudaTypedefs.h>
 #include <limits.h>
 #include <math.h>
@@ -226,8 +230,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int st = kb % kTcStages, ph = (kb / kTcStages) & 1;
             const int y = page_row(e_next);
             if (kb + 1 < nkb) e_next = page_entry(kb + 1);
+            // the whole warp waits (it parks and wakes as one)
+            const bool freed = __all_sync(0xffffffffu, mbar_wait_suspend(smem_addr(&kv_empty[st]), ph ^ 1, limit));
             if (lane == 0) {
-                if (!mbar_wait_suspend(smem_addr(&kv_empty[st]), ph ^ 1, limit)) fail();
+                if (!freed) fail();
                 mbar_arrive_expect_tx(smem_addr(&kv_full[st]), kTcKVStage);
             }
             __syncwarp();
@@ -242,8 +248,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // zero those V rows before a PV reads them (P is 0 there, but
             // 0 x garbage could be NaN)
             const int kb = nkb - 1, st = kb % kTcStages;
-            if (lane == 0 && !mbar_wait_suspend(smem_addr(&kv_full[st]), (kb / kTcStages) & 1, limit)) fail();
-            __syncwarp();
+            const bool landed = mbar_wait_suspend(smem_addr(&kv_full[st]), (kb / kTcStages) & 1, limit);
+            if (!__all_sync(0xffffffffu, landed) && lane == 0) fail();
             const uint32_t vbase = base + kTcVOff + st * kTcKVStage;
             for (int r2 = kend - kb * kTcKeys + lane; r2 < kTcKeys; r2 += 32)
                 for (int sl = 0; sl < 2; ++sl)
@@ -261,12 +267,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int kb = max(0, nkb - kTcStages); kb < nkb; ++kb)
                 mbar_wait_suspend(smem_addr(&kv_full[kb % kTcStages]), (kb / kTcStages) & 1, kTcWaitNs);
     } else if (warp == kTcMmaWarp || warp == kTcMmaWarpB) {
-        // ---------------- MMA issue, one thread per tile ----------------
+        // ---------------- MMA issue, one warp per tile ----------------
         // S(j + 1) is issued once the softmax has S(j) in registers, then
         // PV(j) once P(j) is written; P has its own columns, so no S waits
         // for a PV.
         const int T = warp == kTcMmaWarp ? 0 : 1;
-        if (lane == 0 && T < ntiles) {
+        if (T < ntiles) {
             constexpr uint32_t idesc_qk = tc_idesc_bf16(kTcRows, kTcKeys, 0, 0);
             constexpr uint32_t idesc_pv = tc_idesc_bf16(kTcRows, 128, 0, 1);
             // a descriptor's start address is its low field (16-byte units,
@@ -276,26 +282,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint64_t k_desc = tc_smem_desc(base + kTcKOff, 16, 1024, 2);
             const uint64_t v_desc = tc_smem_desc(base + kTcVOff, kTcKVSlab, 1024, 2);
             const uint32_t tS = tmem + T * 256, tP = tS + kTcPCol, tQ = tS + kTcQCol, tO = tS + kTcOCol;
+            // every lane waits (the warp parks and wakes as one); a limit that
+            // runs out on any lane counts for the warp
+            auto wait = [&](uint64_t &bar, uint32_t parity) {
+                const bool r = mbar_wait_suspend(smem_addr(&bar), parity, limit);
+                return __all_sync(0xffffffffu, r) != 0;
+            };
             // test hook: give up at once on a barrier that nothing completes
-            bool ok = !a.stall_first_wait || mbar_wait_suspend(smem_addr(&stall_bar), 0, limit);
-            ok = ok && mbar_wait_suspend(smem_addr(&q_full), 0, limit) &&
-                 mbar_wait_suspend(smem_addr(&q_tmem[T]), 0, limit);
+            bool ok = !a.stall_first_wait || wait(stall_bar, 0);
+            ok = ok && wait(q_full, 0) && wait(q_tmem[T], 0);
             auto qk = [&](int kb) {  // S(kb) = Q K(kb)^T
                 const int ks = kb % kTcStages;
                 // K and V of the block: V(kb) is in place for PV(kb) too
-                ok = ok && mbar_wait_suspend(smem_addr(&kv_full[ks]), (kb / kTcStages) & 1, limit);
+                ok = ok && wait(kv_full[ks], (kb / kTcStages) & 1);
                 tc_fence_after();
                 if (ok) {
                     const uint64_t b0 = k_desc + ((ks * kTcKVStage) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)  // dims 16 kk .. 16 kk + 15: query from tensor memory
-                        tc_mma_bf16_ts(tS, tQ + kk * 8, b0 + ((kk * 32) >> 4), idesc_qk, kk > 0);
+                        tc_mma_bf16_ts_elect(tS, tQ + kk * 8, b0 + ((kk * 32) >> 4), idesc_qk, kk > 0);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)  // dims 64 + 16 kk ..: both from shared memory
-                        tc_mma_bf16(tS, q_desc + ((kk * 32) >> 4), b0 + ((kTcKVSlab + kk * 32) >> 4), idesc_qk,
-                                    true);
+                        tc_mma_bf16_elect(tS, q_desc + ((kk * 32) >> 4), b0 + ((kTcKVSlab + kk * 32) >> 4), idesc_qk,
+                                          true);
                 }
-                tc_commit(smem_addr(&s_full[T]));
+                tc_commit_elect(smem_addr(&s_full[T]));
             };
             const int nkb_t = tile_blocks(T);
             qk(0);
@@ -303,24 +314,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int vs = kb % kTcStages;
                 if (kb + 1 < nkb_t) {
                     // the softmax holds S(kb) in registers
-                    ok = ok && mbar_wait_suspend(smem_addr(&s_free[T]), kb & 1, limit);
+                    ok = ok && wait(s_free[T], kb & 1);
                     qk(kb + 1);
                 }
-                ok = ok && mbar_wait_suspend(smem_addr(&p_full[T]), kb & 1, limit);
-                if (kb == nkb - 1 && partial) ok = ok && mbar_wait_suspend(smem_addr(&v_zeroed), 0, limit);
+                ok = ok && wait(p_full[T], kb & 1);
+                if (kb == nkb - 1 && partial) ok = ok && wait(v_zeroed, 0);
                 tc_fence_after();
                 if (ok) {  // O += P(kb) V(kb)
                     const uint64_t b0 = v_desc + ((vs * kTcKVStage) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kTcKeys / 16; ++kk)
-                        tc_mma_bf16_ts(tO, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_pv, kb > 0 || kk > 0);
+                        tc_mma_bf16_ts_elect(tO, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_pv, kb > 0 || kk > 0);
                 }
-                tc_commit(smem_addr(&pv_done[T]));
+                tc_commit_elect(smem_addr(&pv_done[T]));
             }
-            if (!ok) fail();
+            if (!ok && lane == 0) fail();
             // every MMA issued above is complete before the TMEM is released
-            tc_commit(smem_addr(&drain[T]));
+            tc_commit_elect(smem_addr(&drain[T]));
             mbar_wait_suspend(smem_addr(&drain[T]), 0, kTcWaitNs);
+            __syncwarp();
         }
     } else {
         // ------------- softmax: one query row per thread, 64 keys a block -------------
