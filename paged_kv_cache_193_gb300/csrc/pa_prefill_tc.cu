@@ -8,7 +8,7 @@
 //    tiles read every K/V stage, so each SM moves half the page bytes per
 //    FLOP that one tile per CTA would.  One CTA per SM: 225 KB of shared
 //    memory (both query tiles, five K and five V stages of 64 keys) and all
-//    512 TMEM columns (per tile: S, P, the first half of the query and O).
+//    512 TMEM columns (per tile: two S buffers and O).
 //  * Thread 0 requests the query tiles (3-D TMA) as soon as the barriers
 //    exist.  Warp 8 streams the K pages of each block of 64 keys, warp 10
 //    the V pages; lane p issues page p's 2-D TMA boxes (hardware 128-byte
@@ -16,18 +16,22 @@
 //    Warp 10 also zeroes the V rows past the context in the last block.
 //  * Warp 9 + 2 T issues tile T's MMAs (tcgen05.mma.cta_group::1.kind::f16):
 //    the whole warp runs the issue loop, so the operand arithmetic stays
-//    warp-uniform, and one lane chosen by elect.sync issues: S = Q K^T (M 128 x N 64 x K 128; K K-major in shared
-//    memory, query dims 0-63 from tensor memory and 64-127 from shared
-//    memory, which halves the shared-memory reads of the query), and
-//    O += P V (P read from tensor memory, V read MN-major straight from the
-//    page layout).  Each group is committed to an mbarrier.  S(j + 1) is
-//    issued as soon as the softmax holds S(j) in registers, before PV(j).
+//    warp-uniform, and the lane elect.sync picks issues every MMA and commit
+//    (with all 32 lanes active always lane 0, so the commits track that
+//    lane's MMAs).  S = Q K^T (M 128 x N 64 x K 128; query and K both
+//    K-major in shared memory), and O += P V (P read from tensor memory, V
+//    read MN-major straight from the page layout).  S is double-buffered:
+//    S(j) goes to buffer j % 2, and S(j + 2) is issued right after PV(j), so
+//    the softmax finds S(j + 1) computed while it worked on S(j).  P(j) is
+//    written over the first half of S(j)'s buffer; the MMAs of one thread
+//    run in issue order, so S(j + 2) overwrites it only after PV(j) read
+//    it.  Each group is committed to an mbarrier, and the commit after
+//    PV(j) also releases block j's K/V stage.
 //  * Warps 4 T .. 4 T + 3 do tile T's softmax, one query row (TMEM lane) per
-//    thread: copy the row's first 64 query dims into tensor memory once,
-//    then per block read S, apply the causal mask, keep the row's sum
+//    thread: per block read S, apply the causal mask, keep the row's sum
 //    against a reference max that only moves when the row max outgrows it
 //    by 2^8 (so O is rescaled in tensor memory rarely), and store P as bf16
-//    pairs in its own columns, which PV(j) reads.
+//    pairs over S, which PV(j) reads.
 //  * Every wait lets the hardware suspend the waiting threads until the phase
 //    completes (try_wait with a time hint) rather than spin: the MMA warps
 //    share their SM sub-partitions with softmax warps, and a spinning waiter
@@ -86,11 +90,10 @@ constexpr int kTcSmem = kTcVOff + kTcStages * kTcKVStage + 1024;
 // grows past it by more than this (base-2 units): P <= 2^8, and O is
 // rescaled in tensor memory only then.
 constexpr float kTcRescaleThreshold = 8.f;
-// Tensor memory, tile T at columns [256 T, 256 T + 256): S [0, 64), P (bf16
-// pairs) [64, 96), query dims 0-63 (bf16 pairs) [96, 128), O [128, 256).
+// Tensor memory, tile T at columns [256 T, 256 T + 256): S buffers [0, 64)
+// and [64, 128) (P as bf16 pairs over the first 32 columns of its S), O
+// [128, 256).
 constexpr int kTcTmemCols = 512;
-constexpr int kTcPCol = 64;
-constexpr int kTcQCol = 96;
 constexpr int kTcOCol = 128;
 // Drain limit: after a wait gave up, the copies already issued are still
 // waited for with this before the CTA ends.
@@ -105,13 +108,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t q_full, v_zeroed;
     // kv_full[st]: both the K and the V pages of the stage's block have landed;
-    // kv_empty[st]: every tile's PV of that block is done (its QK came before),
-    // as seen by one softmax thread of each tile
+    // kv_empty[st]: every tile's PV of that block is done (its QK came
+    // before), by a commit of each tile's MMA thread
     __shared__ __align__(8) uint64_t kv_full[kTcStages], kv_empty[kTcStages];
-    // per tile: S written (s_full), S read into registers (s_free), P
-    // written (p_full), PV done (pv_done), query half in TMEM (q_tmem)
-    __shared__ __align__(8) uint64_t s_full[kTcTiles], s_free[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles],
-        q_tmem[kTcTiles], drain[kTcTiles];
+    // per tile: S written into buffer b (s_full[T][b]), P written over it
+    // (p_full[T][b]), PV done (pv_done), every MMA done (drain).  With two
+    // buffers the softmax may write P(j + 1) before the MMA thread saw P(j),
+    // so P has a barrier per buffer too: neither barrier of a buffer can
+    // complete twice before its waiter looked.
+    __shared__ __align__(8) uint64_t s_full[kTcTiles][2], p_full[kTcTiles][2], pv_done[kTcTiles],
+        drain[kTcTiles];
     __shared__ __align__(8) uint64_t stall_bar;  // never completed (wait-limit test hook)
     __shared__ uint32_t tmem_base_s;
     __shared__ int failed_s;
@@ -172,10 +178,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(smem_addr(&kv_empty[i]), ntiles);
         }
         for (int t = 0; t < kTcTiles; ++t) {
-            mbar_init(smem_addr(&s_full[t]), 1);
-            mbar_init(smem_addr(&s_free[t]), 4);  // one arrival per softmax warp
-            mbar_init(smem_addr(&p_full[t]), 4);
-            mbar_init(smem_addr(&q_tmem[t]), 4);
+            mbar_init(smem_addr(&s_full[t][0]), 1);
+            mbar_init(smem_addr(&s_full[t][1]), 1);
+            mbar_init(smem_addr(&p_full[t][0]), 4);  // one arrival per softmax warp
+            mbar_init(smem_addr(&p_full[t][1]), 4);
             mbar_init(smem_addr(&pv_done[t]), 1);
             mbar_init(smem_addr(&drain[t]), 1);
         }
@@ -230,7 +236,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int st = kb % kTcStages, ph = (kb / kTcStages) & 1;
             const int y = page_row(e_next);
             if (kb + 1 < nkb) e_next = page_entry(kb + 1);
-            // the whole warp waits (it parks and wakes as one)
             const bool freed = __all_sync(0xffffffffu, mbar_wait_suspend(smem_addr(&kv_empty[st]), ph ^ 1, limit));
             if (lane == 0) {
                 if (!freed) fail();
@@ -248,8 +253,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // zero those V rows before a PV reads them (P is 0 there, but
             // 0 x garbage could be NaN)
             const int kb = nkb - 1, st = kb % kTcStages;
-            const bool landed = mbar_wait_suspend(smem_addr(&kv_full[st]), (kb / kTcStages) & 1, limit);
-            if (!__all_sync(0xffffffffu, landed) && lane == 0) fail();
+            const bool landed = __all_sync(0xffffffffu, mbar_wait_suspend(smem_addr(&kv_full[st]), (kb / kTcStages) & 1, limit));
+            if (!landed && lane == 0) fail();
             const uint32_t vbase = base + kTcVOff + st * kTcKVStage;
             for (int r2 = kend - kb * kTcKeys + lane; r2 < kTcKeys; r2 += 32)
                 for (int sl = 0; sl < 2; ++sl)
@@ -267,10 +272,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int kb = max(0, nkb - kTcStages); kb < nkb; ++kb)
                 mbar_wait_suspend(smem_addr(&kv_full[kb % kTcStages]), (kb / kTcStages) & 1, kTcWaitNs);
     } else if (warp == kTcMmaWarp || warp == kTcMmaWarpB) {
-        // ---------------- MMA issue, one warp per tile ----------------
-        // S(j + 1) is issued once the softmax has S(j) in registers, then
-        // PV(j) once P(j) is written; P has its own columns, so no S waits
-        // for a PV.
+        // ---------------- MMA issue, one thread per tile ----------------
+        // S(0) and S(1) first; then per block j: PV(j) once P(j) is written,
+        // and S(j + 2) into the buffer P(j) came from.
         const int T = warp == kTcMmaWarp ? 0 : 1;
         if (T < ntiles) {
             constexpr uint32_t idesc_qk = tc_idesc_bf16(kTcRows, kTcKeys, 0, 0);
@@ -278,20 +282,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // a descriptor's start address is its low field (16-byte units,
             // no carry out within shared memory): every operand descriptor is
             // a base descriptor plus an offset, so issuing an MMA costs one add
-            const uint64_t q_desc = tc_smem_desc(base + kTcQOff + T * kTcQTile + kTcQSlab, 16, 1024, 2);
+            const uint64_t q_desc = tc_smem_desc(base + kTcQOff + T * kTcQTile, 16, 1024, 2);
             const uint64_t k_desc = tc_smem_desc(base + kTcKOff, 16, 1024, 2);
             const uint64_t v_desc = tc_smem_desc(base + kTcVOff, kTcKVSlab, 1024, 2);
-            const uint32_t tS = tmem + T * 256, tP = tS + kTcPCol, tQ = tS + kTcQCol, tO = tS + kTcOCol;
-            // every lane waits (the warp parks and wakes as one); a limit that
-            // runs out on any lane counts for the warp
+            const uint32_t tS = tmem + T * 256, tO = tS + kTcOCol;
             auto wait = [&](uint64_t &bar, uint32_t parity) {
-                const bool r = mbar_wait_suspend(smem_addr(&bar), parity, limit);
-                return __all_sync(0xffffffffu, r) != 0;
+                return __all_sync(0xffffffffu, mbar_wait_suspend(smem_addr(&bar), parity, limit)) != 0;
             };
             // test hook: give up at once on a barrier that nothing completes
             bool ok = !a.stall_first_wait || wait(stall_bar, 0);
-            ok = ok && wait(q_full, 0) && wait(q_tmem[T], 0);
-            auto qk = [&](int kb) {  // S(kb) = Q K(kb)^T
+            ok = ok && wait(q_full, 0);
+            auto qk = [&](int kb) {  // S(kb) = Q K(kb)^T into buffer kb % 2
                 const int ks = kb % kTcStages;
                 // K and V of the block: V(kb) is in place for PV(kb) too
                 ok = ok && wait(kv_full[ks], (kb / kTcStages) & 1);
@@ -299,34 +300,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (ok) {
                     const uint64_t b0 = k_desc + ((ks * kTcKVStage) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)  // dims 16 kk .. 16 kk + 15: query from tensor memory
-                        tc_mma_bf16_ts_elect(tS, tQ + kk * 8, b0 + ((kk * 32) >> 4), idesc_qk, kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)  // dims 64 + 16 kk ..: both from shared memory
-                        tc_mma_bf16_elect(tS, q_desc + ((kk * 32) >> 4), b0 + ((kTcKVSlab + kk * 32) >> 4), idesc_qk,
-                                          true);
+                    for (int kk = 0; kk < 8; ++kk) {  // dims 16 kk .. 16 kk + 15
+                        const int qoff = (kk >> 2) * kTcQSlab + (kk & 3) * 32;
+                        const int koff = (kk >> 2) * kTcKVSlab + (kk & 3) * 32;
+                        tc_mma_bf16_elect(tS + (kb & 1) * kTcKeys, q_desc + (qoff >> 4), b0 + (koff >> 4),
+                                          idesc_qk, kk > 0);
+                    }
                 }
-                tc_commit_elect(smem_addr(&s_full[T]));
+                tc_commit_elect(smem_addr(&s_full[T][kb & 1]));
             };
             const int nkb_t = tile_blocks(T);
             qk(0);
+            if (nkb_t > 1) qk(1);
             for (int kb = 0; kb < nkb_t; ++kb) {
                 const int vs = kb % kTcStages;
-                if (kb + 1 < nkb_t) {
-                    // the softmax holds S(kb) in registers
-                    ok = ok && wait(s_free[T], kb & 1);
-                    qk(kb + 1);
-                }
-                ok = ok && wait(p_full[T], kb & 1);
+                ok = ok && wait(p_full[T][kb & 1], (kb >> 1) & 1);
                 if (kb == nkb - 1 && partial) ok = ok && wait(v_zeroed, 0);
                 tc_fence_after();
                 if (ok) {  // O += P(kb) V(kb)
                     const uint64_t b0 = v_desc + ((vs * kTcKVStage) >> 4);
+                    const uint32_t tP = tS + (kb & 1) * kTcKeys;
 #pragma unroll
                     for (int kk = 0; kk < kTcKeys / 16; ++kk)
-                        tc_mma_bf16_ts_elect(tO, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_pv, kb > 0 || kk > 0);
+                        tc_mma_bf16_ts_elect(tO, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_pv,
+                                             kb > 0 || kk > 0);
                 }
                 tc_commit_elect(smem_addr(&pv_done[T]));
+                // this tile is done with block kb's stage once PV(kb) is
+                tc_commit_elect(smem_addr(&kv_empty[vs]));
+                if (kb + 2 < nkb_t) qk(kb + 2);
             }
             if (!ok && lane == 0) fail();
             // every MMA issued above is complete before the TMEM is released
@@ -346,41 +348,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // blocks ending at or before every row's position need no mask
             const int warp_min_pos = __reduce_min_sync(0xffffffffu, pos);
             const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-            const uint32_t tS = tmem + lane_addr + T * 256, tP = tS + kTcPCol, tO = tS + kTcOCol;
+            const uint32_t tS = tmem + lane_addr + T * 256, tO = tS + kTcOCol;
             const float scale = a.score_scale;
             float m_ref = -INFINITY, l_run = 0.f;
+            // the query tile has landed before its shared memory stages the output
             bool ok = mbar_wait_suspend(smem_addr(&q_full), 0, limit);
-            {
-                // the row's query dims 0-63 (128-byte swizzled in shared
-                // memory) as bf16 pairs in tensor memory: the A operand of
-                // QK's first four MMAs
-                const uint32_t qrow = base + kTcQOff + T * kTcQTile + row * 128;
-                uint32_t w[32];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint4 c = lds128(qrow + ((j ^ (row & 7)) << 4));
-                    w[4 * j] = c.x;
-                    w[4 * j + 1] = c.y;
-                    w[4 * j + 2] = c.z;
-                    w[4 * j + 3] = c.w;
-                }
-                tc_st32(tS + kTcQCol, w);
-                tc_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&q_tmem[T]));
-            }
             const int nkb_t = tile_blocks(T);
             for (int kb = 0; kb < nkb_t; ++kb) {
                 const int key0 = kb * kTcKeys;
                 const bool masked = key0 + kTcKeys - 1 > warp_min_pos;
-                ok = ok && mbar_wait_suspend(smem_addr(&s_full[T]), kb & 1, limit);
+                const uint32_t tSb = tS + (kb & 1) * kTcKeys;  // S(kb), then P(kb)
+                ok = ok && mbar_wait_suspend(smem_addr(&s_full[T][kb & 1]), (kb >> 1) & 1, limit);
                 tc_fence_after();
                 float v[64];
                 {
                     float lo[32], hi[32];
-                    tc_ld32(tS, lo);
-                    tc_ld32(tS + 32, hi);
+                    tc_ld32(tSb, lo);
+                    tc_ld32(tSb + 32, hi);
                     tc_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -388,10 +372,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         v[32 + i] = hi[i];
                     }
                 }
-                // S may now be overwritten by S(kb + 1)
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&s_free[T]));
                 if (masked) {
 #pragma unroll
                     for (int i = 0; i < 64; ++i) v[i] = key0 + i <= pos ? v[i] : -INFINITY;
@@ -416,7 +396,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     rescale = kb > 0;
                 }
                 if (__any_sync(0xffffffffu, rescale)) {
-                    // O must hold PV(kb - 1) before it is scaled
+                    // O must hold PV(kb - 1) before it is scaled.  PV(kb - 2)
+                    // completed before S(kb) (issued after it) was committed,
+                    // and PV(kb) waits for this P: the barrier is at most one
+                    // phase away, so its parity is unambiguous.
                     ok = ok && mbar_wait_suspend(smem_addr(&pv_done[T]), (kb - 1) & 1, limit);
                     tc_fence_after();
 #pragma unroll
@@ -447,18 +430,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) pk[i] = pack2<false>(v[2 * i], v[2 * i + 1]);
-                if (kb > 0) {  // PV(kb - 1) has read P(kb - 1), and K and V of block kb - 1
-                    ok = ok && mbar_wait_suspend(smem_addr(&pv_done[T]), (kb - 1) & 1, limit);
-                    tc_fence_after();
-                    // the tile's release of that block's stage (the last
-                    // block's stage is never reused, so it is not released)
-                    if ((warp & 3) == 0 && lane == 0) mbar_arrive(smem_addr(&kv_empty[(kb - 1) % kTcStages]));
-                }
-                tc_st32(tP, pk);
+                // over S(kb), which this thread holds in registers; no MMA
+                // writes this buffer before PV(kb), which waits for P
+                tc_st32(tSb, pk);
                 tc_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&p_full[T]));
+                if (lane == 0) mbar_arrive(smem_addr(&p_full[T][kb & 1]));
             }
             // every PV is done once the tile's MMA thread's final commit lands
             ok = ok && mbar_wait_suspend(smem_addr(&drain[T]), 0, limit);
