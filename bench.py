@@ -100,6 +100,8 @@ def parse():
                     help="time chunked prefill (16 sequences x 512-token chunks) instead of decode")
     ap.add_argument("--q-heads", type=int, default=32, help="prefill: query heads (default 32)")
     ap.add_argument("--kv-heads", type=int, default=8, help="prefill: KV heads (default 8)")
+    ap.add_argument("--head-dim", type=int, default=128, choices=(64, 128),
+                    help="prefill: head dim (default 128)")
     ap.add_argument("--separate", action="store_true",
                     help="time the unfused entry points (3-4 kernels per step)")
     ap.add_argument("--no-secondary", action="store_true",
@@ -950,7 +952,7 @@ def run_prefill(args):
     init_dist(world, "nccl")
     from paged_kv_cache_193_gb300 import api
     wl = W.make_prefill(device, num_seqs=args.num_seqs or 16, block_size=args.block_size or 16,
-                        num_q_heads=args.q_heads, num_kv_heads=args.kv_heads)
+                        num_q_heads=args.q_heads, num_kv_heads=args.kv_heads, head_dim=args.head_dim)
     sh = wl.shape
     bt = torch.from_numpy(wl.block_tables).to(device)
     cl = torch.from_numpy(wl.context_lens).to(device)

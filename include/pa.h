@@ -349,8 +349,8 @@ pa_status pa_decode_step_fp8_qk(const void *q, const void *k_new, const void *v_
  *   max_query_len >= every C_s (host-side bound used for the grid).
  *   Supported: bf16 cache, group 1, 2, 4, 8 or 16, head_dim 64/128, block 16/32,
  *   softmax_scale > 0 (PA_ERR_UNSUPPORTED otherwise).
- *   One kernel: for head_dim 128 on the tcgen05 tensor cores (accumulators
- *   in tensor memory), otherwise with warp-level MMA.  kv_scale is unused.
+ *   One kernel on the tcgen05 tensor cores (accumulators in tensor
+ *   memory), head_dim 64 or 128.  kv_scale is unused.
  * pa_prefill_mma: the same computation always with the warp-level MMA
  *   kernel (kept as the comparison point for the tensor-memory kernel).
  */

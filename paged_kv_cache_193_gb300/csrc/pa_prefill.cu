@@ -340,7 +340,7 @@ pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_ca
                             const int32_t *block_tables, int max_blocks_per_seq,
                             const int32_t *context_lens, const int32_t *query_start, int num_seqs,
                             int total_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
-                            int num_blocks, int block_size, float softmax_scale, void *out,
+                            int head_dim, int num_blocks, int block_size, float softmax_scale, void *out,
                             unsigned int *err, cudaStream_t stream);
 static pa_status prefill_impl(const void *q, const void *k_cache, const void *v_cache,
                               const int32_t *block_tables, int max_blocks_per_seq,
@@ -443,11 +443,11 @@ static pa_status prefill_impl(const void *q, const void *k_cache, const void *v_
         return fail(PA_ERR_INVALID_ARG, "q, caches and out must be 16-byte aligned");
     unsigned int *err0 = device_error_word();
     if (!err0) return fail(PA_ERR_CUDA, "cannot resolve the device error word");
-    if (tensor_memory && head_dim == 128)
+    if (tensor_memory)
         return launch_prefill_tc(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                  context_lens, query_start, num_seqs, num_tokens, max_query_len,
-                                 num_q_heads, num_kv_heads, num_blocks, block_size, softmax_scale,
-                                 out, err0, stream);
+                                 num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                                 softmax_scale, out, err0, stream);
     const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
     CUtensorMap tk, tv;
     pa_status st = make_map(&tk, k_cache, false, head_dim, rows, block_size);

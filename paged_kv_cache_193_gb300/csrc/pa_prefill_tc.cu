@@ -6,9 +6,10 @@
 //  * One CTA per (two neighbouring query tiles, KV head, sequence).  A tile is
 //    128 rows = (chunk token, query head of the KV head's group) pairs; both
 //    tiles read every K/V stage, so each SM moves half the page bytes per
-//    FLOP that one tile per CTA would.  One CTA per SM: 225 KB of shared
-//    memory (both query tiles, five K and five V stages of 64 keys) and all
-//    512 TMEM columns (per tile: two S buffers and O).
+//    FLOP that one tile per CTA would.  One CTA per SM: at head dim 128,
+//    225 KB of shared memory (both query tiles, five K and five V stages of
+//    64 keys; at head dim 64, ten stages of half the size) and all 512 TMEM
+//    columns (per tile: two S buffers and O).
 //  * Thread 0 requests the query tiles (3-D TMA) as soon as the barriers
 //    exist.  Warp 8 streams the K pages of each block of 64 keys, warp 10
 //    the V pages; lane p issues page p's 2-D TMA boxes (hardware 128-byte
@@ -18,7 +19,7 @@
 //    the whole warp runs the issue loop, so the operand arithmetic stays
 //    warp-uniform, and the lane elect.sync picks issues every MMA and commit
 //    (with all 32 lanes active always lane 0, so the commits track that
-//    lane's MMAs).  S = Q K^T (M 128 x N 64 x K 128; query and K both
+//    lane's MMAs).  S = Q K^T (M 128 x N 64 x K head dim; query and K both
 //    K-major in shared memory), and O += P V (P read from tensor memory, V
 //    read MN-major straight from the page layout).  S is double-buffered:
 //    S(j) goes to buffer j % 2, and S(j + 2) is issued right after PV(j), so
@@ -78,14 +79,21 @@ constexpr int kTcMmaWarp = 9;
 constexpr int kTcVLoadWarp = 10;
 constexpr int kTcMmaWarpB = 11;
 constexpr int kTcQSlab = 16384;       // 64 dims of a 128-row query tile
-constexpr int kTcQTile = 2 * kTcQSlab;
 constexpr int kTcKVSlab = kTcKeys * 128;  // 64 dims of a 64-key block
-constexpr int kTcKVStage = 2 * kTcKVSlab;
-constexpr int kTcStages = 5;          // K and V rings
 constexpr int kTcQOff = 0;                            // one query tile after the other
-constexpr int kTcKOff = kTcTiles * kTcQTile;
-constexpr int kTcVOff = kTcKOff + kTcStages * kTcKVStage;
-constexpr int kTcSmem = kTcVOff + kTcStages * kTcKVStage + 1024;
+// Shared memory for head dim D (64 or 128): every operand is stored as
+// 64-dim slabs of 128-byte rows (the swizzle span).  At head dim 64 a stage
+// is half the size, so the rings hold twice the blocks.
+template <int D>
+struct TcLayout {
+    static constexpr int kSlabs = D / 64;
+    static constexpr int kQTile = kSlabs * kTcQSlab;
+    static constexpr int kKVStage = kSlabs * kTcKVSlab;
+    static constexpr int kStages = D == 128 ? 5 : 10;  // K and V rings
+    static constexpr int kKOff = kTcTiles * kQTile;
+    static constexpr int kVOff = kKOff + kStages * kKVStage;
+    static constexpr int kSmem = kVOff + kStages * kKVStage + 1024;
+};
 // P is written against a reference max that only moves when the row max
 // grows past it by more than this (base-2 units): P <= 2^8, and O is
 // rescaled in tensor memory only then.
@@ -99,12 +107,15 @@ constexpr int kTcOCol = 128;
 // waited for with this before the CTA ends.
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 
-template <int BS>
+template <int D, int BS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                       const PrefillTcArgs a) {
     constexpr int NPG = kTcKeys / BS;  // pages per key block
+    using L = TcLayout<D>;
+    constexpr int kSlabs = L::kSlabs, kTcQTile = L::kQTile, kTcKVStage = L::kKVStage, kTcStages = L::kStages;
+    constexpr int kTcKOff = L::kKOff, kTcVOff = L::kVOff;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t q_full, v_zeroed;
     // kv_full[st]: both the K and the V pages of the stage's block have landed;
@@ -190,7 +201,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // the query tiles are requested before the tensor-memory setup
         mbar_arrive_expect_tx(smem_addr(&q_full), ntiles * kTcQTile);
         for (int T = 0; T < ntiles; ++T)
-            for (int sl = 0; sl < 2; ++sl)
+            for (int sl = 0; sl < kSlabs; ++sl)
                 tma_load_3d(base + kTcQOff + T * kTcQTile + sl * kTcQSlab, &tmQ, sl * 64, h * a.group,
                             q0 + tok_begin0 + T * a.tile_tokens, smem_addr(&q_full));
         prefetch_tensormap(&tmK);
@@ -243,7 +254,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             __syncwarp();
             if (lane < NPG) {
-                for (int sl = 0; sl < 2; ++sl)
+                for (int sl = 0; sl < kSlabs; ++sl)
                     tma_load_2d(ring + st * kTcKVStage + sl * kTcKVSlab + lane * BS * 128, map, sl * 64, y,
                                 smem_addr(&kv_full[st]), policy);
             }
@@ -257,7 +268,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!landed && lane == 0) fail();
             const uint32_t vbase = base + kTcVOff + st * kTcKVStage;
             for (int r2 = kend - kb * kTcKeys + lane; r2 < kTcKeys; r2 += 32)
-                for (int sl = 0; sl < 2; ++sl)
+                for (int sl = 0; sl < kSlabs; ++sl)
                     for (int c16 = 0; c16 < 8; ++c16)
                         st_shared_zero16(vbase + sl * kTcKVSlab + r2 * 128 + c16 * 16);
             fence_proxy_async_smem();
@@ -278,7 +289,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int T = warp == kTcMmaWarp ? 0 : 1;
         if (T < ntiles) {
             constexpr uint32_t idesc_qk = tc_idesc_bf16(kTcRows, kTcKeys, 0, 0);
-            constexpr uint32_t idesc_pv = tc_idesc_bf16(kTcRows, 128, 0, 1);
+            constexpr uint32_t idesc_pv = tc_idesc_bf16(kTcRows, D, 0, 1);
             // a descriptor's start address is its low field (16-byte units,
             // no carry out within shared memory): every operand descriptor is
             // a base descriptor plus an offset, so issuing an MMA costs one add
@@ -300,7 +311,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (ok) {
                     const uint64_t b0 = k_desc + ((ks * kTcKVStage) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {  // dims 16 kk .. 16 kk + 15
+                    for (int kk = 0; kk < D / 16; ++kk) {  // dims 16 kk .. 16 kk + 15
                         const int qoff = (kk >> 2) * kTcQSlab + (kk & 3) * 32;
                         const int koff = (kk >> 2) * kTcKVSlab + (kk & 3) * 32;
                         tc_mma_bf16_elect(tS + (kb & 1) * kTcKeys, q_desc + (qoff >> 4), b0 + (koff >> 4),
@@ -403,7 +414,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ok = ok && mbar_wait_suspend(smem_addr(&pv_done[T]), (kb - 1) & 1, limit);
                     tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < 128; c += 32) {
+                    for (int c = 0; c < D; c += 32) {
                         float o[32];
                         tc_ld32(tO + c, o);
                         tc_wait_ld();
@@ -450,9 +461,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool full_tile = tok_begin + a.tile_tokens <= chunk;
             const uint32_t stage = base + kTcQOff + T * kTcQTile;
             __nv_bfloat16 *dst = a.out + ((static_cast<int64_t>(q0) + tok_begin + t) * a.num_q_heads +
-                                          h * a.group + g) * 128;
+                                          h * a.group + g) * D;
 #pragma unroll
-            for (int c = 0; c < 128; c += 32) {
+            for (int c = 0; c < D; c += 32) {
                 float o[32];
                 tc_ld32(tO + c, o);
                 tc_wait_ld();
@@ -474,7 +485,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 fence_proxy_async_smem();
                 asm volatile("bar.sync %0, 128;" ::"r"(1 + T) : "memory");  // the tile's four softmax warps
                 if ((warp & 3) == 0 && lane == 0) {
-                    for (int sl = 0; sl < 2; ++sl)
+                    for (int sl = 0; sl < kSlabs; ++sl)
                         tma_store_3d(&tmO, sl * 64, h * a.group, q0 + tok_begin, stage + sl * kTcQSlab);
                     tma_store_commit_and_wait_read();
                 }
@@ -495,7 +506,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // Queries [Tq][Hq][D] as a 3-D tensor (D, Hq, Tq); one box is 64 dims x
 // `group` heads x `tile_tokens` tokens with the 128-byte swizzle.
 static pa_status make_q_map(CUtensorMap *map, const void *q, int total_tokens, int num_q_heads,
-                            int group, int tile_tokens) {
+                            int head_dim, int group, int tile_tokens) {
     void *p = nullptr;
     cudaDriverEntryPointQueryResult qr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) !=
@@ -503,8 +514,10 @@ static pa_status make_q_map(CUtensorMap *map, const void *q, int total_tokens, i
         qr != cudaDriverEntryPointSuccess)
         return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(num_q_heads), static_cast<cuuint64_t>(total_tokens)};
-    cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(num_q_heads) * 128 * 2};
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_q_heads),
+                          static_cast<cuuint64_t>(total_tokens)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                             static_cast<cuuint64_t>(num_q_heads) * head_dim * 2};
     cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(tile_tokens)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box,
@@ -514,11 +527,12 @@ static pa_status make_q_map(CUtensorMap *map, const void *q, int total_tokens, i
     return PA_OK;
 }
 
-template <int BS>
+template <int D, int BS>
 static pa_status launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const CUtensorMap &to,
                            const PrefillTcArgs &a, dim3 grid, cudaStream_t stream) {
-    auto kern = prefill_tc_kernel<BS>;
+    auto kern = prefill_tc_kernel<D, BS>;
+    constexpr int kTcSmem = TcLayout<D>::kSmem;
     static std::atomic<uint64_t> raised{0};
     int dev = 0;
     pa_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
@@ -534,12 +548,12 @@ static pa_status launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const C
     return cuda_check(cudaGetLastError(), "prefill tcgen05 launch");
 }
 
-// Called by pa_prefill for head_dim 128 (arguments already checked).
+// Called by pa_prefill for head_dim 64 and 128 (arguments already checked).
 pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_cache,
                             const int32_t *block_tables, int max_blocks_per_seq,
                             const int32_t *context_lens, const int32_t *query_start, int num_seqs,
                             int total_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
-                            int num_blocks, int block_size, float softmax_scale, void *out,
+                            int head_dim, int num_blocks, int block_size, float softmax_scale, void *out,
                             unsigned int *err, cudaStream_t stream) {
     const int group = num_q_heads / num_kv_heads;
     PrefillTcArgs a;
@@ -559,18 +573,21 @@ pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_ca
     a.err = err;
     const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
     CUtensorMap tq, tk, tv, to;
-    pa_status st = make_q_map(&tq, q, total_tokens, num_q_heads, group, a.tile_tokens);
+    pa_status st = make_q_map(&tq, q, total_tokens, num_q_heads, head_dim, group, a.tile_tokens);
     if (st != PA_OK) return st;
-    st = make_q_map(&to, out, total_tokens, num_q_heads, group, a.tile_tokens);  // same geometry
+    st = make_q_map(&to, out, total_tokens, num_q_heads, head_dim, group, a.tile_tokens);  // same geometry
     if (st != PA_OK) return st;
-    st = make_map(&tk, k_cache, false, 128, rows, block_size);
+    st = make_map(&tk, k_cache, false, head_dim, rows, block_size);
     if (st != PA_OK) return st;
-    st = make_map(&tv, v_cache, false, 128, rows, block_size);
+    st = make_map(&tv, v_cache, false, head_dim, rows, block_size);
     if (st != PA_OK) return st;
     const int tiles = (max_query_len + a.tile_tokens - 1) / a.tile_tokens;
     dim3 grid((tiles + kTcTiles - 1) / kTcTiles, num_kv_heads, num_seqs);
-    return block_size == 16 ? launch_tc<16>(tq, tk, tv, to, a, grid, stream)
-                            : launch_tc<32>(tq, tk, tv, to, a, grid, stream);
+    if (head_dim == 64)
+        return block_size == 16 ? launch_tc<64, 16>(tq, tk, tv, to, a, grid, stream)
+                                : launch_tc<64, 32>(tq, tk, tv, to, a, grid, stream);
+    return block_size == 16 ? launch_tc<128, 16>(tq, tk, tv, to, a, grid, stream)
+                            : launch_tc<128, 32>(tq, tk, tv, to, a, grid, stream);
 }
 
 }  // namespace pa
