@@ -64,6 +64,8 @@ struct PrefillTcArgs {
     float score_scale;
     uint64_t wait_limit_ns;  // give up on a wait after this long
     int stall_first_wait;    // test hook: the MMA threads' first wait is on a barrier nothing completes
+    int num_seqs;
+    int longest_first;       // sequences run longest context first (grids of under two waves, <= 32 sequences)
     __nv_bfloat16 *out;
     unsigned int *err;
 };
@@ -138,8 +140,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint64_t limit = a.wait_limit_ns;
 
     const int pair = gridDim.x - 1 - blockIdx.x;  // tiles 2 pair and 2 pair + 1
-    const int h = blockIdx.y, s = blockIdx.z;
+    const int h = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // With few CTAs per SM the last wave decides the launch's length: then
+    // blockIdx.z takes the sequences longest context first (ties by index),
+    // a sequence's tile pairs staying next to each other.  Every warp ranks
+    // the (at most 32) contexts itself: lane j holds sequence j's.
+    int s = blockIdx.z;
+    if (a.longest_first) {
+        const int cj = lane < a.num_seqs ? a.context_lens[lane] : INT_MIN;
+        int rank = 0;
+        for (int j = 0; j < a.num_seqs; ++j) {
+            const int ck = __shfl_sync(0xffffffffu, cj, j);
+            rank += ck > cj || (ck == cj && j < lane);
+        }
+        s = __ffs(__ballot_sync(0xffffffffu, lane < a.num_seqs && rank == static_cast<int>(blockIdx.z))) - 1;
+    }
     const int q0 = a.query_start[s];
     const int chunk = a.query_start[s + 1] - q0;
     const int ctx = a.context_lens[s];
@@ -569,6 +585,7 @@ pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_ca
     a.score_scale = softmax_scale * 1.4426950408889634f;
     a.wait_limit_ns = wait_limit_ns();
     a.stall_first_wait = stall_first_wait();
+    a.num_seqs = num_seqs;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.err = err;
     const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
@@ -583,6 +600,10 @@ pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_ca
     if (st != PA_OK) return st;
     const int tiles = (max_query_len + a.tile_tokens - 1) / a.tile_tokens;
     dim3 grid((tiles + kTcTiles - 1) / kTcTiles, num_kv_heads, num_seqs);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return fail(PA_ERR_CUDA, "cannot read the SM count");
+    a.longest_first = num_seqs <= 32 && static_cast<int64_t>(grid.x) * grid.y * grid.z < 2LL * sms;
     if (head_dim == 64)
         return block_size == 16 ? launch_tc<64, 16>(tq, tk, tv, to, a, grid, stream)
                                 : launch_tc<64, 32>(tq, tk, tv, to, a, grid, stream);
