@@ -64,8 +64,9 @@ def test_prefill_matches_oracle(api, oracle, cuda_device, D, B, G, Hkv, kernel):
     assert api.device_errors() == 0
 
 
-@pytest.mark.parametrize("G,Hkv,B", [(4, 2, 16), (16, 1, 32), (1, 4, 16)])
-def test_prefill_many_items_matches_oracle(api, oracle, cuda_device, G, Hkv, B):
+@pytest.mark.parametrize("G,Hkv,B,D", [(4, 2, 16, 128), (16, 1, 32, 128), (1, 4, 16, 128), (4, 2, 16, 64),
+                                       (1, 4, 32, 64)])
+def test_prefill_many_items_matches_oracle(api, oracle, cuda_device, G, Hkv, B, D):
     """Several waves of (query-tile pair, KV head, sequence) blocks over 48
     sequences with ragged chunks and prefixes: blocks with no rows, with one
     tile, with a partial tile and with a partial last key block, all checked
@@ -74,14 +75,36 @@ def test_prefill_many_items_matches_oracle(api, oracle, cuda_device, G, Hkv, B):
     S = 48
     chunks = rng.integers(1, 200, size=S, endpoint=True).tolist()
     prefixes = rng.integers(16, 300, size=S, endpoint=True).tolist()
-    wl = W.make_prefill(cuda_device, seed=G + Hkv + B, num_seqs=S, chunk=chunks, prefixes=prefixes,
-                        num_q_heads=G * Hkv, num_kv_heads=Hkv, head_dim=128, block_size=B)
+    wl = W.make_prefill(cuda_device, seed=G + Hkv + B + D, num_seqs=S, chunk=chunks, prefixes=prefixes,
+                        num_q_heads=G * Hkv, num_kv_heads=Hkv, head_dim=D, block_size=B)
     W.poison_prefill(wl)
     api.device_errors(clear=True)
     slots_ref, kc_ref, vc_ref, ref = _oracle_step(oracle, wl)
     slots, out = _gpu_step(api, wl, cuda_device, "auto")
     assert np.array_equal(slots, slots_ref)
-    compare(out, ref, what=f"prefill many items G{G} B{B}")
+    compare(out, ref, what=f"prefill many items G{G} B{B} D{D}")
+    assert api.device_errors() == 0
+
+
+@pytest.mark.parametrize("S,ties", [(8, True), (32, False), (33, False), (32, True)])
+def test_prefill_sequence_order(api, oracle, cuda_device, S, ties):
+    """Grids of under two waves run their sequences longest context first,
+    ranked inside the kernel (up to 32 sequences; 33 keep the launch order).
+    Equal contexts rank by index.  Every sequence is computed exactly once,
+    so each output row matches the oracle."""
+    rng = np.random.default_rng(200 + S)
+    chunks = [40] * S if ties else rng.integers(1, 90, size=S, endpoint=True).tolist()
+    prefixes = [100] * S if ties else rng.integers(0, 400, size=S, endpoint=True).tolist()
+    if ties and S > 8:
+        prefixes[S // 2] = 300  # one longer among equal ones
+    wl = W.make_prefill(cuda_device, seed=300 + S, num_seqs=S, chunk=chunks, prefixes=prefixes,
+                        num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16)
+    W.poison_prefill(wl)
+    api.device_errors(clear=True)
+    slots_ref, kc_ref, vc_ref, ref = _oracle_step(oracle, wl)
+    slots, out = _gpu_step(api, wl, cuda_device, "auto")
+    assert np.array_equal(slots, slots_ref)
+    compare(out, ref, what=f"prefill sequence order S{S} ties={ties}")
     assert api.device_errors() == 0
 
 

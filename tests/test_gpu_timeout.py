@@ -77,12 +77,12 @@ def test_wait_limit_is_validated():
     assert lib.pa_test_set_wait(0, 0) == _lib.PA_OK
 
 
-@pytest.mark.parametrize("G,Hkv,B", [(4, 2, 16), (1, 4, 32), (16, 1, 16)])
-def test_prefill_wait_runs_out_then_recovers(api, oracle, cuda_device, G, Hkv, B):
+@pytest.mark.parametrize("G,Hkv,B,D", [(4, 2, 16, 128), (1, 4, 32, 128), (16, 1, 16, 128), (4, 2, 16, 64)])
+def test_prefill_wait_runs_out_then_recovers(api, oracle, cuda_device, G, Hkv, B, D):
     lib = _lib.load()
     wl = W.make_prefill(cuda_device, seed=40 + G + B, num_seqs=5, chunk=[1, 7, 64, 300, 33],
                         prefixes=[0, 5, 33, 300, 16], num_q_heads=G * Hkv, num_kv_heads=Hkv,
-                        head_dim=128, block_size=B)
+                        head_dim=D, block_size=B)
     W.poison_prefill(wl)
     _, _, _, ref = _oracle_prefill(oracle, wl)
     bt, cl, qs = _dev(wl, cuda_device)
@@ -98,5 +98,5 @@ def test_prefill_wait_runs_out_then_recovers(api, oracle, cuda_device, G, Hkv, B
     # the next call, at the default limit, is correct
     out = api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, wl.max_query_len, wl.softmax_scale)
     torch.cuda.synchronize()
-    compare(out, ref, what=f"prefill G{G} B{B} after a timed-out call")
+    compare(out, ref, what=f"prefill G{G} B{B} D{D} after a timed-out call")
     assert api.device_errors() == 0
