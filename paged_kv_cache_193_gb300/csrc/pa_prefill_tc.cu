@@ -9,7 +9,8 @@
 //    FLOP that one tile per CTA would.  One CTA per SM: at head dim 128,
 //    225 KB of shared memory (both query tiles, five K and five V stages of
 //    64 keys; at head dim 64, ten stages of half the size) and all 512 TMEM
-//    columns (per tile: two S buffers and O).
+//    columns (per tile: two S buffers and O).  A grid of under two waves
+//    takes its sequences longest context first.
 //  * Thread 0 requests the query tiles (3-D TMA) as soon as the barriers
 //    exist.  Warp 8 streams the K pages of each block of 64 keys, warp 10
 //    the V pages; lane p issues page p's 2-D TMA boxes (hardware 128-byte
@@ -74,7 +75,7 @@ constexpr int kTcRows = 128;          // query rows per tile (TMEM lanes)
 constexpr int kTcKeys = 64;           // keys per block
 constexpr int kTcTiles = 2;           // query tiles per CTA; both read every K/V stage
 // warps 0-3 softmax of tile 0 and 4-7 of tile 1 (one query row per thread),
-// 8 Q/K loads, 9 and 11 the MMAs of tiles 0 and 1, 10 V loads
+// 8 K loads, 9 and 11 the MMAs of tiles 0 and 1, 10 V loads (thread 0 requests the queries)
 constexpr int kTcThreads = 384;
 constexpr int kTcLoadWarp = 8;
 constexpr int kTcMmaWarp = 9;
