@@ -347,7 +347,7 @@ def cpu_baseline(wl, budget_s: float):
                       f"{t_total:.1f} s wall"}
 
 
-def cpu_baseline_prefill(wl, budget_s: float):
+def cpu_baseline_prefill(wl, budget_s: float, kv_scale=None):
     """The oracle's chunked-prefill attention (as it stands) on growing
     subsets of the step's sequences until the wall-time budget is used;
     TFLOP/s over the causal pairs it processed."""
@@ -366,7 +366,8 @@ def cpu_baseline_prefill(wl, budget_s: float):
         ctx = wl.context_lens[seqs].astype(np.int32)
         t0 = time.perf_counter()
         o.prefill(qb[np.concatenate(rows)], kc, vc, wl.block_tables[seqs], ctx, qs, sh.num_kv_heads,
-                  sh.block_size, wl.softmax_scale)
+                  sh.block_size, wl.softmax_scale, kv_dtype=0 if kv_scale is None else 1,
+                  kv_scale=1.0 if kv_scale is None else kv_scale)
         t_total += time.perf_counter() - t0
         pairs = sum(int(c) - int(ch) + k + 1 for c, ch in zip(ctx, chunks) for k in range(int(ch)))
         flops += 4 * sh.head_dim * sh.num_q_heads * pairs
@@ -411,7 +412,7 @@ def recorded_traffic(wl, ps, args):
     return entry.get("dram_bytes_per_launch")
 
 
-def recorded_prefill_traffic(sh, mq, num_seqs):
+def recorded_prefill_traffic(sh, mq, num_seqs, fp8=False):
     """DRAM bytes per tcgen05 prefill launch from a committed ncu capture of
     the same kernel source and workload shape, else None."""
     try:
@@ -420,6 +421,8 @@ def recorded_prefill_traffic(sh, mq, num_seqs):
     except (OSError, ValueError):
         return None
     key = f"S{num_seqs}/C{mq}/H{sh.num_q_heads}/KV{sh.num_kv_heads}/D{sh.head_dim}/B{sh.block_size}"
+    if fp8:
+        key += "/e4m3"
     entry = rec.get(key)
     if not entry or entry.get("source_digest") != source_digest(PREFILL_SOURCES):
         return None
@@ -854,7 +857,7 @@ def run_reference(args):
     print(json.dumps(result), flush=True)
 
 
-def run_prefill_e2e(api, wl, bt, K, world, device):
+def run_prefill_e2e(api, wl, bt, K, world, device, kv_scale=1.0):
     """The prefill metric through the public API with the step's inputs in
     pinned host memory: the queries, the chunk's new K/V rows, the context
     lengths and the chunk offsets are copied in, the step runs (chunk slots,
@@ -887,9 +890,9 @@ def run_prefill_e2e(api, wl, bt, K, world, device):
     def step_on(d_in, d_slots, d_out):
         d_q, d_k, d_v, d_cl, d_qs = d_in
         api.chunk_slot_mapping(bt, d_cl, d_qs, sh.block_size, out=d_slots, stream=comp)
-        api.cache_append(d_k, d_v, d_slots, wl.k_cache, wl.v_cache, stream=comp)
+        api.cache_append(d_k, d_v, d_slots, wl.k_cache, wl.v_cache, scale=kv_scale, stream=comp)
         api.prefill(d_q, wl.k_cache, wl.v_cache, bt, d_cl, d_qs, mq, wl.softmax_scale, out=d_out,
-                    stream=comp)
+                    stream=comp, kv_scale=kv_scale)
 
     def run(i, n):
         d_in, d_slots, d_out = bufs[i & 1]
@@ -954,6 +957,14 @@ def run_prefill(args):
     wl = W.make_prefill(device, num_seqs=args.num_seqs or 16, block_size=args.block_size or 16,
                         num_q_heads=args.q_heads, num_kv_heads=args.kv_heads, head_dim=args.head_dim)
     sh = wl.shape
+    kv_scale = 1.0
+    if args.fp8:
+        # an E4M3 pool of x / kv_scale (torch's conversion, only to make the
+        # input pool; the step's own append writes the chunk with the library)
+        kv_scale = W.fp8_scale_from(wl.k_cache, wl.v_cache, wl.k_new, wl.v_new)
+        for name in ("k_cache", "v_cache"):
+            x = getattr(wl, name)
+            setattr(wl, name, (x.float() / kv_scale).to(torch.float8_e4m3fn).view(torch.uint8).contiguous())
     bt = torch.from_numpy(wl.block_tables).to(device)
     cl = torch.from_numpy(wl.context_lens).to(device)
     qs = torch.from_numpy(wl.query_start).to(device)
@@ -965,8 +976,8 @@ def run_prefill(args):
 
     def step():
         api.chunk_slot_mapping(bt, cl, qs, sh.block_size, out=slots)
-        api.cache_append(wl.k_new, wl.v_new, slots, wl.k_cache, wl.v_cache)
-        api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, mq, wl.softmax_scale, out=out)
+        api.cache_append(wl.k_new, wl.v_new, slots, wl.k_cache, wl.v_cache, scale=kv_scale)
+        api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, mq, wl.softmax_scale, out=out, kv_scale=kv_scale)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -989,9 +1000,9 @@ def run_prefill(args):
         flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
         api.chunk_slot_mapping(bt, cl, qs, sh.block_size, out=slots)
-        api.cache_append(wl.k_new, wl.v_new, slots, wl.k_cache, wl.v_cache)
+        api.cache_append(wl.k_new, wl.v_new, slots, wl.k_cache, wl.v_cache, scale=kv_scale)
         kev[i][0].record(stream)
-        api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, mq, wl.softmax_scale, out=out)
+        api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, mq, wl.softmax_scale, out=out, kv_scale=kv_scale)
         kev[i][1].record(stream)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
@@ -1001,15 +1012,17 @@ def run_prefill(args):
     assert api.device_errors() == 0
     step_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev])), world, device)
     kern_ms = float(np.mean([a.elapsed_time(b) for a, b in kev]))
-    # the warp-level MMA kernel on the same inputs, for comparison
-    mev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(min(K, 50))]
-    for a_, b_ in mev:
-        a_.record(stream)
-        api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, mq, wl.softmax_scale, out=out,
-                    kernel="mma")
-        b_.record(stream)
-    torch.cuda.synchronize()
-    mma_ms = float(np.mean([a_.elapsed_time(b_) for a_, b_ in mev]))
+    # the warp-level MMA kernel on the same inputs, for comparison (bf16 caches)
+    mma_ms = None
+    if not args.fp8:
+        mev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(min(K, 50))]
+        for a_, b_ in mev:
+            a_.record(stream)
+            api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, mq, wl.softmax_scale, out=out,
+                        kernel="mma")
+            b_.record(stream)
+        torch.cuda.synchronize()
+        mma_ms = float(np.mean([a_.elapsed_time(b_) for a_, b_ in mev]))
     flops = wl.attention_flops()
     peaks, kind = measured_peaks()
     peak = float(peaks.get("bf16_tflops", 1900.0))
@@ -1018,31 +1031,32 @@ def run_prefill(args):
         "metric": "paged chunked-prefill attention TFLOP/s", "value": round(world * flops / (step_ms / 1e3) / 1e12, 2),
         "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16",
+        "vs_baseline": None, "dtype": "f16 products on e4m3 KV" if args.fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) bf16, shuffled block tables)",
         "config": {"workload": f"chunked prefill: {sh.num_seqs} seqs x {mq}-token chunks after "
                                f"cached prefixes U[0,2048], {sh.num_q_heads}q/{sh.num_kv_heads}kv heads, "
-                               f"head_dim {sh.head_dim}, block {sh.block_size}, bf16",
+                               f"head_dim {sh.head_dim}, block {sh.block_size}, "
+                               + ("e4m3 KV with per-tensor scale" if args.fp8 else "bf16"),
                    "chunk_tokens": T, "attention_flops_per_step": flops, "seed": wl.seed,
-                   "l2": f"KV pool {2 * wl.k_cache.numel() * 2 / 1e9:.2f} GB; 256 MB written "
-                         "between timed steps (L2 flush)"},
+                   "l2": f"KV pool {2 * wl.k_cache.numel() * wl.k_cache.element_size() / 1e9:.2f} GB; "
+                         "256 MB written between timed steps (L2 flush)"},
         "tokens_per_s": round(world * T / (step_ms / 1e3), 1),
         "breakdown_ms": {"prefill_kernel": round(kern_ms, 5),
                          "slots+append": round(step_ms - kern_ms, 5),
-                         "prefill_kernel_warp_mma": round(mma_ms, 5)},
-        "warp_mma_kernel_tflops": round(flops / (mma_ms / 1e3) / 1e12, 1),
+                         "prefill_kernel_warp_mma": None if mma_ms is None else round(mma_ms, 5)},
+        "warp_mma_kernel_tflops": None if mma_ms is None else round(flops / (mma_ms / 1e3) / 1e12, 1),
         "gpu_launches": 3 * K,  # per timed step: chunk slots, append, attention
         "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel (tcgen05, TMEM accumulators)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
                      "peak_kind": f"{kind} cuBLAS bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
-                     "traffic": recorded_prefill_traffic(sh, mq, sh.num_seqs)},
+                     "traffic": recorded_prefill_traffic(sh, mq, sh.num_seqs, fp8=args.fp8)},
         "clocks": clocks.summary(t0 - 1.0, t1),
     }
     if not args.no_e2e:
-        res["e2e"] = run_prefill_e2e(api, wl, bt, K, world, device)
+        res["e2e"] = run_prefill_e2e(api, wl, bt, K, world, device, kv_scale=kv_scale)
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline_prefill(wl, args.cpu_seconds)
+        res["cpu_baseline"] = cpu_baseline_prefill(wl, args.cpu_seconds, kv_scale if args.fp8 else None)
     if rank == 0:
         print(json.dumps(res), flush=True)
 

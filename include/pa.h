@@ -347,12 +347,18 @@ pa_status pa_decode_step_fp8_qk(const void *q, const void *k_new, const void *v_
  *   q, out bf16 [num_tokens][num_q_heads][head_dim], num_tokens =
  *   query_start[num_seqs] (the host's count of chunk rows).
  *   max_query_len >= every C_s (host-side bound used for the grid).
- *   Supported: bf16 cache, group 1, 2, 4, 8 or 16, head_dim 64/128, block 16/32,
- *   softmax_scale > 0 (PA_ERR_UNSUPPORTED otherwise).
- *   One kernel on the tcgen05 tensor cores (accumulators in tensor
- *   memory), head_dim 64 or 128.  kv_scale is unused.
+ *   Supported: group 1, 2, 4, 8 or 16, block 16/32, softmax_scale > 0, and
+ *   a bf16 cache at head_dim 64/128 or an E4M3 cache (x / kv_scale, one
+ *   scale for K and V, kv_scale > 0) at head_dim 128 (PA_ERR_UNSUPPORTED
+ *   otherwise; the E4M3 cache is the one "Step 3 (FP8 KV cache)" of the
+ *   tuning guide names).  One kernel on the tcgen05 tensor cores
+ *   (accumulators in tensor memory); with an E4M3 cache the pages are
+ *   widened exactly to fp16 in shared memory and the products run in
+ *   fp16 (the query rounded to fp16, exact for bf16 values in its range).
+ *   kv_scale is unused for a bf16 cache.
  * pa_prefill_mma: the same computation always with the warp-level MMA
- *   kernel (kept as the comparison point for the tensor-memory kernel).
+ *   kernel (kept as the comparison point for the tensor-memory kernel);
+ *   bf16 caches only.
  */
 pa_status pa_chunk_slot_mapping(const int32_t *block_tables, int max_blocks_per_seq,
                                 const int32_t *context_lens, const int32_t *query_start,

@@ -262,10 +262,10 @@ def chunk_slot_mapping(block_tables, context_lens, query_start, block_size, out=
 
 
 def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, max_query_len,
-            softmax_scale=None, out=None, stream=None, kernel="auto") -> torch.Tensor:
+            softmax_scale=None, out=None, stream=None, kernel="auto", kv_scale=1.0) -> torch.Tensor:
     """Chunked prefill attention: bf16 [T, Hq, D] for the chunk rows q.
-    ``kernel`` "auto" (tensor-memory kernel for head_dim 128) or "mma"
-    (warp-level MMA kernel)."""
+    ``kernel`` "auto" (tensor-memory kernel) or "mma" (warp-level MMA
+    kernel, bf16 caches only).  An E4M3 cache (uint8) holds x / kv_scale."""
     _need(q, "q", (torch.bfloat16,), 3)
     _need(query_start, "query_start", (torch.int32,), 1)
     kv_dtype = cache_dtype_of(k_cache)
@@ -283,7 +283,7 @@ def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, max_qu
     fn = _lib_handle().pa_prefill if kernel == "auto" else _lib_handle().pa_prefill_mma
     _check(fn(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
               block_tables.shape[1], context_lens.data_ptr(), query_start.data_ptr(), S, T,
-              int(max_query_len), Hq, Hkv, D, NB, B, kv_dtype, 1.0, float(softmax_scale),
+              int(max_query_len), Hq, Hkv, D, NB, B, kv_dtype, float(kv_scale), float(softmax_scale),
               out.data_ptr(), _stream(stream)))
     return out
 

@@ -340,8 +340,8 @@ pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_ca
                             const int32_t *block_tables, int max_blocks_per_seq,
                             const int32_t *context_lens, const int32_t *query_start, int num_seqs,
                             int total_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
-                            int head_dim, int num_blocks, int block_size, float softmax_scale, void *out,
-                            unsigned int *err, cudaStream_t stream);
+                            int head_dim, int num_blocks, int block_size, bool fp8, float kv_scale,
+                            float softmax_scale, void *out, unsigned int *err, cudaStream_t stream);
 static pa_status prefill_impl(const void *q, const void *k_cache, const void *v_cache,
                               const int32_t *block_tables, int max_blocks_per_seq,
                               const int32_t *context_lens, const int32_t *query_start,
@@ -411,7 +411,6 @@ static pa_status prefill_impl(const void *q, const void *k_cache, const void *v_
                               pa_kv_dtype kv_dtype, float kv_scale, float softmax_scale,
                               void *out, cudaStream_t stream, bool tensor_memory) {
     clear_error();
-    (void)kv_scale;
     if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || num_q_heads <= 0 ||
         num_kv_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
         return fail(PA_ERR_INVALID_ARG, "bad size");
@@ -425,8 +424,12 @@ static pa_status prefill_impl(const void *q, const void *k_cache, const void *v_
         return fail(PA_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
     if (block_size != 16 && block_size != 32)
         return fail(PA_ERR_UNSUPPORTED, "block_size %d (supported: 16, 32)", block_size);
-    if (kv_dtype != PA_KV_BF16)
-        return fail(PA_ERR_UNSUPPORTED, "prefill reads bf16 caches only");
+    const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
+    if (kv_dtype != PA_KV_BF16 && !fp8) return fail(PA_ERR_INVALID_ARG, "unknown kv_dtype %d", static_cast<int>(kv_dtype));
+    if (fp8 && !(tensor_memory && head_dim == 128))
+        return fail(PA_ERR_UNSUPPORTED, "E4M3 caches: pa_prefill at head_dim 128 only");
+    if (fp8 && !(kv_scale > 0.f && isfinite(kv_scale)))
+        return fail(PA_ERR_INVALID_ARG, "kv_scale must be positive and finite for an E4M3 cache");
     if (static_cast<int64_t>(num_blocks) * num_kv_heads * block_size > 0x7fffffffLL)
         return fail(PA_ERR_UNSUPPORTED, "pool exceeds 2^31 rows");
     if (num_seqs > 65535 || num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "grid too large");
@@ -446,8 +449,8 @@ static pa_status prefill_impl(const void *q, const void *k_cache, const void *v_
     if (tensor_memory)
         return launch_prefill_tc(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                  context_lens, query_start, num_seqs, num_tokens, max_query_len,
-                                 num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
-                                 softmax_scale, out, err0, stream);
+                                 num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, fp8,
+                                 kv_scale, softmax_scale, out, err0, stream);
     const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
     CUtensorMap tk, tv;
     pa_status st = make_map(&tk, k_cache, false, head_dim, rows, block_size);

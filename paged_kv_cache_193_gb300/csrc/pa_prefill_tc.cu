@@ -62,7 +62,8 @@ struct PrefillTcArgs {
     int num_kv_heads;
     int group;
     int tile_tokens;  // 128 / group
-    float score_scale;
+    float score_scale;       // softmax scale x log2(e) (x the E4M3 scale of K)
+    float v_scale;           // the E4M3 scale of V, applied to the output (1 for bf16)
     uint64_t wait_limit_ns;  // give up on a wait after this long
     int stall_first_wait;    // test hook: the MMA threads' first wait is on a barrier nothing completes
     int num_seqs;
@@ -110,7 +111,7 @@ constexpr int kTcOCol = 128;
 // waited for with this before the CTA ends.
 constexpr uint64_t kTcWaitNs = 2000000000ull;
 
-template <int D, int BS>
+template <int D, int BS, bool FP8>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -125,6 +126,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // kv_empty[st]: every tile's PV of that block is done (its QK came
     // before), by a commit of each tile's MMA thread
     __shared__ __align__(8) uint64_t kv_full[kTcStages], kv_empty[kTcStages];
+    // E4M3 caches: the stage's E4M3 pages have landed (kv_landed); each
+    // tile's query row turned to fp16 (q_conv)
+    __shared__ __align__(8) uint64_t kv_landed[2][kTcStages], q_conv[kTcTiles];
     // per tile: S written into buffer b (s_full[T][b]), P written over it
     // (p_full[T][b]), PV done (pv_done), every MMA done (drain).  With two
     // buffers the softmax may write P(j + 1) before the MMA thread saw P(j),
@@ -204,6 +208,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int i = 0; i < kTcStages; ++i) {
             mbar_init(smem_addr(&kv_full[i]), 2);  // the K loader and the V loader
             mbar_init(smem_addr(&kv_empty[i]), ntiles);
+            mbar_init(smem_addr(&kv_landed[0][i]), 1);
+            mbar_init(smem_addr(&kv_landed[1][i]), 1);
         }
         for (int t = 0; t < kTcTiles; ++t) {
             mbar_init(smem_addr(&s_full[t][0]), 1);
@@ -212,6 +218,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(smem_addr(&p_full[t][1]), 4);
             mbar_init(smem_addr(&pv_done[t]), 1);
             mbar_init(smem_addr(&drain[t]), 1);
+            mbar_init(smem_addr(&q_conv[t]), 4);
         }
         failed_s = 0;
         fence_barrier_init();
@@ -254,59 +261,141 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
 
     if (loader) {
-        // ------------- loads: warp 8 K, warp 10 V (thread 0 requested the queries) -------------
-        const bool is_k = warp == kTcLoadWarp;
-        const CUtensorMap *map = is_k ? &tmK : &tmV;
-        const uint32_t ring = base + (is_k ? kTcKOff : kTcVOff);
-        const uint64_t policy = l2_evict_first_policy();
-        int e_next = e_first;
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int st = kb % kTcStages, ph = (kb / kTcStages) & 1;
-            const int y = page_row(e_next);
-            if (kb + 1 < nkb) e_next = page_entry(kb + 1);
-            const bool freed = __all_sync(0xffffffffu, mbar_wait_suspend(smem_addr(&kv_empty[st]), ph ^ 1, limit));
-            if (lane == 0) {
-                if (!freed) fail();
-                mbar_arrive_expect_tx(smem_addr(&kv_full[st]), kTcKVStage);
+        if constexpr (FP8) {
+            // ---- E4M3 pages: warp 8 loads K, warp 10 V, each into the second
+            // 64-dim slab of its stages, and each widens its block in place to
+            // fp16 rows (exact) in the layout bf16 pages would have, zeroing
+            // rows past the context, two blocks after requesting it; only then
+            // is the block given to the MMAs.  A stage wait for block kb needs
+            // block kb - 5 widened, which happened two iterations before. ----
+            constexpr int kLag = 2;
+            const bool is_k = warp == kTcLoadWarp;
+            const int w = is_k ? 0 : 1;
+            const CUtensorMap *map = is_k ? &tmK : &tmV;
+            const uint32_t ring = base + (is_k ? kTcKOff : kTcVOff);
+            const uint64_t policy = l2_evict_first_policy();
+            bool ok = true;
+            auto widen = [&](int kb) {
+                const int st = kb % kTcStages;
+                ok = ok && __all_sync(0xffffffffu, mbar_wait_suspend(smem_addr(&kv_landed[w][st]),
+                                                                     (kb / kTcStages) & 1, limit));
+                // lane widens rows lane and lane + 32.  An E4M3 row is 128
+                // bytes (chunk c = dims 16 c .. 16 c + 15 at chunk c ^ (row % 8));
+                // its fp16 dims 64 s .. 64 s + 63 go to slab s, chunk f = dims
+                // 8 f .. at chunk f ^ (row % 8).  Both rows are read whole
+                // before either's slab-1 half is written over it.
+                const uint32_t sb = ring + st * kTcKVStage;
+                uint4 e[2][8];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int r = lane + 32 * h2;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) e[h2][c] = lds128(sb + kTcKVSlab + r * 128 + ((c ^ (r & 7)) << 4));
+                }
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int r = lane + 32 * h2;
+                    const bool valid = kb * kTcKeys + r < kend;
+                    const uint32_t sw = static_cast<uint32_t>(r & 7);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+                        if (valid) {
+                            e4m3x4_to_f16x2x2(e[h2][c].x, lo.x, lo.y);
+                            e4m3x4_to_f16x2x2(e[h2][c].y, lo.z, lo.w);
+                            e4m3x4_to_f16x2x2(e[h2][c].z, hi.x, hi.y);
+                            e4m3x4_to_f16x2x2(e[h2][c].w, hi.z, hi.w);
+                        }
+                        const int f = 2 * c;
+                        const uint32_t rb = sb + (f >> 3) * kTcKVSlab + r * 128;
+                        st_shared16(rb + (((f & 7) ^ sw) << 4), lo);
+                        st_shared16(rb + ((((f + 1) & 7) ^ sw) << 4), hi);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&kv_full[st]));
+            };
+            int e_next = e_first;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int st = kb % kTcStages, ph = (kb / kTcStages) & 1;
+                const int y = page_row(e_next);
+                if (kb + 1 < nkb) e_next = page_entry(kb + 1);
+                const bool freed =
+                    __all_sync(0xffffffffu, mbar_wait_suspend(smem_addr(&kv_empty[st]), ph ^ 1, limit));
+                if (lane == 0) {
+                    if (!freed) fail();
+                    mbar_arrive_expect_tx(smem_addr(&kv_landed[w][st]), kTcKeys * 128);
+                }
+                __syncwarp();
+                if (lane < NPG)
+                    tma_load_2d(ring + st * kTcKVStage + kTcKVSlab + lane * BS * 128, map, 0, y,
+                                smem_addr(&kv_landed[w][st]), policy);
+                if (kb >= kLag) widen(kb - kLag);
             }
-            __syncwarp();
-            if (lane < NPG) {
-                for (int sl = 0; sl < kSlabs; ++sl)
-                    tma_load_2d(ring + st * kTcKVStage + sl * kTcKVSlab + lane * BS * 128, map, sl * 64, y,
-                                smem_addr(&kv_full[st]), policy);
+            for (int kb = max(0, nkb - kLag); kb < nkb; ++kb) widen(kb);
+            if (!ok && lane == 0) fail();
+            // a wait that gave up may leave copies in flight: only the last
+            // kTcStages blocks' can be
+            if (lane == 0)
+                for (int kb = max(0, nkb - kTcStages); kb < nkb; ++kb)
+                    mbar_wait_suspend(smem_addr(&kv_landed[w][kb % kTcStages]), (kb / kTcStages) & 1, kTcWaitNs);
+        } else {
+            // ------------- loads: warp 8 K, warp 10 V (thread 0 requested the queries) -------------
+            const bool is_k = warp == kTcLoadWarp;
+            const CUtensorMap *map = is_k ? &tmK : &tmV;
+            const uint32_t ring = base + (is_k ? kTcKOff : kTcVOff);
+            const uint64_t policy = l2_evict_first_policy();
+            int e_next = e_first;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int st = kb % kTcStages, ph = (kb / kTcStages) & 1;
+                const int y = page_row(e_next);
+                if (kb + 1 < nkb) e_next = page_entry(kb + 1);
+                const bool freed = __all_sync(0xffffffffu, mbar_wait_suspend(smem_addr(&kv_empty[st]), ph ^ 1, limit));
+                if (lane == 0) {
+                    if (!freed) fail();
+                    mbar_arrive_expect_tx(smem_addr(&kv_full[st]), kTcKVStage);
+                }
+                __syncwarp();
+                if (lane < NPG) {
+                    for (int sl = 0; sl < kSlabs; ++sl)
+                        tma_load_2d(ring + st * kTcKVStage + sl * kTcKVSlab + lane * BS * 128, map, sl * 64, y,
+                                    smem_addr(&kv_full[st]), policy);
+                }
             }
+            if (!is_k && partial) {
+                // keys past the context in the last block may hold anything:
+                // zero those V rows before a PV reads them (P is 0 there, but
+                // 0 x garbage could be NaN)
+                const int kb = nkb - 1, st = kb % kTcStages;
+                const bool landed = __all_sync(0xffffffffu, mbar_wait_suspend(smem_addr(&kv_full[st]), (kb / kTcStages) & 1, limit));
+                if (!landed && lane == 0) fail();
+                const uint32_t vbase = base + kTcVOff + st * kTcKVStage;
+                for (int r2 = kend - kb * kTcKeys + lane; r2 < kTcKeys; r2 += 32)
+                    for (int sl = 0; sl < kSlabs; ++sl)
+                        for (int c16 = 0; c16 < 8; ++c16)
+                            st_shared_zero16(vbase + sl * kTcKVSlab + r2 * 128 + c16 * 16);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&v_zeroed));
+            }
+            // Both loaders issue every block, so each stage's phase completes
+            // once its copies land; issuing block kb needed block kb - kTcStages
+            // released, so only the last kTcStages blocks can still be in flight.
+            // Wait for them (2 s) before the CTA may end, whatever gave up.
+            if (lane == 0)
+                for (int kb = max(0, nkb - kTcStages); kb < nkb; ++kb)
+                    mbar_wait_suspend(smem_addr(&kv_full[kb % kTcStages]), (kb / kTcStages) & 1, kTcWaitNs);
         }
-        if (!is_k && partial) {
-            // keys past the context in the last block may hold anything:
-            // zero those V rows before a PV reads them (P is 0 there, but
-            // 0 x garbage could be NaN)
-            const int kb = nkb - 1, st = kb % kTcStages;
-            const bool landed = __all_sync(0xffffffffu, mbar_wait_suspend(smem_addr(&kv_full[st]), (kb / kTcStages) & 1, limit));
-            if (!landed && lane == 0) fail();
-            const uint32_t vbase = base + kTcVOff + st * kTcKVStage;
-            for (int r2 = kend - kb * kTcKeys + lane; r2 < kTcKeys; r2 += 32)
-                for (int sl = 0; sl < kSlabs; ++sl)
-                    for (int c16 = 0; c16 < 8; ++c16)
-                        st_shared_zero16(vbase + sl * kTcKVSlab + r2 * 128 + c16 * 16);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&v_zeroed));
-        }
-        // Both loaders issue every block, so each stage's phase completes
-        // once its copies land; issuing block kb needed block kb - kTcStages
-        // released, so only the last kTcStages blocks can still be in flight.
-        // Wait for them (2 s) before the CTA may end, whatever gave up.
-        if (lane == 0)
-            for (int kb = max(0, nkb - kTcStages); kb < nkb; ++kb)
-                mbar_wait_suspend(smem_addr(&kv_full[kb % kTcStages]), (kb / kTcStages) & 1, kTcWaitNs);
     } else if (warp == kTcMmaWarp || warp == kTcMmaWarpB) {
         // ---------------- MMA issue, one thread per tile ----------------
         // S(0) and S(1) first; then per block j: PV(j) once P(j) is written,
         // and S(j + 2) into the buffer P(j) came from.
         const int T = warp == kTcMmaWarp ? 0 : 1;
         if (T < ntiles) {
-            constexpr uint32_t idesc_qk = tc_idesc_bf16(kTcRows, kTcKeys, 0, 0);
-            constexpr uint32_t idesc_pv = tc_idesc_bf16(kTcRows, D, 0, 1);
+            // E4M3 caches: fp16 products (the pages widen to fp16 exactly)
+            constexpr uint32_t idesc_qk = FP8 ? tc_idesc_f16(kTcRows, kTcKeys, 0, 0) : tc_idesc_bf16(kTcRows, kTcKeys, 0, 0);
+            constexpr uint32_t idesc_pv = FP8 ? tc_idesc_f16(kTcRows, D, 0, 1) : tc_idesc_bf16(kTcRows, D, 0, 1);
             // a descriptor's start address is its low field (16-byte units,
             // no carry out within shared memory): every operand descriptor is
             // a base descriptor plus an offset, so issuing an MMA costs one add
@@ -319,7 +408,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             };
             // test hook: give up at once on a barrier that nothing completes
             bool ok = !a.stall_first_wait || wait(stall_bar, 0);
-            ok = ok && wait(q_full, 0);
+            // E4M3 caches: the softmax warps turned the tile's query to fp16
+            if constexpr (FP8) ok = ok && wait(q_conv[T], 0);
+            else ok = ok && wait(q_full, 0);
             auto qk = [&](int kb) {  // S(kb) = Q K(kb)^T into buffer kb % 2
                 const int ks = kb % kTcStages;
                 // K and V of the block: V(kb) is in place for PV(kb) too
@@ -343,7 +434,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int kb = 0; kb < nkb_t; ++kb) {
                 const int vs = kb % kTcStages;
                 ok = ok && wait(p_full[T][kb & 1], (kb >> 1) & 1);
-                if (kb == nkb - 1 && partial) ok = ok && wait(v_zeroed, 0);
+                if (!FP8 && kb == nkb - 1 && partial) ok = ok && wait(v_zeroed, 0);
                 tc_fence_after();
                 if (ok) {  // O += P(kb) V(kb)
                     const uint64_t b0 = v_desc + ((vs * kTcKVStage) >> 4);
@@ -381,6 +472,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float m_ref = -INFINITY, l_run = 0.f;
             // the query tile has landed before its shared memory stages the output
             bool ok = mbar_wait_suspend(smem_addr(&q_full), 0, limit);
+            if constexpr (FP8) {
+                // the products run in fp16: each thread turns its query row
+                // (bf16, exact in fp16 within its range) to fp16 in place
+                for (int sl = 0; sl < kSlabs; ++sl)
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t ad = base + kTcQOff + T * kTcQTile + sl * kTcQSlab + row * 128 + ((c ^ (row & 7)) << 4);
+                        uint4 x = lds128(ad);
+                        x.x = pack2<true>(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u));
+                        x.y = pack2<true>(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u));
+                        x.z = pack2<true>(__uint_as_float(x.z << 16), __uint_as_float(x.z & 0xffff0000u));
+                        x.w = pack2<true>(__uint_as_float(x.w << 16), __uint_as_float(x.w & 0xffff0000u));
+                        st_shared16(ad, x);
+                    }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&q_conv[T]));
+            }
             const int nkb_t = tile_blocks(T);
             for (int kb = 0; kb < nkb_t; ++kb) {
                 const int key0 = kb * kTcKeys;
@@ -457,7 +565,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 l_run += sa[0] + sb[0];
                 uint32_t pk[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) pk[i] = pack2<false>(v[2 * i], v[2 * i + 1]);
+                for (int i = 0; i < 32; ++i) pk[i] = pack2<FP8>(v[2 * i], v[2 * i + 1]);
                 // over S(kb), which this thread holds in registers; no MMA
                 // writes this buffer before PV(kb), which waits for P
                 tc_st32(tSb, pk);
@@ -470,7 +578,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = ok && mbar_wait_suspend(smem_addr(&drain[T]), 0, limit);
             tc_fence_after();
             if (!ok) fail();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float inv = l_run > 0.f ? a.v_scale / l_run : 0.f;
             // A tile wholly inside its chunk leaves through shared memory (its
             // query tile's space, in the same swizzled layout) and two TMA
             // stores; a tile at the chunk's end is written row by row, so no
@@ -544,11 +652,11 @@ static pa_status make_q_map(CUtensorMap *map, const void *q, int total_tokens, i
     return PA_OK;
 }
 
-template <int D, int BS>
+template <int D, int BS, bool FP8>
 static pa_status launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const CUtensorMap &to,
                            const PrefillTcArgs &a, dim3 grid, cudaStream_t stream) {
-    auto kern = prefill_tc_kernel<D, BS>;
+    auto kern = prefill_tc_kernel<D, BS, FP8>;
     constexpr int kTcSmem = TcLayout<D>::kSmem;
     static std::atomic<uint64_t> raised{0};
     int dev = 0;
@@ -565,13 +673,14 @@ static pa_status launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const C
     return cuda_check(cudaGetLastError(), "prefill tcgen05 launch");
 }
 
-// Called by pa_prefill for head_dim 64 and 128 (arguments already checked).
+// Called by pa_prefill for head_dim 64 and 128, bf16 caches, and for
+// head_dim 128 with E4M3 caches (arguments already checked).
 pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_cache,
                             const int32_t *block_tables, int max_blocks_per_seq,
                             const int32_t *context_lens, const int32_t *query_start, int num_seqs,
                             int total_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
-                            int head_dim, int num_blocks, int block_size, float softmax_scale, void *out,
-                            unsigned int *err, cudaStream_t stream) {
+                            int head_dim, int num_blocks, int block_size, bool fp8, float kv_scale,
+                            float softmax_scale, void *out, unsigned int *err, cudaStream_t stream) {
     const int group = num_q_heads / num_kv_heads;
     PrefillTcArgs a;
     a.block_tables = block_tables;
@@ -583,7 +692,8 @@ pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_ca
     a.num_kv_heads = num_kv_heads;
     a.group = group;
     a.tile_tokens = kTcRows / group;
-    a.score_scale = softmax_scale * 1.4426950408889634f;
+    a.score_scale = softmax_scale * 1.4426950408889634f * (fp8 ? kv_scale : 1.f);
+    a.v_scale = fp8 ? kv_scale : 1.f;
     a.wait_limit_ns = wait_limit_ns();
     a.stall_first_wait = stall_first_wait();
     a.num_seqs = num_seqs;
@@ -595,9 +705,9 @@ pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_ca
     if (st != PA_OK) return st;
     st = make_q_map(&to, out, total_tokens, num_q_heads, head_dim, group, a.tile_tokens);  // same geometry
     if (st != PA_OK) return st;
-    st = make_map(&tk, k_cache, false, head_dim, rows, block_size);
+    st = make_map(&tk, k_cache, fp8, head_dim, rows, block_size);
     if (st != PA_OK) return st;
-    st = make_map(&tv, v_cache, false, head_dim, rows, block_size);
+    st = make_map(&tv, v_cache, fp8, head_dim, rows, block_size);
     if (st != PA_OK) return st;
     const int tiles = (max_query_len + a.tile_tokens - 1) / a.tile_tokens;
     dim3 grid((tiles + kTcTiles - 1) / kTcTiles, num_kv_heads, num_seqs);
@@ -605,11 +715,14 @@ pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_ca
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return fail(PA_ERR_CUDA, "cannot read the SM count");
     a.longest_first = num_seqs <= 32 && static_cast<int64_t>(grid.x) * grid.y * grid.z < 2LL * sms;
+    if (fp8)
+        return block_size == 16 ? launch_tc<128, 16, true>(tq, tk, tv, to, a, grid, stream)
+                                : launch_tc<128, 32, true>(tq, tk, tv, to, a, grid, stream);
     if (head_dim == 64)
-        return block_size == 16 ? launch_tc<64, 16>(tq, tk, tv, to, a, grid, stream)
-                                : launch_tc<64, 32>(tq, tk, tv, to, a, grid, stream);
-    return block_size == 16 ? launch_tc<128, 16>(tq, tk, tv, to, a, grid, stream)
-                            : launch_tc<128, 32>(tq, tk, tv, to, a, grid, stream);
+        return block_size == 16 ? launch_tc<64, 16, false>(tq, tk, tv, to, a, grid, stream)
+                                : launch_tc<64, 32, false>(tq, tk, tv, to, a, grid, stream);
+    return block_size == 16 ? launch_tc<128, 16, false>(tq, tk, tv, to, a, grid, stream)
+                            : launch_tc<128, 32, false>(tq, tk, tv, to, a, grid, stream);
 }
 
 }  // namespace pa

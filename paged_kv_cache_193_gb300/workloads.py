@@ -410,6 +410,9 @@ def poison_prefill(wl: PrefillWorkload) -> None:
             live[wl.block_tables[s, t // B], t % B] = True
     dead = torch.from_numpy(~live).to(wl.k_cache.device)
     mask = dead[:, None, :, None].expand(-1, sh.num_kv_heads, -1, sh.head_dim)
-    fill = torch.tensor(np.int16(np.uint16(BF16_NAN_BITS).view(np.int16)), device=wl.k_cache.device)
     for c_ in (wl.k_cache, wl.v_cache):
-        c_.view(torch.int16).masked_fill_(mask, fill)
+        if c_.dtype == torch.uint8:  # an E4M3 pool
+            c_.masked_fill_(mask, E4M3_NAN_CODE)
+        else:
+            fill = torch.tensor(np.int16(np.uint16(BF16_NAN_BITS).view(np.int16)), device=c_.device)
+            c_.view(torch.int16).masked_fill_(mask, fill)

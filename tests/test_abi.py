@@ -129,7 +129,8 @@ def _prefill(lib, fn="pa_prefill", **kw):
     (dict(Hq=64, Hkv=2), 2),                        # group of 32
     (dict(D=96), 2),
     (dict(B=8), 2),
-    (dict(dt=1), 2),                                # prefill reads bf16 caches only
+    (dict(dt=7), 1),                                # no such cache type
+    (dict(dt=1, D=64), 2),                          # E4M3 caches: head_dim 128 only
     (dict(NB=0), 1),
     (dict(T=-1), 1),
     (dict(S=70000), 2),
@@ -143,6 +144,16 @@ def _prefill(lib, fn="pa_prefill", **kw):
 def test_prefill_rejects_on_host(lib, fn, kw, status):
     assert _prefill(lib, fn, **kw) == status
     assert lib.pa_last_error()
+
+
+@pytest.mark.parametrize("kw,tc_status,mma_status", [
+    (dict(dt=1, kvs=0.0), 1, 2),                    # E4M3 needs a positive, finite scale ...
+    (dict(dt=1, kvs=float("inf")), 1, 2),
+    (dict(dt=1, kvs=-1.0), 1, 2),                   # ... and the warp-level MMA kernel reads bf16 only
+])
+def test_prefill_e4m3_checks_on_host(lib, kw, tc_status, mma_status):
+    assert _prefill(lib, "pa_prefill", **kw) == tc_status
+    assert _prefill(lib, "pa_prefill_mma", **kw) == mma_status
 
 
 @pytest.mark.parametrize("kw", [dict(T=0), dict(S=0), dict(mq=0)])

@@ -108,6 +108,78 @@ def test_prefill_sequence_order(api, oracle, cuda_device, S, ties):
     assert api.device_errors() == 0
 
 
+def make_e4m3_prefill(oracle, device, **kw):
+    """A prefill workload whose pool is E4M3: the bf16 pool's codes of
+    x / kv_scale by the oracle's encoder (token i of the pool -> slot i),
+    kv_scale = the largest magnitude / 448.  Returns (workload, kv_scale)."""
+    wl = W.make_prefill(device, **kw)
+    scale = W.fp8_scale_from(wl.k_cache, wl.v_cache, wl.k_new, wl.v_new)
+    kb, vb = W.bits(wl.k_cache), W.bits(wl.v_cache)
+    NB, Hkv, B, D = kb.shape
+    kc = np.zeros((NB, Hkv, B, D), np.uint8)
+    vc = np.zeros_like(kc)
+    oracle.cache_append(kb.transpose(0, 2, 1, 3).reshape(NB * B, Hkv, D),
+                        vb.transpose(0, 2, 1, 3).reshape(NB * B, Hkv, D),
+                        np.arange(NB * B, dtype=np.int32), kc, vc, B, 1, scale)
+    wl.k_cache = torch.from_numpy(kc).to(device)
+    wl.v_cache = torch.from_numpy(vc).to(device)
+    return wl, scale
+
+
+def e4m3_prefill_step(api, oracle, wl, scale, device):
+    """Oracle and library of one E4M3 prefill step: chunk slots, the chunk's
+    E4M3 append (bit for bit), attention.  Returns (oracle out, library out)."""
+    kc, vc = W.bits(wl.k_cache).copy(), W.bits(wl.v_cache).copy()
+    slots_ref = oracle.chunk_slot_mapping(wl.block_tables, wl.context_lens, wl.query_start,
+                                          wl.shape.block_size)
+    oracle.cache_append(W.bits(wl.k_new), W.bits(wl.v_new), slots_ref, kc, vc, wl.shape.block_size, 1, scale)
+    ref = oracle.prefill(W.bits(wl.q), kc, vc, wl.block_tables, wl.context_lens, wl.query_start,
+                         wl.shape.num_kv_heads, wl.shape.block_size, wl.softmax_scale, kv_dtype=1,
+                         kv_scale=scale)
+    bt, cl, qs = _dev(wl, device)
+    g_out = Guarded(wl.q.shape, torch.bfloat16, device, fill=float("nan"))
+    slots = api.chunk_slot_mapping(bt, cl, qs, wl.shape.block_size)
+    api.cache_append(wl.k_new, wl.v_new, slots, wl.k_cache, wl.v_cache, scale=scale)
+    out = api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, wl.max_query_len, wl.softmax_scale,
+                      out=g_out.tensor, kv_scale=scale)
+    torch.cuda.synchronize()
+    g_out.check("prefill E4M3 out")
+    assert np.array_equal(slots.cpu().numpy(), slots_ref)
+    assert np.array_equal(W.bits(wl.k_cache), kc) and np.array_equal(W.bits(wl.v_cache), vc)
+    return ref, out
+
+
+@pytest.mark.parametrize("G,Hkv,B", [(4, 2, 16), (1, 4, 32), (16, 1, 16), (8, 1, 32)])
+def test_prefill_e4m3_matches_oracle(api, oracle, cuda_device, G, Hkv, B):
+    """E4M3 cache (one scale for K and V): the pages widen to fp16 in
+    shared memory and the products run in fp16; against the oracle fed the
+    same E4M3 bytes, with NaN codes in every row outside the contexts."""
+    wl, scale = make_e4m3_prefill(oracle, cuda_device, seed=70 + G + B, num_seqs=5,
+                                  chunk=[1, 7, 64, 300, 33], prefixes=[0, 5, 33, 300, 16],
+                                  num_q_heads=G * Hkv, num_kv_heads=Hkv, head_dim=128, block_size=B)
+    W.poison_prefill(wl)
+    api.device_errors(clear=True)
+    ref, out = e4m3_prefill_step(api, oracle, wl, scale, cuda_device)
+    compare(out, ref, what=f"prefill E4M3 G{G} B{B}")
+    assert api.device_errors() == 0
+
+
+@pytest.mark.parametrize("G,Hkv,B", [(4, 2, 16), (1, 4, 32)])
+def test_prefill_e4m3_many_items(api, oracle, cuda_device, G, Hkv, B):
+    """48 ragged sequences over several waves of blocks, E4M3 cache."""
+    rng = np.random.default_rng(400 + G + B)
+    S = 48
+    wl, scale = make_e4m3_prefill(oracle, cuda_device, seed=80 + G + B, num_seqs=S,
+                                  chunk=rng.integers(1, 200, size=S, endpoint=True).tolist(),
+                                  prefixes=rng.integers(16, 300, size=S, endpoint=True).tolist(),
+                                  num_q_heads=G * Hkv, num_kv_heads=Hkv, head_dim=128, block_size=B)
+    W.poison_prefill(wl)
+    api.device_errors(clear=True)
+    ref, out = e4m3_prefill_step(api, oracle, wl, scale, cuda_device)
+    compare(out, ref, what=f"prefill E4M3 many items G{G} B{B}")
+    assert api.device_errors() == 0
+
+
 @pytest.mark.parametrize("kernel", ["auto", "mma"])
 def test_prefill_empty_chunks(api, oracle, cuda_device, kernel):
     """Sequences that bring no chunk rows sit between ones that do: their

@@ -18,7 +18,7 @@ from gpu_helpers import compare, device_tables
 from paged_kv_cache_193_gb300 import _lib
 from paged_kv_cache_193_gb300 import workloads as W
 from test_gpu_kernels import _oracle_step
-from test_gpu_prefill import _dev, _oracle_step as _oracle_prefill
+from test_gpu_prefill import _dev, _oracle_step as _oracle_prefill, e4m3_prefill_step, make_e4m3_prefill
 
 pytestmark = pytest.mark.gpu
 
@@ -99,4 +99,24 @@ def test_prefill_wait_runs_out_then_recovers(api, oracle, cuda_device, G, Hkv, B
     out = api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, wl.max_query_len, wl.softmax_scale)
     torch.cuda.synchronize()
     compare(out, ref, what=f"prefill G{G} B{B} D{D} after a timed-out call")
+    assert api.device_errors() == 0
+
+
+def test_prefill_e4m3_wait_runs_out_then_recovers(api, oracle, cuda_device):
+    """The E4M3 prefill kernel (a loader warp and a converting warp) gives up
+    the same way, and the next call is correct."""
+    lib = _lib.load()
+    wl, scale = make_e4m3_prefill(oracle, cuda_device, seed=45, num_seqs=5, chunk=[1, 7, 64, 300, 33],
+                                  prefixes=[0, 5, 33, 300, 16], num_q_heads=8, num_kv_heads=2,
+                                  head_dim=128, block_size=16)
+    W.poison_prefill(wl)
+    bt, cl, qs = _dev(wl, cuda_device)
+    api.device_errors(clear=True)
+    _stalled(lib, lambda: api.prefill(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, wl.max_query_len,
+                                      wl.softmax_scale, kv_scale=scale))
+    flags = api.device_errors(clear=True)
+    assert flags & _lib.PA_DEVERR_TIMEOUT, hex(flags)
+    assert flags & ~_lib.PA_DEVERR_TIMEOUT == 0, hex(flags)
+    ref, out = e4m3_prefill_step(api, oracle, wl, scale, cuda_device)
+    compare(out, ref, what="prefill E4M3 after a timed-out call")
     assert api.device_errors() == 0
