@@ -66,6 +66,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
                                             I, P]
     lib.pa_oracle_block_alloc.restype = I
     lib.pa_oracle_block_alloc.argtypes = [P, I, P, I, I, P, P, P, I, P, P, I, I, I, P]
+    lib.pa_oracle_block_alloc_chunk.restype = I
+    lib.pa_oracle_block_alloc_chunk.argtypes = [P, I, P, P, I, I, P, P, P, I, P, P, I, I, I, P]
     lib.pa_oracle_chunk_slot_mapping.restype = None
     lib.pa_oracle_chunk_slot_mapping.argtypes = [P, I, P, P, I, I, P]
     lib.pa_oracle_prefill.restype = None
@@ -312,6 +314,28 @@ class Oracle:
                                             _p(free_blocks), _p(fc), _p(refcounts), NB,
                                             _p(k_cache.view(np.uint8)), _p(v_cache.view(np.uint8)),
                                             Hkv, D, elem, _p(cow))
+        return int(st), int(fc[0]), cow
+
+    def block_alloc_chunk(self, block_tables, context_lens, query_start, block_size, free_blocks,
+                          free_count, refcounts, k_cache, v_cache):
+        """In place, for a chunk of new tokens per sequence (context_lens
+        counts them): copy-on-write of a shared, partly filled last block,
+        fresh blocks for every further block the chunk reaches.  Returns
+        (status, free_count, cow_src)."""
+        for a, dt in ((block_tables, np.int32), (free_blocks, np.int32), (refcounts, np.int32)):
+            assert a.dtype == dt and a.flags.c_contiguous
+        assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+        cl = _c(context_lens, np.int32)
+        qs = _c(query_start, np.int32)
+        S, MB = block_tables.shape
+        NB, Hkv, B, D = k_cache.shape
+        elem = k_cache.dtype.itemsize
+        fc = np.array([free_count], np.int32)
+        cow = np.empty(S, np.int32)
+        st = self.lib.pa_oracle_block_alloc_chunk(_p(block_tables), MB, _p(cl), _p(qs), S, block_size,
+                                                  _p(free_blocks), _p(fc), _p(refcounts), NB,
+                                                  _p(k_cache.view(np.uint8)), _p(v_cache.view(np.uint8)),
+                                                  Hkv, D, elem, _p(cow))
         return int(st), int(fc[0]), cow
 
     # -- threads -------------------------------------------------------------

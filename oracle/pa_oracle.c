@@ -658,6 +658,114 @@ int pa_oracle_block_alloc(int32_t *block_tables, int max_blocks_per_seq,
     return 0;
 }
 
+/* The same for a chunk of new tokens per sequence (chunked prefill): sequence
+ * s with c = query_start[s+1] - query_start[s] > 0 new tokens and
+ * n = context_lens[s] (which counts them) holds old = n - c tokens already.
+ *   - if old % B != 0 and the block holding them, j0 = old / B, is
+ *     referenced by more than one sequence (counted before the call): it
+ *     gets a fresh block holding a copy of rows [0, old % B) (every KV head,
+ *     K and V), and the old block loses one reference;
+ *   - every logical block the chunk reaches beyond that, from
+ *     (old % B == 0 ? old / B : old / B + 1) to (n - 1) / B, gets a fresh
+ *     block.
+ * Fresh blocks come off the top of the stack in sequence order, a
+ * sequence's copy first and then its new blocks in logical order; each gets
+ * refcount 1.  Sequences with c <= 0, with c > n or whose last block lies
+ * past max_blocks_per_seq are left alone.  Freed blocks go back as in
+ * pa_oracle_block_alloc.  If the stack holds fewer blocks than needed
+ * nothing changes and the call returns 1 (else 0). */
+int pa_oracle_block_alloc_chunk(int32_t *block_tables, int max_blocks_per_seq,
+                                const int32_t *context_lens, const int32_t *query_start,
+                                int num_seqs, int block_size, int32_t *free_blocks,
+                                int32_t *free_count, int32_t *refcounts, int num_blocks,
+                                uint8_t *k_cache, uint8_t *v_cache, int num_kv_heads, int head_dim,
+                                int elem_bytes, int32_t *cow_src)
+{
+    int need = 0;
+    int *copy = (int *)malloc(sizeof(int) * (size_t)(num_seqs > 0 ? num_seqs : 1));
+    int *first = (int *)malloc(sizeof(int) * (size_t)(num_seqs > 0 ? num_seqs : 1));
+    int *last = (int *)malloc(sizeof(int) * (size_t)(num_seqs > 0 ? num_seqs : 1));
+    /* decide, from the state before the call */
+    for (int s = 0; s < num_seqs; ++s) {
+        int c = query_start[s + 1] - query_start[s];
+        int n = context_lens[s];
+        int old = n - c;
+        copy[s] = 0;
+        first[s] = 0;
+        last[s] = -1; /* no new blocks */
+        cow_src[s] = -1;
+        if (c <= 0 || old < 0 || (n - 1) / block_size >= max_blocks_per_seq)
+            continue;
+        if (old % block_size != 0) {
+            int32_t cur = block_tables[(int64_t)s * max_blocks_per_seq + old / block_size];
+            if (cur >= 0 && cur < num_blocks && refcounts[cur] > 1)
+                copy[s] = 1;
+            first[s] = old / block_size + 1;
+        } else {
+            first[s] = old / block_size;
+        }
+        last[s] = (n - 1) / block_size;
+        need += copy[s] + (last[s] - first[s] + 1);
+    }
+    if (need > *free_count) {
+        free(copy);
+        free(first);
+        free(last);
+        return 1;
+    }
+    int top = *free_count;
+    int taken = 0;
+    int32_t *freed = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_seqs > 0 ? num_seqs : 1));
+    int nfreed = 0;
+    int64_t row_bytes = (int64_t)head_dim * elem_bytes;
+    for (int s = 0; s < num_seqs; ++s) {
+        int64_t row0 = (int64_t)s * max_blocks_per_seq;
+        if (copy[s]) {
+            int old = context_lens[s] - (query_start[s + 1] - query_start[s]);
+            int64_t entry = row0 + old / block_size;
+            int32_t src_block = block_tables[entry];
+            int32_t fresh = free_blocks[top - 1 - taken];
+            ++taken;
+            int rows = old % block_size;
+            for (int h = 0; h < num_kv_heads; ++h) {
+                int64_t src = (((int64_t)src_block * num_kv_heads + h) * block_size) * row_bytes;
+                int64_t dst = (((int64_t)fresh * num_kv_heads + h) * block_size) * row_bytes;
+                memcpy(k_cache + dst, k_cache + src, (size_t)(rows * row_bytes));
+                memcpy(v_cache + dst, v_cache + src, (size_t)(rows * row_bytes));
+            }
+            refcounts[src_block] -= 1;
+            cow_src[s] = src_block;
+            block_tables[entry] = fresh;
+            refcounts[fresh] = 1;
+        }
+        for (int j = first[s]; j <= last[s]; ++j) {
+            int32_t fresh = free_blocks[top - 1 - taken];
+            ++taken;
+            block_tables[row0 + j] = fresh;
+            refcounts[fresh] = 1;
+        }
+    }
+    /* push blocks left without references, in order of their last copier */
+    for (int s = 0; s < num_seqs; ++s) {
+        if (!copy[s] || refcounts[cow_src[s]] != 0)
+            continue;
+        int is_last = 1;
+        for (int t = s + 1; t < num_seqs; ++t)
+            if (copy[t] && cow_src[t] == cow_src[s])
+                is_last = 0;
+        if (is_last)
+            freed[nfreed++] = cow_src[s];
+    }
+    *free_count = top - taken;
+    for (int i = 0; i < nfreed; ++i)
+        free_blocks[(*free_count)++] = freed[i];
+    free(freed);
+    free(copy);
+    free(first);
+    free(last);
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* threads                                                                   */
 /* ------------------------------------------------------------------------ */

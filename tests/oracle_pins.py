@@ -385,6 +385,133 @@ def pin_block_alloc(o):
     assert np.array_equal(st["tables"], t0) and np.array_equal(st["refc"], r0)
 
 
+
+def _chunk_state(seed, chunks, NB=128):
+    """A pre-step state from make_state, with sequence s bringing chunks[s %
+    len(chunks)] new tokens (empty sequences bring none)."""
+    from alloc_cases import make_state
+    st = make_state(seed, NB=NB)
+    pre = np.where(st["ctx"] > 0, st["ctx"] - 1, 0)
+    c = np.array([chunks[i % len(chunks)] if pre[i] > 0 else 0 for i in range(len(pre))], np.int32)
+    st["ctx"] = (pre + c).astype(np.int32)
+    st["qs"] = np.concatenate([[0], np.cumsum(c)]).astype(np.int32)
+    st["pre"] = pre
+    return st
+
+
+def pin_block_alloc_chunk(o):
+    """Allocation for a chunk of new tokens per sequence.  (1) One-token
+    chunks give exactly what the single-token allocator gives.  (2) Any
+    chunks keep the allocator's invariants: blocks conserved, reference
+    counts equal to the references in the tables, every block the chunk
+    writes owned by the sequence alone, earlier entries and logical rows
+    unchanged, fresh blocks from the top of the stack in sequence order
+    (a sequence's copy first).  (3) A chunk allocated at once and then
+    written holds the same logical rows as its tokens allocated and written
+    one at a time.  (4) A short stack changes nothing."""
+    from alloc_cases import gather_rows, make_state
+    # (1) one-token chunks
+    for seed in (1, 2, 3):
+        a, b = make_state(seed), make_state(seed)
+        fa = np.concatenate([a["free"], np.zeros(a["NB"], np.int32)])
+        fb = fa.copy()
+        c = (b["ctx"] > 0).astype(np.int32)
+        qs = np.concatenate([[0], np.cumsum(c)]).astype(np.int32)
+        ra = o.block_alloc(a["tables"], a["ctx"], a["B"], fa, a["free_count"], a["refc"], a["k"], a["v"])
+        rb = o.block_alloc_chunk(b["tables"], b["ctx"], qs, b["B"], fb, b["free_count"], b["refc"], b["k"], b["v"])
+        assert ra[0] == rb[0] == 0 and ra[1] == rb[1] and np.array_equal(ra[2], rb[2])
+        for x, y in ((a["tables"], b["tables"]), (fa, fb), (a["refc"], b["refc"]), (a["k"], b["k"]), (a["v"], b["v"])):
+            assert np.array_equal(x, y)
+    # (2) invariants, chunks crossing block boundaries from shared and private blocks
+    for seed, chunks in ((1, [2, 7, 1, 4]), (2, [3, 9, 4, 13]), (3, [1, 5, 8, 12])):
+        st = _chunk_state(seed, chunks)
+        B, NB = st["B"], st["NB"]
+        t0, r0, f0 = st["tables"].copy(), st["refc"].copy(), st["free"].copy()
+        k0, v0 = st["k"].copy(), st["v"].copy()
+        tables, refc = st["tables"], st["refc"]
+        free = np.concatenate([st["free"], np.zeros(NB, np.int32)])
+        status, fc, cow = o.block_alloc_chunk(tables, st["ctx"], st["qs"], B, free, st["free_count"], refc,
+                                              st["k"], st["v"])
+        assert status == 0
+        ctx, pre, S = st["ctx"], st["pre"], len(st["ctx"])
+        recount = np.zeros(NB, np.int32)
+        for s_ in range(S):
+            for j in range((int(ctx[s_]) + B - 1) // B):
+                assert 0 <= tables[s_, j] < NB
+                recount[tables[s_, j]] += 1
+        assert np.array_equal(recount, refc)
+        free_now = free[:fc]
+        assert len(set(free_now.tolist())) == fc
+        assert not (set(free_now.tolist()) & set(np.flatnonzero(recount).tolist()))
+        assert fc + np.count_nonzero(recount) == NB
+        taken = 0
+        for s_ in range(S):
+            n, old = int(ctx[s_]), int(pre[s_])
+            if n == old:
+                assert np.array_equal(tables[s_], t0[s_]) and cow[s_] == -1
+                continue
+            j0, jl = old // B, (n - 1) // B
+            shared = old % B != 0 and r0[t0[s_, j0]] > 1
+            assert np.array_equal(tables[s_, :j0], t0[s_, :j0])      # earlier entries unchanged
+            for j in range(j0 if old % B else old // B, jl + 1):
+                assert refc[tables[s_, j]] == 1                      # written blocks owned alone
+            if old % B != 0 and not shared:
+                assert tables[s_, j0] == t0[s_, j0]                  # sole owner: in place
+            assert cow[s_] == (t0[s_, j0] if shared else -1)
+            first = j0 if (old % B == 0 or shared) else j0 + 1
+            for j in range(first, jl + 1):
+                assert tables[s_, j] == f0[st["free_count"] - 1 - taken]  # stack top, in order
+                taken += 1
+            for c0, c1 in ((k0, st["k"]), (v0, st["v"])):
+                a_ = gather_rows(t0, old, s_, c0, B)
+                b_ = gather_rows(tables, old, s_, c1, B)
+                assert (a_ is None and b_ is None) or np.array_equal(a_, b_)
+        assert fc == st["free_count"] - taken + len(set(int(c) for c in cow if c >= 0 and refc[c] == 0))
+    # (3) at once vs token by token: the same logical rows once the chunk is written
+    for seed, chunks in ((4, [3, 6, 9]), (5, [1, 4, 10, 2])):
+        a, b = _chunk_state(seed, chunks), _chunk_state(seed, chunks)
+        B = a["B"]
+        rows = np.random.default_rng(seed + 7).integers(0, 2**15, size=(len(a["ctx"]), 64) + a["k"].shape[1:2]
+                                                        + a["k"].shape[3:]).astype(a["k"].dtype)
+        fa = np.concatenate([a["free"], np.zeros(a["NB"], np.int32)])
+        st_, fca, _ = o.block_alloc_chunk(a["tables"], a["ctx"], a["qs"], B, fa, a["free_count"], a["refc"],
+                                          a["k"], a["v"])
+        assert st_ == 0
+        for s_ in range(len(a["ctx"])):
+            for t in range(int(a["pre"][s_]), int(a["ctx"][s_])):
+                blk = a["tables"][s_, t // B]
+                a["k"][blk, :, t % B] = rows[s_, t - a["pre"][s_]]
+                a["v"][blk, :, t % B] = rows[s_, t - a["pre"][s_]] ^ 1
+        fb = np.concatenate([b["free"], np.zeros(b["NB"], np.int32)])
+        fcb = b["free_count"]
+        cur = b["pre"].copy()
+        for _ in range(int((b["ctx"] - b["pre"]).max())):
+            grow = (cur < b["ctx"]).astype(np.int32)
+            n1 = (cur + grow).astype(np.int32)
+            qs1 = np.concatenate([[0], np.cumsum(grow)]).astype(np.int32)
+            st1, fcb, _ = o.block_alloc_chunk(b["tables"], n1, qs1, B, fb, fcb, b["refc"], b["k"], b["v"])
+            assert st1 == 0
+            for s_ in np.flatnonzero(grow):
+                t = int(cur[s_])
+                blk = b["tables"][s_, t // B]
+                b["k"][blk, :, t % B] = rows[s_, t - b["pre"][s_]]
+                b["v"][blk, :, t % B] = rows[s_, t - b["pre"][s_]] ^ 1
+            cur = n1
+        assert fca == fcb
+        for s_ in range(len(a["ctx"])):
+            n = int(a["ctx"][s_])
+            for x, y in ((a["k"], b["k"]), (a["v"], b["v"])):
+                ga, gb = gather_rows(a["tables"], n, s_, x, B), gather_rows(b["tables"], n, s_, y, B)
+                assert (ga is None and gb is None) or np.array_equal(ga, gb)
+    # (4) a short stack changes nothing
+    st = _chunk_state(6, [5, 9])
+    st["free"] = st["free"][:3]
+    t0, r0, f0 = st["tables"].copy(), st["refc"].copy(), st["free"].copy()
+    status, fc, cow = o.block_alloc_chunk(st["tables"], st["ctx"], st["qs"], st["B"], st["free"], 3, st["refc"],
+                                          st["k"], st["v"])
+    assert status == 1 and fc == 3 and np.all(cow == -1)
+    assert np.array_equal(st["tables"], t0) and np.array_equal(st["refc"], r0) and np.array_equal(st["free"], f0)
+
 def pin_prefill(o):
     """Chunked prefill: a chunk covering the whole sequence is causal
     attention (torch SDPA, is_causal); a chunk after a cached prefix is SDPA
@@ -564,5 +691,6 @@ def pin_decode_pairs(o):
 ALL = [pin_kv_formula, pin_e4m3_decode, pin_e4m3_encode, pin_e4m3_roundtrip, pin_attention_sdpa,
        pin_attention_fp8, pin_extreme_scores, pin_permutation, pin_prefix_sharing, pin_context_one,
        pin_identical_keys, pin_empty_context, pin_slot_mapping, pin_append_readback,
-       pin_partition_merge, pin_fp8_per_head_scales, pin_block_alloc, pin_prefill, pin_fp8_qk,
+       pin_partition_merge, pin_fp8_per_head_scales, pin_block_alloc, pin_block_alloc_chunk, pin_prefill,
+       pin_fp8_qk,
        pin_decode_pairs]

@@ -1,8 +1,8 @@
 """Each plausible mistake planted in a COPY of the oracle (compiled on the CPU
 into a temporary directory) must trip at least one pin.  This shows the pins
 constrain every part of the oracle: the gather index, the grouping, the
-softmax, the value sum, the fp8 codec, the slot formula, the append and the
-partition merge."""
+softmax, the value sum, the fp8 codec, the slot formula, the append, the
+partition merge and both block allocators."""
 import os
 import subprocess
 import sys
@@ -75,6 +75,14 @@ MUTANTS = {
     "pairs_output_row_of_sequence": ("kv_dtype, kv_scale, kv_scale, x,\n                     out + (int64_t)i * head_dim, &m, &l);",
                                      "kv_dtype, kv_scale, kv_scale, x,\n                     out + (int64_t)s * head_dim, &m, &l);"),
     "partition_short": ("int t1 = t0 + partition_size;", "int t1 = t0 + partition_size - 1;"),
+    "chunk_alloc_copies_sole_owner": ("refcounts[cur] > 1)\n                copy[s] = 1;",
+                                      "refcounts[cur] > 0)\n                copy[s] = 1;"),
+    "chunk_alloc_partial_block_fresh": ("first[s] = old / block_size + 1;", "first[s] = old / block_size;"),
+    "chunk_alloc_last_block_missed": ("last[s] = (n - 1) / block_size;", "last[s] = (n - 2) / block_size;"),
+    "chunk_alloc_copy_short": ("int rows = old % block_size;", "int rows = old % block_size - 1;"),
+    "chunk_alloc_blocks_reversed": ("for (int j = first[s]; j <= last[s]; ++j) {",
+                                    "for (int j = last[s]; j >= first[s]; --j) {"),
+    "chunk_alloc_no_release": ("refcounts[src_block] -= 1;", "refcounts[src_block] -= 0;"),
     "last_token_dropped": ("attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s],",
                            "attend_range(q + ((int64_t)s * num_q_heads + hq) * head_dim, k_cache, v_cache,\n                             block_tables, max_blocks_per_seq, s, kvh, 0, context_lens[s] - (context_lens[s] > 1),"),
 }
