@@ -305,6 +305,35 @@ pa_status pa_block_alloc(int32_t *block_tables, int max_blocks_per_seq, int32_t 
                          int32_t *cow_src, cudaStream_t stream);
 
 /*
+ * pa_block_alloc_chunk -- the same for a chunk of new tokens per sequence
+ * (chunked prefill).  Same source and readings as pa_block_alloc.
+ *   query_start  int32 [num_seqs + 1] (device): sequence s brings
+ *                c = query_start[s+1] - query_start[s] tokens at the end of
+ *                its context; context_lens[s] (device, read only) counts
+ *                them, so old = context_lens[s] - c tokens are cached.
+ *   For each sequence with c > 0:
+ *     if old % block_size != 0 and refcounts[block_tables[s][old / B]] > 1
+ *       (counted before the call): that entry = a fresh block holding a
+ *       copy of rows [0, old % block_size) of the old block (every KV head,
+ *       K and V), and the old block loses one reference;
+ *     every logical block from (old % B ? old / B + 1 : old / B) to
+ *       (context_lens[s] - 1) / B gets a fresh block.
+ *   Fresh blocks come off the top of the stack in sequence order, a
+ *   sequence's copy first and then its new blocks in logical order; freed
+ *   blocks go back as in pa_block_alloc.  A sequence with c > context_lens[s]
+ *   or a last block past max_blocks_per_seq is left alone and
+ *   PA_DEVERR_BAD_CONTEXT is set.  If the stack holds fewer blocks than
+ *   needed nothing changes and PA_DEVERR_OUT_OF_BLOCKS is set.
+ *   num_seqs <= 16384.  Two kernels (decide, copy).
+ */
+pa_status pa_block_alloc_chunk(int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *context_lens, const int32_t *query_start,
+                               int num_seqs, int block_size, int32_t *free_blocks,
+                               int32_t *free_count, int32_t *refcounts, int num_blocks,
+                               void *k_cache, void *v_cache, int num_kv_heads, int head_dim,
+                               pa_kv_dtype kv_dtype, int32_t *cow_src, cudaStream_t stream);
+
+/*
  * pa_decode_step_fp8_qk -- pa_decode_step_scaled with the scores taken as an
  * E4M3 x E4M3 tensor-core product (the first ranked variant of the FP8 KV
  * cache; the tuning guide's Step 3 quantises only the cache, so this is an

@@ -48,6 +48,7 @@ SIGNATURES = {
     "pa_decode_step_fp8_qk": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P,
                                    _P, _F, _F, _I, _P, _SZ, _P, _P, _P]),
     "pa_block_alloc": (_I, [_P, _I, _P, _I, _I, _I, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P]),
+    "pa_block_alloc_chunk": (_I, [_P, _I, _P, _P, _I, _I, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P]),
     "pa_chunk_slot_mapping": (_I, [_P, _I, _P, _P, _I, _I, _P, _P]),
     "pa_prefill": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _F, _P,
                         _P]),

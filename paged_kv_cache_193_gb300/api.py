@@ -320,6 +320,26 @@ class DeviceBlockPool:
             _stream(stream)))
         return cow_src
 
+    def allocate_chunk(self, block_tables, context_lens, query_start, k_cache, v_cache, cow_src=None,
+                       stream=None) -> torch.Tensor:
+        """Fresh blocks / copy-on-write for a chunk of new tokens per sequence
+        (see pa_block_alloc_chunk; context_lens counts the chunk); returns
+        cow_src (int32 [S])."""
+        _need(block_tables, "block_tables", (torch.int32,), 2)
+        _need(context_lens, "context_lens", (torch.int32,), 1)
+        _need(query_start, "query_start", (torch.int32,), 1)
+        kv_dtype = cache_dtype_of(k_cache)
+        NB, Hkv, B, D = k_cache.shape
+        S, MB = block_tables.shape
+        if cow_src is None:
+            cow_src = torch.empty(S, dtype=torch.int32, device=block_tables.device)
+        _check(_lib_handle().pa_block_alloc_chunk(
+            block_tables.data_ptr(), MB, context_lens.data_ptr(), query_start.data_ptr(), S, B,
+            self.free_blocks.data_ptr(), self.free_count.data_ptr(), self.refcounts.data_ptr(), NB,
+            k_cache.data_ptr(), v_cache.data_ptr(), Hkv, D, kv_dtype, cow_src.data_ptr(),
+            _stream(stream)))
+        return cow_src
+
 
 def decode_partitions(q, k_cache, v_cache, block_tables, context_lens, softmax_scale, kv_scale,
                       partition_size, workspace, stream=None) -> None:

@@ -51,6 +51,19 @@ def make_state(seed: int, B: int = 4, NB: int = 64, Hkv: int = 2, D: int = 8, el
                 B=B, NB=NB)
 
 
+def make_chunk_state(seed, chunks, NB=128, **kw):
+    """A pre-step state from make_state in which sequence s brings
+    chunks[s % len(chunks)] new tokens (empty sequences bring none):
+    ctx counts them, qs holds the chunk offsets, pre the cached lengths."""
+    st = make_state(seed, NB=NB, **kw)
+    pre = np.where(st["ctx"] > 0, st["ctx"] - 1, 0)
+    c = np.array([chunks[i % len(chunks)] if pre[i] > 0 else 0 for i in range(len(pre))], np.int32)
+    st["ctx"] = (pre + c).astype(np.int32)
+    st["qs"] = np.concatenate([[0], np.cumsum(c)]).astype(np.int32)
+    st["pre"] = pre.astype(np.int32)
+    return st
+
+
 def gather_rows(tables, n, s, cache, B):
     """Logical rows [0, n) of sequence s through its table (all heads)."""
     return np.stack([cache[tables[s, t // B], :, t % B] for t in range(n)]) if n else None

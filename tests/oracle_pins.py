@@ -386,19 +386,6 @@ def pin_block_alloc(o):
 
 
 
-def _chunk_state(seed, chunks, NB=128):
-    """A pre-step state from make_state, with sequence s bringing chunks[s %
-    len(chunks)] new tokens (empty sequences bring none)."""
-    from alloc_cases import make_state
-    st = make_state(seed, NB=NB)
-    pre = np.where(st["ctx"] > 0, st["ctx"] - 1, 0)
-    c = np.array([chunks[i % len(chunks)] if pre[i] > 0 else 0 for i in range(len(pre))], np.int32)
-    st["ctx"] = (pre + c).astype(np.int32)
-    st["qs"] = np.concatenate([[0], np.cumsum(c)]).astype(np.int32)
-    st["pre"] = pre
-    return st
-
-
 def pin_block_alloc_chunk(o):
     """Allocation for a chunk of new tokens per sequence.  (1) One-token
     chunks give exactly what the single-token allocator gives.  (2) Any
@@ -409,7 +396,7 @@ def pin_block_alloc_chunk(o):
     (a sequence's copy first).  (3) A chunk allocated at once and then
     written holds the same logical rows as its tokens allocated and written
     one at a time.  (4) A short stack changes nothing."""
-    from alloc_cases import gather_rows, make_state
+    from alloc_cases import gather_rows, make_chunk_state, make_state
     # (1) one-token chunks
     for seed in (1, 2, 3):
         a, b = make_state(seed), make_state(seed)
@@ -424,7 +411,7 @@ def pin_block_alloc_chunk(o):
             assert np.array_equal(x, y)
     # (2) invariants, chunks crossing block boundaries from shared and private blocks
     for seed, chunks in ((1, [2, 7, 1, 4]), (2, [3, 9, 4, 13]), (3, [1, 5, 8, 12])):
-        st = _chunk_state(seed, chunks)
+        st = make_chunk_state(seed, chunks)
         B, NB = st["B"], st["NB"]
         t0, r0, f0 = st["tables"].copy(), st["refc"].copy(), st["free"].copy()
         k0, v0 = st["k"].copy(), st["v"].copy()
@@ -469,7 +456,7 @@ def pin_block_alloc_chunk(o):
         assert fc == st["free_count"] - taken + len(set(int(c) for c in cow if c >= 0 and refc[c] == 0))
     # (3) at once vs token by token: the same logical rows once the chunk is written
     for seed, chunks in ((4, [3, 6, 9]), (5, [1, 4, 10, 2])):
-        a, b = _chunk_state(seed, chunks), _chunk_state(seed, chunks)
+        a, b = make_chunk_state(seed, chunks), make_chunk_state(seed, chunks)
         B = a["B"]
         rows = np.random.default_rng(seed + 7).integers(0, 2**15, size=(len(a["ctx"]), 64) + a["k"].shape[1:2]
                                                         + a["k"].shape[3:]).astype(a["k"].dtype)
@@ -504,7 +491,7 @@ def pin_block_alloc_chunk(o):
                 ga, gb = gather_rows(a["tables"], n, s_, x, B), gather_rows(b["tables"], n, s_, y, B)
                 assert (ga is None and gb is None) or np.array_equal(ga, gb)
     # (4) a short stack changes nothing
-    st = _chunk_state(6, [5, 9])
+    st = make_chunk_state(6, [5, 9])
     st["free"] = st["free"][:3]
     t0, r0, f0 = st["tables"].copy(), st["refc"].copy(), st["free"].copy()
     status, fc, cow = o.block_alloc_chunk(st["tables"], st["ctx"], st["qs"], st["B"], st["free"], 3, st["refc"],

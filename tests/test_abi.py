@@ -264,3 +264,33 @@ def test_block_alloc_rejects_on_host(lib, kw, status):
 
 def test_empty_block_alloc_is_a_no_op(lib):
     assert _alloc(lib, S=0, bt=None, free=None) == 0
+
+
+def _alloc_chunk(lib, **kw):
+    a = dict(bt=FAKE, mb=8, cl=FAKE, qs=FAKE, S=4, B=16, free=FAKE, fc=FAKE, rc=FAKE, NB=64, kc=FAKE,
+             vc=FAKE, Hkv=2, D=64, dt=0, cow=FAKE)
+    a.update(kw)
+    return lib.pa_block_alloc_chunk(a["bt"], a["mb"], a["cl"], a["qs"], a["S"], a["B"], a["free"], a["fc"],
+                                    a["rc"], a["NB"], a["kc"], a["vc"], a["Hkv"], a["D"], a["dt"], a["cow"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(NB=0), 1),
+    (dict(mb=0), 1),
+    (dict(S=-1), 1),
+    (dict(S=16385), 2),
+    (dict(D=96), 2),
+    (dict(B=8), 2),
+    (dict(dt=7), 2),
+    (dict(qs=None), 1),
+    (dict(free=None), 1),
+    (dict(cow=None), 1),
+    (dict(kc=ctypes.c_void_p((1 << 20) + 4)), 1),
+])
+def test_block_alloc_chunk_rejects_on_host(lib, kw, status):
+    assert _alloc_chunk(lib, **kw) == status
+    assert lib.pa_last_error()
+
+
+def test_empty_block_alloc_chunk_is_a_no_op(lib):
+    assert _alloc_chunk(lib, S=0, bt=None, qs=None, free=None) == 0

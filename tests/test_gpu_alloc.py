@@ -1,13 +1,15 @@
 """Device-side block allocation with copy-on-write: bit for bit against the
 oracle (tables, free stack, counts, reference counts, copied rows), the
 all-or-nothing refusal, and a device-driven decode loop (allocate with
-advance, then the fused step) against the oracle step by step."""
+advance, then the fused step) against the oracle step by step; the same for
+a chunk of new tokens per sequence, and a device-driven chunked prefill."""
 import numpy as np
 import pytest
 import torch
 
-from alloc_cases import make_state
+from alloc_cases import make_chunk_state, make_state
 from gpu_helpers import compare
+from paged_kv_cache_193_gb300 import _lib
 from paged_kv_cache_193_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -126,3 +128,93 @@ def test_device_driven_decode_loop(api, oracle, cuda_device):
         assert np.array_equal(cl.cpu().numpy(), h_ctx)
         assert np.array_equal(W.bits(dk), h_k) and np.array_equal(W.bits(dv), h_v)
     assert api.device_errors() == 0
+
+
+# ---------------------------------------------------------------------------
+# a chunk of new tokens per sequence (chunked prefill)
+# ---------------------------------------------------------------------------
+
+def _chunk_both(api, oracle, dev, st):
+    B, NB = st["B"], st["NB"]
+    pool = api.DeviceBlockPool(st["free"], st["refc"], dev)
+    bt = torch.from_numpy(st["tables"].copy()).to(dev)
+    cl = torch.from_numpy(st["ctx"]).to(dev)
+    qs = torch.from_numpy(st["qs"]).to(dev)
+    kc = W.from_bits(st["k"], dev)
+    vc = W.from_bits(st["v"], dev)
+    cow = pool.allocate_chunk(bt, cl, qs, kc, vc)
+    torch.cuda.synchronize()
+    tables, refc = st["tables"].copy(), st["refc"].copy()
+    free = np.concatenate([st["free"], np.zeros(NB, np.int32)])[:NB].copy()
+    k, v = st["k"].copy(), st["v"].copy()
+    status, fc, cow_ref = oracle.block_alloc_chunk(tables, st["ctx"], st["qs"], B, free, st["free_count"],
+                                                   refc, k, v)
+    return dict(pool=pool, bt=bt, cl=cl, qs=qs, kc=kc, vc=vc, cow=cow), dict(
+        status=status, fc=fc, tables=tables, refc=refc, free=free, k=k, v=v, cow=cow_ref)
+
+
+@pytest.mark.parametrize("seed,chunks", [(1, [2, 7, 1, 4]), (2, [3, 9, 4, 13]), (3, [1, 5, 8, 12]),
+                                         (4, [17, 40, 33, 1])])
+@pytest.mark.parametrize("B", [16, 32])
+def test_block_alloc_chunk_matches_oracle(api, oracle, cuda_device, seed, chunks, B):
+    """Chunks crossing block boundaries from shared (full and partly filled)
+    and private blocks: tables, free stack, counts, reference counts,
+    copy sources and copied rows bit for bit."""
+    st = make_chunk_state(seed, chunks, B=B, NB=192, Hkv=2, D=128)
+    gpu, ref = _chunk_both(api, oracle, cuda_device, st)
+    assert ref["status"] == 0
+    fc = int(gpu["pool"].free_count.item())
+    assert fc == ref["fc"]
+    assert np.array_equal(gpu["pool"].free_blocks.cpu().numpy()[:fc], ref["free"][:fc])
+    assert np.array_equal(gpu["pool"].refcounts.cpu().numpy(), ref["refc"])
+    assert np.array_equal(gpu["bt"].cpu().numpy(), ref["tables"])
+    assert np.array_equal(gpu["cow"].cpu().numpy(), ref["cow"])
+    assert np.array_equal(W.bits(gpu["kc"]), ref["k"]) and np.array_equal(W.bits(gpu["vc"]), ref["v"])
+    assert api.device_errors() == 0
+
+
+def test_block_alloc_chunk_short_stack_changes_nothing(api, oracle, cuda_device):
+    st = make_chunk_state(6, [5, 9, 40], B=16, NB=192, Hkv=2, D=128)
+    st["free"] = st["free"][:3]
+    st["free_count"] = 3
+    api.device_errors(clear=True)
+    gpu, ref = _chunk_both(api, oracle, cuda_device, st)
+    assert ref["status"] == 1
+    assert int(gpu["pool"].free_count.item()) == 3
+    assert np.array_equal(gpu["bt"].cpu().numpy(), st["tables"])
+    assert np.array_equal(gpu["pool"].refcounts.cpu().numpy(), st["refc"])
+    assert np.all(gpu["cow"].cpu().numpy() == -1)
+    assert api.device_errors(clear=True) == _lib.PA_DEVERR_OUT_OF_BLOCKS
+
+
+@pytest.mark.parametrize("B", [16, 32])
+def test_device_driven_chunked_prefill(api, oracle, cuda_device, B):
+    """Sequences sharing prompt blocks each bring a chunk: blocks allocated on
+    the device, chunk slots, the chunk's append and the attention, against
+    the oracle doing the same four steps."""
+    st = make_chunk_state(7, [3, 21, 40, 9], B=B, NB=192, Hkv=2, D=128)
+    S = len(st["ctx"])
+    g = torch.Generator().manual_seed(B)
+    # the pool's rows as N(0, 1) values (the allocation states carry raw bits)
+    for name in ("k", "v"):
+        st[name] = W.bits(torch.randn(st[name].shape, generator=g).to(torch.bfloat16))
+    T = int(st["qs"][-1])
+    q = torch.randn((T, 8, 128), generator=g).to(torch.bfloat16)
+    k_new = torch.randn((T, 2, 128), generator=g).to(torch.bfloat16)
+    v_new = torch.randn((T, 2, 128), generator=g).to(torch.bfloat16)
+    gpu, ref = _chunk_both(api, oracle, cuda_device, st)
+    assert ref["status"] == 0
+    slots = api.chunk_slot_mapping(gpu["bt"], gpu["cl"], gpu["qs"], B)
+    api.cache_append(k_new.to(cuda_device), v_new.to(cuda_device), slots, gpu["kc"], gpu["vc"])
+    out = api.prefill(q.to(cuda_device), gpu["kc"], gpu["vc"], gpu["bt"], gpu["cl"], gpu["qs"],
+                      int(np.diff(st["qs"]).max()), 1.0 / np.sqrt(128))
+    torch.cuda.synchronize()
+    slots_ref = oracle.chunk_slot_mapping(ref["tables"], st["ctx"], st["qs"], B)
+    oracle.cache_append(W.bits(k_new), W.bits(v_new), slots_ref, ref["k"], ref["v"], B, 0, 1.0)
+    out_ref = oracle.prefill(W.bits(q), ref["k"], ref["v"], ref["tables"], st["ctx"], st["qs"], 2, B,
+                             1.0 / np.sqrt(128))
+    assert np.array_equal(slots.cpu().numpy(), slots_ref)
+    assert np.array_equal(W.bits(gpu["kc"]), ref["k"]) and np.array_equal(W.bits(gpu["vc"]), ref["v"])
+    compare(out, out_ref, what=f"device-driven chunked prefill B{B}")
+    assert api.device_errors() == 0
+    assert S > 0
