@@ -66,6 +66,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
                                             I, P]
     lib.pa_oracle_block_alloc.restype = I
     lib.pa_oracle_block_alloc.argtypes = [P, I, P, I, I, P, P, P, I, P, P, I, I, I, P]
+    lib.pa_oracle_prefill_scaled.restype = None
+    lib.pa_oracle_prefill_scaled.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, D, P, P, P]
     lib.pa_oracle_block_alloc_chunk.restype = I
     lib.pa_oracle_block_alloc_chunk.argtypes = [P, I, P, P, I, I, P, P, P, I, P, P, I, I, I, P]
     lib.pa_oracle_chunk_slot_mapping.restype = None
@@ -293,6 +295,25 @@ class Oracle:
         self.lib.pa_oracle_prefill(_p(q), _p(kc), _p(vc), _p(bt), bt.shape[1], _p(cl), _p(qs),
                                    cl.shape[0], Hq, num_kv_heads, D, block_size,
                                    float(softmax_scale), kv_dtype, float(kv_scale), _p(out))
+        return out
+
+    def prefill_scaled(self, q_bits, k_cache, v_cache, block_tables, context_lens, query_start,
+                       num_kv_heads, block_size, softmax_scale, k_scales, v_scales) -> np.ndarray:
+        """fp64 [Tq, Hq, D]: chunked prefill over an E4M3 cache with a K and
+        a V scale per KV head."""
+        q = _c(q_bits, np.uint16)
+        bt = _c(block_tables, np.int32)
+        cl = _c(context_lens, np.int32)
+        qs = _c(query_start, np.int32)
+        kc = np.ascontiguousarray(k_cache)
+        vc = np.ascontiguousarray(v_cache)
+        ks = _c(k_scales, np.float32)
+        vs = _c(v_scales, np.float32)
+        T, Hq, D = q.shape
+        out = np.zeros((T, Hq, D), np.float64)
+        self.lib.pa_oracle_prefill_scaled(_p(q), _p(kc), _p(vc), _p(bt), bt.shape[1], _p(cl), _p(qs),
+                                          cl.shape[0], Hq, num_kv_heads, D, block_size, float(softmax_scale),
+                                          _p(ks), _p(vs), _p(out))
         return out
 
     # -- block allocation with copy-on-write ------------------------------------

@@ -547,6 +547,38 @@ void pa_oracle_prefill(const uint16_t *q, const void *k_cache, const void *v_cac
     }
 }
 
+/* Chunked prefill over an E4M3 cache with a K scale and a V scale per KV
+ * head (k_scales[h], v_scales[h]), as pa_oracle_decode_scaled reads it;
+ * otherwise as pa_oracle_prefill. */
+void pa_oracle_prefill_scaled(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, const int32_t *query_start, int num_seqs,
+                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                              double softmax_scale, const float *k_scales, const float *v_scales,
+                              double *out)
+{
+    int group = num_q_heads / num_kv_heads;
+    int total = query_start[num_seqs];
+#pragma omp parallel for schedule(dynamic)
+    for (int i = 0; i < total; ++i) {
+        int s = 0;
+        while (query_start[s + 1] <= i)
+            ++s;
+        int c = query_start[s + 1] - query_start[s];
+        int pos = context_lens[s] - c + (i - query_start[s]);
+        double *x = (double *)malloc(sizeof(double) * (size_t)(context_lens[s] > 0 ? context_lens[s] : 1));
+        for (int hq = 0; hq < num_q_heads; ++hq) {
+            int kvh = hq / group;
+            double m, l;
+            attend_range(q + ((int64_t)i * num_q_heads + hq) * head_dim, k_cache, v_cache,
+                         block_tables, max_blocks_per_seq, s, kvh, 0, pos + 1, num_kv_heads, head_dim,
+                         block_size, softmax_scale, 1, (double)k_scales[kvh], (double)v_scales[kvh], x,
+                         out + ((int64_t)i * num_q_heads + hq) * head_dim, &m, &l);
+        }
+        free(x);
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* block allocation for the newest tokens, with copy-on-write                */
 /* ------------------------------------------------------------------------ */

@@ -319,6 +319,38 @@ def pin_fp8_per_head_scales(o):
     assert np.array_equal(k1, k2) and np.array_equal(v1, v2)
 
 
+
+def pin_prefill_scaled(o):
+    """Chunked prefill over an E4M3 cache with a scale per KV head for K and
+    for V: every chunk's last row equals the per-head-scaled decode (pinned
+    against torch) bit for bit; with one scale everywhere it equals the
+    one-scale prefill bit for bit."""
+    rng = np.random.default_rng(16)
+    c = _case(Hq=12, Hkv=3, seed=42)
+    B = 16
+    tables, _, _ = c.paged(B, 30, rng)
+    ks = np.array([0.011, 0.023, 0.007], np.float32)
+    vs = np.array([0.019, 0.005, 0.031], np.float32)
+    kc = np.full((30, c.Hkv, B, c.D), 0x7F, np.uint8)
+    vc = np.full_like(kc, 0x7F)
+    for s_, n in enumerate(c.ctx):
+        slots = np.array([tables[s_, t // B] * B + t % B for t in range(n)], np.int32)
+        o.cache_append_scaled(c.k[s_].transpose(1, 0, 2), c.v[s_].transpose(1, 0, 2), slots, kc, vc, B, ks, vs)
+    ctx = np.array(c.ctx, np.int32)
+    chunk = np.minimum(ctx, np.array([3, 1, 7, 2, 5, 4, 6, 8][:len(ctx)], np.int32))
+    qs = np.concatenate([[0], np.cumsum(chunk)]).astype(np.int32)
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn(int(qs[-1]), c.Hq, c.D, generator=g).to(torch.bfloat16)
+    qb = q.view(torch.int16).numpy().view(np.uint16)
+    out = o.prefill_scaled(qb, kc, vc, tables, ctx, qs, c.Hkv, B, 0.21, ks, vs)
+    live = np.flatnonzero(chunk > 0)
+    last = qs[1:][live] - 1
+    dec = o.decode_scaled(qb[last], kc, vc, tables[live], ctx[live], c.Hkv, B, 0.21, ks, vs)
+    assert np.array_equal(out[last], dec)
+    same = np.full(c.Hkv, 0.013, np.float32)
+    one = o.prefill(qb, kc, vc, tables, ctx, qs, c.Hkv, B, 0.21, kv_dtype=1, kv_scale=float(same[0]))
+    assert np.array_equal(o.prefill_scaled(qb, kc, vc, tables, ctx, qs, c.Hkv, B, 0.21, same, same), one)
+
 def pin_block_alloc(o):
     """Allocation for the newest tokens: checked against invariants that any
     correct allocator with these rules keeps (conservation of blocks,
@@ -678,6 +710,7 @@ def pin_decode_pairs(o):
 ALL = [pin_kv_formula, pin_e4m3_decode, pin_e4m3_encode, pin_e4m3_roundtrip, pin_attention_sdpa,
        pin_attention_fp8, pin_extreme_scores, pin_permutation, pin_prefix_sharing, pin_context_one,
        pin_identical_keys, pin_empty_context, pin_slot_mapping, pin_append_readback,
-       pin_partition_merge, pin_fp8_per_head_scales, pin_block_alloc, pin_block_alloc_chunk, pin_prefill,
+       pin_partition_merge, pin_fp8_per_head_scales, pin_prefill_scaled, pin_block_alloc, pin_block_alloc_chunk,
+       pin_prefill,
        pin_fp8_qk,
        pin_decode_pairs]

@@ -75,6 +75,10 @@ MUTANTS = {
     "pairs_output_row_of_sequence": ("kv_dtype, kv_scale, kv_scale, x,\n                     out + (int64_t)i * head_dim, &m, &l);",
                                      "kv_dtype, kv_scale, kv_scale, x,\n                     out + (int64_t)s * head_dim, &m, &l);"),
     "partition_short": ("int t1 = t0 + partition_size;", "int t1 = t0 + partition_size - 1;"),
+    "prefill_scaled_kv_swapped": ("softmax_scale, 1, (double)k_scales[kvh], (double)v_scales[kvh], x,",
+                                  "softmax_scale, 1, (double)v_scales[kvh], (double)k_scales[kvh], x,"),
+    "prefill_scaled_head_ignored": ("softmax_scale, 1, (double)k_scales[kvh], (double)v_scales[kvh], x,",
+                                    "softmax_scale, 1, (double)k_scales[0], (double)v_scales[0], x,"),
     "chunk_alloc_copies_sole_owner": ("refcounts[cur] > 1)\n                copy[s] = 1;",
                                       "refcounts[cur] > 0)\n                copy[s] = 1;"),
     "chunk_alloc_partial_block_fresh": ("first[s] = old / block_size + 1;", "first[s] = old / block_size;"),
