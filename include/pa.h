@@ -385,6 +385,11 @@ pa_status pa_decode_step_fp8_qk(const void *q, const void *k_new, const void *v_
  *   widened exactly to fp16 in shared memory and the products run in
  *   fp16 (the query rounded to fp16, exact for bf16 values in its range).
  *   kv_scale is unused for a bf16 cache.
+ * pa_prefill_scaled: the same over an E4M3 cache with a K and a V scale per
+ *   KV head (k_scales, v_scales: float32 [num_kv_heads], device), the cache
+ *   holding x / scale[h] as pa_cache_append_scaled writes it ("Step 3 (FP8
+ *   KV cache)" of the tuning guide; per-head scales are a reading, as for
+ *   pa_decode_step_scaled).  head_dim 128; null scale arrays are rejected.
  * pa_prefill_mma: the same computation always with the warp-level MMA
  *   kernel (kept as the comparison point for the tensor-memory kernel);
  *   bf16 caches only.
@@ -399,6 +404,12 @@ pa_status pa_prefill(const void *q, const void *k_cache, const void *v_cache,
                      int num_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
                      int head_dim, int num_blocks, int block_size, pa_kv_dtype kv_dtype,
                      float kv_scale, float softmax_scale, void *out, cudaStream_t stream);
+pa_status pa_prefill_scaled(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, const int32_t *query_start, int num_seqs,
+                            int num_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
+                            int head_dim, int num_blocks, int block_size, const float *k_scales,
+                            const float *v_scales, float softmax_scale, void *out, cudaStream_t stream);
 pa_status pa_prefill_mma(const void *q, const void *k_cache, const void *v_cache,
                          const int32_t *block_tables, int max_blocks_per_seq,
                          const int32_t *context_lens, const int32_t *query_start, int num_seqs,

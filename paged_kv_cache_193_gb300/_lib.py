@@ -52,6 +52,8 @@ SIGNATURES = {
     "pa_chunk_slot_mapping": (_I, [_P, _I, _P, _P, _I, _I, _P, _P]),
     "pa_prefill": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _F, _P,
                         _P]),
+    "pa_prefill_scaled": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _F, _P,
+                               _P]),
     "pa_prefill_mma": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _F,
                             _P, _P]),
     "pa_decode_static_workspace": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _F,

@@ -288,6 +288,32 @@ def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, max_qu
     return out
 
 
+def prefill_scaled(q, k_cache, v_cache, block_tables, context_lens, query_start, max_query_len,
+                   k_scales, v_scales, softmax_scale=None, out=None, stream=None) -> torch.Tensor:
+    """Chunked prefill over an E4M3 cache (uint8) holding x / scale[h], with
+    a K and a V scale per KV head (float32 device tensors [num_kv_heads])."""
+    _need(q, "q", (torch.bfloat16,), 3)
+    _need(query_start, "query_start", (torch.int32,), 1)
+    _need(k_cache, "k_cache", (torch.uint8,), 4)
+    _need(v_cache, "v_cache", (torch.uint8,), 4)
+    _need(block_tables, "block_tables", (torch.int32,), 2)
+    _need(context_lens, "context_lens", (torch.int32,), 1)
+    _need(k_scales, "k_scales", (torch.float32,), 1)
+    _need(v_scales, "v_scales", (torch.float32,), 1)
+    T, Hq, D = q.shape
+    NB, Hkv, B, _ = k_cache.shape
+    S = context_lens.shape[0]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(_lib_handle().pa_prefill_scaled(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
+        context_lens.data_ptr(), query_start.data_ptr(), S, T, int(max_query_len), Hq, Hkv, D, NB, B,
+        k_scales.data_ptr(), v_scales.data_ptr(), float(softmax_scale), out.data_ptr(), _stream(stream)))
+    return out
+
+
 class DeviceBlockPool:
     """Device-side free stack and reference counts of a paged cache's blocks,
     driven by ``pa_block_alloc``.  Build it from the host state once

@@ -341,14 +341,16 @@ pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_ca
                             const int32_t *context_lens, const int32_t *query_start, int num_seqs,
                             int total_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
                             int head_dim, int num_blocks, int block_size, bool fp8, float kv_scale,
-                            float softmax_scale, void *out, unsigned int *err, cudaStream_t stream);
+                            const float *k_scales, const float *v_scales, float softmax_scale, void *out,
+                            unsigned int *err, cudaStream_t stream);
 static pa_status prefill_impl(const void *q, const void *k_cache, const void *v_cache,
                               const int32_t *block_tables, int max_blocks_per_seq,
                               const int32_t *context_lens, const int32_t *query_start,
                               int num_seqs, int num_tokens, int max_query_len, int num_q_heads,
                               int num_kv_heads, int head_dim, int num_blocks, int block_size,
                               pa_kv_dtype kv_dtype, float kv_scale, float softmax_scale,
-                              void *out, cudaStream_t stream, bool tensor_memory);
+                              void *out, cudaStream_t stream, bool tensor_memory,
+                              const float *k_scales = nullptr, const float *v_scales = nullptr);
 
 }  // namespace pa
 
@@ -399,6 +401,22 @@ pa_status pa_prefill_mma(const void *q, const void *k_cache, const void *v_cache
                         softmax_scale, out, stream, false);
 }
 
+pa_status pa_prefill_scaled(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, const int32_t *query_start, int num_seqs,
+                            int num_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
+                            int head_dim, int num_blocks, int block_size, const float *k_scales,
+                            const float *v_scales, float softmax_scale, void *out, cudaStream_t stream) {
+    if (!k_scales || !v_scales) {
+        clear_error();
+        return fail(PA_ERR_INVALID_ARG, "null scale array");
+    }
+    return prefill_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                        query_start, num_seqs, num_tokens, max_query_len, num_q_heads,
+                        num_kv_heads, head_dim, num_blocks, block_size, PA_KV_FP8_E4M3, 1.f,
+                        softmax_scale, out, stream, true, k_scales, v_scales);
+}
+
 }  // extern "C"
 
 namespace pa {
@@ -409,7 +427,8 @@ static pa_status prefill_impl(const void *q, const void *k_cache, const void *v_
                               int num_seqs, int num_tokens, int max_query_len, int num_q_heads,
                               int num_kv_heads, int head_dim, int num_blocks, int block_size,
                               pa_kv_dtype kv_dtype, float kv_scale, float softmax_scale,
-                              void *out, cudaStream_t stream, bool tensor_memory) {
+                              void *out, cudaStream_t stream, bool tensor_memory,
+                              const float *k_scales, const float *v_scales) {
     clear_error();
     if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || num_q_heads <= 0 ||
         num_kv_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
@@ -428,7 +447,7 @@ static pa_status prefill_impl(const void *q, const void *k_cache, const void *v_
     if (kv_dtype != PA_KV_BF16 && !fp8) return fail(PA_ERR_INVALID_ARG, "unknown kv_dtype %d", static_cast<int>(kv_dtype));
     if (fp8 && !(tensor_memory && head_dim == 128))
         return fail(PA_ERR_UNSUPPORTED, "E4M3 caches: pa_prefill at head_dim 128 only");
-    if (fp8 && !(kv_scale > 0.f && isfinite(kv_scale)))
+    if (fp8 && !k_scales && !(kv_scale > 0.f && isfinite(kv_scale)))
         return fail(PA_ERR_INVALID_ARG, "kv_scale must be positive and finite for an E4M3 cache");
     if (static_cast<int64_t>(num_blocks) * num_kv_heads * block_size > 0x7fffffffLL)
         return fail(PA_ERR_UNSUPPORTED, "pool exceeds 2^31 rows");
@@ -450,7 +469,7 @@ static pa_status prefill_impl(const void *q, const void *k_cache, const void *v_
         return launch_prefill_tc(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                  context_lens, query_start, num_seqs, num_tokens, max_query_len,
                                  num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, fp8,
-                                 kv_scale, softmax_scale, out, err0, stream);
+                                 kv_scale, k_scales, v_scales, softmax_scale, out, err0, stream);
     const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
     CUtensorMap tk, tv;
     pa_status st = make_map(&tk, k_cache, false, head_dim, rows, block_size);

@@ -64,6 +64,8 @@ struct PrefillTcArgs {
     int tile_tokens;  // 128 / group
     float score_scale;       // softmax scale x log2(e) (x the E4M3 scale of K)
     float v_scale;           // the E4M3 scale of V, applied to the output (1 for bf16)
+    const float *k_scales;   // E4M3: a K and a V scale per KV head (device), or null for
+    const float *v_scales;   // the one scale folded into score_scale and v_scale
     uint64_t wait_limit_ns;  // give up on a wait after this long
     int stall_first_wait;    // test hook: the MMA threads' first wait is on a barrier nothing completes
     int num_seqs;
@@ -468,7 +470,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int warp_min_pos = __reduce_min_sync(0xffffffffu, pos);
             const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
             const uint32_t tS = tmem + lane_addr + T * 256, tO = tS + kTcOCol;
-            const float scale = a.score_scale;
+            float scale = a.score_scale;
+            if constexpr (FP8) {
+                if (a.k_scales) scale *= __ldg(a.k_scales + h);
+            }
             float m_ref = -INFINITY, l_run = 0.f;
             // the query tile has landed before its shared memory stages the output
             bool ok = mbar_wait_suspend(smem_addr(&q_full), 0, limit);
@@ -578,7 +583,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = ok && mbar_wait_suspend(smem_addr(&drain[T]), 0, limit);
             tc_fence_after();
             if (!ok) fail();
-            const float inv = l_run > 0.f ? a.v_scale / l_run : 0.f;
+            float v_scale = a.v_scale;
+            if constexpr (FP8) {
+                if (a.v_scales) v_scale = __ldg(a.v_scales + h);
+            }
+            const float inv = l_run > 0.f ? v_scale / l_run : 0.f;
             // A tile wholly inside its chunk leaves through shared memory (its
             // query tile's space, in the same swizzled layout) and two TMA
             // stores; a tile at the chunk's end is written row by row, so no
@@ -680,7 +689,8 @@ pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_ca
                             const int32_t *context_lens, const int32_t *query_start, int num_seqs,
                             int total_tokens, int max_query_len, int num_q_heads, int num_kv_heads,
                             int head_dim, int num_blocks, int block_size, bool fp8, float kv_scale,
-                            float softmax_scale, void *out, unsigned int *err, cudaStream_t stream) {
+                            const float *k_scales, const float *v_scales, float softmax_scale, void *out,
+                            unsigned int *err, cudaStream_t stream) {
     const int group = num_q_heads / num_kv_heads;
     PrefillTcArgs a;
     a.block_tables = block_tables;
@@ -692,8 +702,13 @@ pa_status launch_prefill_tc(const void *q, const void *k_cache, const void *v_ca
     a.num_kv_heads = num_kv_heads;
     a.group = group;
     a.tile_tokens = kTcRows / group;
-    a.score_scale = softmax_scale * 1.4426950408889634f * (fp8 ? kv_scale : 1.f);
-    a.v_scale = fp8 ? kv_scale : 1.f;
+    // E4M3: one scale folds into the score scale and the output; per-head
+    // scales are read by each CTA for its KV head
+    const bool per_head = fp8 && k_scales;
+    a.score_scale = softmax_scale * 1.4426950408889634f * (fp8 && !per_head ? kv_scale : 1.f);
+    a.v_scale = fp8 && !per_head ? kv_scale : 1.f;
+    a.k_scales = per_head ? k_scales : nullptr;
+    a.v_scales = per_head ? v_scales : nullptr;
     a.wait_limit_ns = wait_limit_ns();
     a.stall_first_wait = stall_first_wait();
     a.num_seqs = num_seqs;

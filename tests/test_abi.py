@@ -294,3 +294,20 @@ def test_block_alloc_chunk_rejects_on_host(lib, kw, status):
 
 def test_empty_block_alloc_chunk_is_a_no_op(lib):
     assert _alloc_chunk(lib, S=0, bt=None, qs=None, free=None) == 0
+
+
+
+def test_prefill_scaled_checks_on_host(lib):
+    a = [FAKE, FAKE, FAKE, FAKE, 16, FAKE, FAKE, 4, 64, 32, 8, 2, 128, 64, 16, FAKE, FAKE, 0.088, FAKE, None]
+    bad = list(a)
+    bad[15] = None                                       # no K scales
+    assert lib.pa_prefill_scaled(*bad) == 1 and lib.pa_last_error()
+    bad = list(a)
+    bad[12] = 64                                         # E4M3 caches: head_dim 128 only
+    assert lib.pa_prefill_scaled(*bad) == 2 and lib.pa_last_error()
+    bad = list(a)
+    bad[10], bad[11] = 6, 2                              # group of 3
+    assert lib.pa_prefill_scaled(*bad) == 2
+    empty = list(a)
+    empty[8] = 0                                         # no chunk rows: nothing to do
+    assert lib.pa_prefill_scaled(*empty) == 0

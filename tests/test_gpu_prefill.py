@@ -164,6 +164,48 @@ def test_prefill_e4m3_matches_oracle(api, oracle, cuda_device, G, Hkv, B):
     assert api.device_errors() == 0
 
 
+@pytest.mark.parametrize("G,Hkv,B", [(4, 2, 16), (1, 4, 32), (16, 1, 16)])
+def test_prefill_scaled_matches_oracle(api, oracle, cuda_device, G, Hkv, B):
+    """E4M3 cache with a K and a V scale per KV head: the pool encoded by
+    the oracle with each head's scales, the chunk appended by the library's
+    per-head append (bit for bit), attention against the oracle."""
+    wl = W.make_prefill(cuda_device, seed=90 + G + B, num_seqs=5, chunk=[1, 7, 64, 300, 33],
+                        prefixes=[0, 5, 33, 300, 16], num_q_heads=G * Hkv, num_kv_heads=Hkv,
+                        head_dim=128, block_size=B)
+    base = W.fp8_scale_from(wl.k_cache, wl.v_cache, wl.k_new, wl.v_new)
+    ks = np.array([base * (1.0 + 0.37 * h) for h in range(Hkv)], np.float32)
+    vs = np.array([base * (1.6 - 0.21 * h) for h in range(Hkv)], np.float32)
+    kb, vb = W.bits(wl.k_cache), W.bits(wl.v_cache)
+    NB, _, _, D = kb.shape
+    kc = np.zeros((NB, Hkv, B, D), np.uint8)
+    vc = np.zeros_like(kc)
+    oracle.cache_append_scaled(kb.transpose(0, 2, 1, 3).reshape(NB * B, Hkv, D),
+                               vb.transpose(0, 2, 1, 3).reshape(NB * B, Hkv, D),
+                               np.arange(NB * B, dtype=np.int32), kc, vc, B, ks, vs)
+    wl.k_cache = torch.from_numpy(kc).to(cuda_device)
+    wl.v_cache = torch.from_numpy(vc).to(cuda_device)
+    W.poison_prefill(wl)
+    api.device_errors(clear=True)
+    kc, vc = W.bits(wl.k_cache).copy(), W.bits(wl.v_cache).copy()
+    slots_ref = oracle.chunk_slot_mapping(wl.block_tables, wl.context_lens, wl.query_start, B)
+    oracle.cache_append_scaled(W.bits(wl.k_new), W.bits(wl.v_new), slots_ref, kc, vc, B, ks, vs)
+    ref = oracle.prefill_scaled(W.bits(wl.q), kc, vc, wl.block_tables, wl.context_lens, wl.query_start,
+                                Hkv, B, wl.softmax_scale, ks, vs)
+    bt, cl, qs = _dev(wl, cuda_device)
+    ks_d, vs_d = torch.from_numpy(ks).to(cuda_device), torch.from_numpy(vs).to(cuda_device)
+    g_out = Guarded(wl.q.shape, torch.bfloat16, cuda_device, fill=float("nan"))
+    slots = api.chunk_slot_mapping(bt, cl, qs, B)
+    api.cache_append_scaled(wl.k_new, wl.v_new, slots, wl.k_cache, wl.v_cache, ks_d, vs_d)
+    out = api.prefill_scaled(wl.q, wl.k_cache, wl.v_cache, bt, cl, qs, wl.max_query_len, ks_d, vs_d,
+                             wl.softmax_scale, out=g_out.tensor)
+    torch.cuda.synchronize()
+    g_out.check("prefill scaled out")
+    assert np.array_equal(slots.cpu().numpy(), slots_ref)
+    assert np.array_equal(W.bits(wl.k_cache), kc) and np.array_equal(W.bits(wl.v_cache), vc)
+    compare(out, ref, what=f"prefill per-head scales G{G} B{B}")
+    assert api.device_errors() == 0
+
+
 @pytest.mark.parametrize("G,Hkv,B", [(4, 2, 16), (1, 4, 32)])
 def test_prefill_e4m3_many_items(api, oracle, cuda_device, G, Hkv, B):
     """48 ragged sequences over several waves of blocks, E4M3 cache."""
