@@ -52,3 +52,18 @@ def test_failing_status_raises_with_the_library_message():
     with pytest.raises(api.PagedAttentionError, match="96"):
         api._check(st)
     api._check(0)  # PA_OK passes silently
+
+
+def test_prefill_and_chunk_allocation_refuse_host_tensors():
+    bt, cl = _host_tables()
+    qs = torch.zeros(5, dtype=torch.int32)
+    q = torch.zeros(4, 8, 128, dtype=torch.bfloat16)
+    kc = torch.zeros(8, 2, 16, 128, dtype=torch.uint8)
+    sc = torch.ones(2, dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        api.prefill_scaled(q, kc, kc, bt, cl, qs, 4, sc, sc)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        api.prefill(q, kc, kc, bt, cl, qs, 4, kv_scale=0.5)
+    pool = api.DeviceBlockPool.__new__(api.DeviceBlockPool)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        pool.allocate_chunk(bt, cl, qs, kc, kc)
